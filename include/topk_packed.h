@@ -1,0 +1,150 @@
+/*
+ * topk_packed.h -- C ABI of the packed-layout top-k + page transform (B300, sm_103a).
+ *
+ * The operation (page "[sglang] [AMD ROCm] GLM-5.x Prefill 성능을 66% 끌어올린
+ * Top-K 커널 최적화 분석", analysis of sglang PR #37889):
+ *   - Intro: in the packed DSA prefill layout many requests share one large
+ *     score buffer and every row starts at its own column offset;
+ *   - section 1 ("TopKPackedParams"): per row i a window length seq_lens[i], a
+ *     column offset row_starts[i] and a page-table row row_to_batch[i] (row i
+ *     itself when the map is absent); the page-table row starts at
+ *     page_table + table_row * stride, and a page transform maps a window index
+ *     through it using page_bits;
+ *   - section 2 ("Vectorized load alignment and masking"): 16-byte loads start
+ *     at a rounded-down address and the lanes before the window are masked so
+ *     they never win.  Here the masking is done in registers; the score buffer
+ *     is never written.
+ * Computed for every row i < num_rows (the page leaves the rule itself
+ * unstated; this is the library's specification):
+ *     n   = max(seq_lens[i], 0)
+ *     v_j = scores[i * row_stride + row_starts[i] + j],   0 <= j < n
+ *     S   = the min(k, n) indices j of largest v_j; between equal scores the
+ *           lower j is taken (-0.0 and +0.0 are equal)
+ *     out[i * k + t] = page_row[j_t >> page_bits] * page_size + (j_t & (page_size - 1))
+ *           for the t-th smallest j_t in S, and -1 for min(k, n) <= t < k,
+ *     with page_row = page_table + b * pt_stride, b = row_to_batch ? row_to_batch[i] : i,
+ *     page_bits = log2(page_size).
+ * The result is unique, so it is bit-exact whatever the algorithm.
+ */
+#ifndef TOPK_PACKED_H_
+#define TOPK_PACKED_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream).  NULL is the legacy default stream. */
+typedef struct CUstream_st* topk_stream_t;
+
+typedef enum {
+  TOPK_OK = 0,
+  TOPK_ERR_INVALID_ARG = 1, /* an argument breaks the contract below; nothing launched */
+  TOPK_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles; nothing launched */
+  TOPK_ERR_LAUNCH = 3,      /* the CUDA launch failed (the CUDA error is kept; see below) */
+  TOPK_ERR_DEVICE = 4       /* no usable sm_103a device, or a CUDA query failed */
+} topk_status_t;
+
+/* Largest k this build accepts. */
+#define TOPK_K_MAX 2048
+
+/*
+ * topk_packed -- the operation above, launched asynchronously on `stream`.
+ *
+ * Arguments (all pointers are DEVICE memory owned by the caller; the library
+ * neither frees nor retains them, and allocates nothing):
+ *   scores       float32 buffer, read-only, 4-byte aligned; element (i, c) at
+ *                scores[i * row_stride + c].
+ *   row_stride   elements between consecutive rows of `scores` (>= 0).
+ *   seq_lens     int32[num_rows]: window length of each row (negative = 0).
+ *   row_starts   int32[num_rows]: window column offset of each row.
+ *   row_to_batch int32[num_rows] page-table row of each row, or NULL (identity).
+ *   page_table   int32 page numbers; row b starts at page_table + b * pt_stride.
+ *   pt_stride    elements between page-table rows (>= 0; 0 lets every row share one).
+ *   page_size    slots per page, a power of two (page_bits = log2(page_size)).
+ *   k            entries per output row, 1 <= k <= TOPK_K_MAX.
+ *   out          int32[num_rows * k], row-major, written completely.
+ *   num_rows     number of query rows (>= 0; 0 returns TOPK_OK and launches nothing).
+ *   stream       stream to launch on.
+ * Preconditions the call cannot check without reading device memory (breaking
+ * one gives an unspecified result; reads stay inside the row's window rounded
+ * out to 16-byte boundaries, and inside page_row[0 .. ceil(n / page_size))):
+ *   0 <= row_starts[i] and row_starts[i] + n <= row_stride for rows read;
+ *   page_row covers ceil(n / page_size) pages; page * page_size + page_size - 1 < 2^31;
+ *   no NaN inside a window.
+ * Returns TOPK_OK once the work is queued.  The call never synchronizes and
+ * never reads device arrays on the host.  Errors:
+ *   TOPK_ERR_INVALID_ARG  num_rows < 0; k <= 0; page_size <= 0 or not a power of
+ *                         two; row_stride < 0 or pt_stride < 0; a required pointer
+ *                         NULL while num_rows > 0.
+ *   TOPK_ERR_UNSUPPORTED  k > TOPK_K_MAX; scores not 4-byte aligned; page_size > 2^30.
+ *   TOPK_ERR_DEVICE       the current device is not sm_103a or cannot be queried.
+ *   TOPK_ERR_LAUNCH       the kernel launch was rejected.
+ * Thread safety: safe to call from several host threads; calls on different
+ * streams may run concurrently (they share no device state).
+ */
+topk_status_t topk_packed(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                          const int32_t* row_starts, const int32_t* row_to_batch,
+                          const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                          int32_t k, int32_t* out, int32_t num_rows, topk_stream_t stream);
+
+/* Kernel families behind topk_packed_ex. */
+typedef enum {
+  TOPK_PATH_AUTO = 0,      /* what topk_packed uses */
+  TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
+  TOPK_PATH_STREAM = 2     /* persistent CTAs (or clusters): TMA ring + running threshold */
+} topk_path_t;
+
+/* Launch choices; zero fields mean "choose automatically". */
+typedef struct {
+  int32_t path;         /* topk_path_t */
+  int32_t cluster_size; /* STREAM: CTAs that share one row (1, 2, 4 or 8); 0 = auto */
+  int32_t max_ctas;     /* STREAM: upper bound on the persistent grid; 0 = auto */
+} topk_launch_config_t;
+
+/*
+ * topk_packed_ex -- topk_packed with explicit launch choices.  `config` may be
+ * NULL (same as topk_packed).  Every path computes the same, bit-identical
+ * result.  Extra error: TOPK_ERR_INVALID_ARG for an unknown path or a
+ * cluster_size other than 0, 1, 2, 4, 8.
+ */
+topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                             const int32_t* row_starts, const int32_t* row_to_batch,
+                             const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                             int32_t k, int32_t* out, int32_t num_rows,
+                             const topk_launch_config_t* config, topk_stream_t stream);
+
+/*
+ * topk_packed_plan -- the launch topk_packed_ex would make for these sizes,
+ * without launching: path, cluster size, grid (in CTAs) and threads per CTA.
+ * Any output pointer may be NULL.  Errors as topk_packed_ex (no pointer checks).
+ */
+topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
+                               const topk_launch_config_t* config, int32_t* path,
+                               int32_t* cluster_size, int32_t* grid_ctas,
+                               int32_t* threads_per_cta);
+
+/* Static description of a status code (never NULL). */
+const char* topk_status_string(topk_status_t status);
+
+/* The CUDA error code (cudaError_t as int) behind the last TOPK_ERR_LAUNCH or
+ * TOPK_ERR_DEVICE returned on the calling host thread, 0 if none. */
+int topk_last_cuda_error(void);
+
+/*
+ * Device-side diagnostics.  Every wait inside the kernels is bounded; a wait
+ * that runs out records a bit here instead of hanging (the kernel then
+ * finishes its control flow and the affected rows are unspecified):
+ *   bit 0: a wait for a TMA chunk of the score stream gave up.
+ * topk_packed_device_flags copies the flags of the current device into *flags
+ * (after the work queued on `stream` so far) and, when `reset` is non-zero,
+ * clears them.  It synchronizes `stream`.
+ */
+topk_status_t topk_packed_device_flags(uint32_t* flags, int32_t reset, topk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPK_PACKED_H_ */

@@ -1,0 +1,168 @@
+"""Pins of the CPU oracle (no GPU).
+
+The oracle (oracle/topk_oracle.c) is checked against things other than itself:
+  * hand-worked examples (tests/golden/page_transform_example.json);
+  * the closed-form rank of each element (oracle/brute_force.py), on >= 10^4
+    random tiny rows with heavy ties, signed zeros and infinities;
+  * special cases that reduce to a library routine (k >= L: the identity
+    selection; page_size 1 with an identity table: raw indices; numpy lexsort);
+  * the invariants of oracle/invariants.py on larger rows;
+  * planted mistakes: mutated copies of the oracle source must fail these pins.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import topk_packed_reference
+from oracle import brute_force
+from oracle.invariants import InvariantError, check_row
+from sparse_attention_top_packed_b300.workloads import random_problem
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_transform_example.json")
+
+
+def _f(x):
+    return float(x)
+
+
+def run_oracle(p, **kw):
+    return topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts, p.row_to_batch,
+                                 p.page_table, p.pt_stride, p.page_size, p.k, **kw)
+
+
+def test_golden_examples():
+    data = json.load(open(GOLDEN))
+    for ex in data["examples"]:
+        values = np.array([_f(v) for v in ex["values"]], dtype=np.float32)
+        for case in ex["cases"]:
+            k = case["k"]
+            got = topk_packed_reference(values, 0, [len(values)], [0], None,
+                                        np.array(ex["page_row"]), 0, ex["page_size"], k)
+            assert got[0].tolist() == case["expected"], (ex["name"], k)
+            # the same row placed at an unaligned offset inside a row of +inf
+            stride = len(values) + 11
+            buf = np.full(2 * stride, np.inf, dtype=np.float32)
+            buf[stride + 3: stride + 3 + len(values)] = values
+            got2 = topk_packed_reference(buf, stride, [0, len(values)], [0, 3], [0, 0],
+                                         np.array(ex["page_row"]), 0, ex["page_size"], k)
+            assert got2[1].tolist() == case["expected"], (ex["name"], k, "offset")
+            assert got2[0].tolist() == [-1] * k
+            # and the brute force agrees with the fixture too
+            assert brute_force.row_result(values.tolist(), ex["page_row"], ex["page_size"], k) \
+                == case["expected"]
+
+
+def _brute_rows(p):
+    return brute_force.packed_result(p.scores, p.row_stride, p.seq_lens, p.row_starts,
+                                     p.row_to_batch, p.page_table, p.pt_stride, p.page_size, p.k)
+
+
+@pytest.mark.parametrize("values", ["ties", "normal", "int", "equal", "bf16"])
+def test_oracle_matches_pure_python_rank(values):
+    rng = np.random.default_rng(1234 + len(values))
+    for trial in range(20):
+        k = int(rng.integers(1, 40))
+        p = random_problem(rng, rows=12, max_len=int(rng.integers(1, 48)), k=k,
+                           page_size=int(rng.choice([1, 2, 4, 16])), values=values,
+                           identity=bool(trial % 3 == 0))
+        assert run_oracle(p).tolist() == _brute_rows(p), (values, trial)
+
+
+def test_oracle_matches_rank_on_ten_thousand_tiny_rows():
+    """>= 10^4 rows, n <= 64, k <= n + 8, tie-heavy values including +-0 and +-inf."""
+    rng = np.random.default_rng(7)
+    rows_checked = 0
+    while rows_checked < 10240:
+        kind = ["ties", "int", "normal", "bf16"][rows_checked // 256 % 4]
+        max_len = int(rng.integers(1, 65))
+        k = int(rng.integers(1, max_len + 9))
+        p = random_problem(rng, rows=64, max_len=max_len, k=k,
+                           page_size=int(rng.choice([1, 4, 64])), values=kind)
+        got = run_oracle(p)
+        for i in range(p.num_rows):
+            L = int(p.seq_lens[i])
+            base = i * p.row_stride + int(p.row_starts[i])
+            chosen = brute_force.select_by_rank_np(p.scores[base: base + L], k)
+            b = int(p.row_to_batch[i])
+            page_row = p.page_table[b * p.pt_stride:(b + 1) * p.pt_stride]
+            expect = [brute_force.page_slot(page_row, p.page_size, int(j)) for j in chosen]
+            expect += [-1] * (k - len(expect))
+            assert got[i].tolist() == expect, (kind, rows_checked + i)
+        rows_checked += p.num_rows
+
+
+def test_k_at_least_window_is_identity_selection():
+    rng = np.random.default_rng(3)
+    p = random_problem(rng, rows=30, max_len=200, k=256, page_size=16, values="normal")
+    got = run_oracle(p)
+    for i in range(p.num_rows):
+        L = int(p.seq_lens[i])
+        b = int(p.row_to_batch[i])
+        j = np.arange(L)
+        pages = p.page_table[b * p.pt_stride + (j // 16)]
+        expect = np.concatenate([pages.astype(np.int64) * 16 + j % 16, -np.ones(256 - L)])
+        assert np.array_equal(got[i], expect.astype(np.int32))
+
+
+def test_unit_pages_identity_table_gives_raw_indices_and_matches_lexsort():
+    rng = np.random.default_rng(5)
+    rows, L, k = 40, 500, 37
+    p = random_problem(rng, rows=rows, max_len=L, k=k, page_size=1, values="bf16",
+                       forced_lens=[L] * rows)
+    table = np.tile(np.arange(p.pt_stride, dtype=np.int32), rows)
+    got = topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts,
+                                np.arange(rows), table, p.pt_stride, 1, k)
+    for i in range(rows):
+        base = i * p.row_stride + int(p.row_starts[i])
+        w = p.scores[base: base + L].astype(np.float64)
+        order = np.lexsort((np.arange(L), -w))  # primary: -w ascending, then index
+        assert got[i].tolist() == sorted(order[:k].tolist())
+
+
+def test_invariants_hold_on_larger_rows():
+    rng = np.random.default_rng(11)
+    for values in ["normal", "bf16", "int", "ties"]:
+        p = random_problem(rng, rows=16, max_len=5000, k=300, page_size=64, values=values)
+        got = run_oracle(p)
+        for i in range(p.num_rows):
+            L = int(p.seq_lens[i])
+            base = i * p.row_stride + int(p.row_starts[i])
+            b = int(p.row_to_batch[i])
+            check_row(p.scores[base: base + L], p.page_table[b * p.pt_stride:(b + 1) * p.pt_stride],
+                      p.page_size, p.k, got[i])
+
+
+def test_invariant_checker_catches_planted_errors():
+    v = np.array([0.5, 2.0, -1.0, 2.0, 0.5, 3.0], dtype=np.float32)
+    pages = [7, 2]
+    check_row(v, pages, 4, 4, [28, 29, 31, 9])
+    bad = {
+        "tie to higher index": [29, 31, 8, 9],
+        "not ascending": [29, 28, 31, 9],
+        "foreign page": [28, 29, 31, 41],
+        "too few": [28, 29, 31, -1],
+        "lower score chosen": [28, 29, 30, 9],
+    }
+    for name, out in bad.items():
+        with pytest.raises(InvariantError):
+            check_row(v, pages, 4, 4, out)
+            pytest.fail(name)
+
+
+def test_oracle_rejects_bad_arguments():
+    for kw in [dict(k=0), dict(page_size=3), dict(page_size=0)]:
+        args = dict(k=2, page_size=4)
+        args.update(kw)
+        with pytest.raises(ValueError):
+            topk_packed_reference(np.zeros(4, np.float32), 4, [4], [0], None, np.zeros(4),
+                                  0, args["page_size"], args["k"])
+
+
+def test_oracle_thread_count_does_not_change_result():
+    rng = np.random.default_rng(9)
+    p = random_problem(rng, rows=50, max_len=3000, k=100, page_size=64, values="bf16")
+    a = run_oracle(p, nthreads=1)
+    b = run_oracle(p, nthreads=7)
+    assert np.array_equal(a, b)
