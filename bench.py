@@ -1,0 +1,425 @@
+"""Benchmark of the packed top-k + page transform.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload prefill|long|mixed|decode|tiny]
+
+One step = one call of topk_packed over the whole workload (every row of the
+batch: window load, selection, ordered emission, page transform, padding).
+Default workload: the prefill chunk at ISL 70000 -- 2 requests x 70000 KV
+tokens side by side (row stride 140000), the last 2048 query tokens of each
+(4096 rows, windows 67953..70000 floats), k = 2048, page size 64.
+
+Prints one JSON line.  `value` is rows/s with inputs resident in HBM (CUDA
+events on the launching stream, max over ranks); `e2e` is the same metric
+through the public API with pinned host buffers and the host<->device copies
+in the timed region; `roofline` relates the kernel's algorithmic bytes (window
+bytes read for rows with seq_len > k, plus 4*k bytes written per row) to the
+measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle on a bounded
+sample of rows.  Under torchrun every rank runs the same workload on its own
+GPU (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+WORKLOAD_TEXT = {
+    "prefill": "prefill chunk ISL 70000: 4096 rows (2 requests x 2048 causal queries), "
+               "row stride 140000 fp32, windows 67953..70000, k=2048, page 64",
+    "long": "long context: 2048 rows, row stride 327680 fp32, windows 325633..327680, k=2048, page 64",
+    "mixed": "mixed batch with ties: 16 requests (KV 1K..64K) side by side, 8192 causal rows, "
+             "bf16-rounded scores, k=2048, page 64",
+    "decode": "decode-like: 64 rows x 8192 fp32, k=2048, page 64",
+    "tiny": "tiny: 8 rows, windows 1..300 at unaligned offsets, k=32, page 64",
+}
+L2_BYTES = 126 * 1024 * 1024
+
+
+def log(msg: str) -> None:
+    print(msg, file=sys.stderr, flush=True)
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured", "sm_max_mhz": d.get("sm_max_mhz")}
+    return {"hbm_gbs": 6400.0, "source": "fallback", "sm_max_mhz": 2032.0}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_top_packed_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(workload)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, line in self.lines:
+            if self.t0 is None or not (self.t0 - 0.15 <= t <= self.t1 + 0.15):
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_workload(name: str, device):
+    from sparse_attention_top_packed_b300 import workloads
+
+    return workloads.named(name, device=device)
+
+
+def l2_flush_buffer(device):
+    return torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+
+
+def prepare_timing(w, steps: int, warmup: int, flush: bool, device):
+    """Arguments of the timed call, after `warmup` untimed calls, and the events."""
+    from sparse_attention_top_packed_b300 import binding
+
+    out = torch.empty((w.num_rows, w.k), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    scratch = l2_flush_buffer(device) if flush else None
+    args = (w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch, w.page_table,
+            w.pt_stride, w.page_size, w.k, out, w.num_rows)
+    for _ in range(warmup):
+        if flush:
+            scratch.fill_(1.0)
+        binding.topk_packed(*args, stream=stream)
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    return args, stream, scratch, starts, ends
+
+
+def run_ours(a, rank: int, world: int, device) -> dict:
+    from sparse_attention_top_packed_b300 import binding
+
+    torch.cuda.set_device(device)
+    w = make_workload(a.workload, device)
+    torch.cuda.synchronize(device)
+    alg_bytes = w.algorithmic_bytes()
+    big = w.window_bytes() > 4 * L2_BYTES
+    flush = not big
+    args, stream, scratch, starts, ends = prepare_timing(w, a.steps, a.warmup, flush, device)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(1.0)  # nvidia-smi needs a moment before its first sample
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark_begin()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(a.steps):
+        if flush:
+            scratch.fill_(1.0)
+        starts[i].record(stream)
+        binding.topk_packed(*args, stream=stream)
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    if sampler:
+        sampler.mark_end()
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(launch_ms) / len(launch_ms)
+    step_ms = kernel_ms if flush else t_begin.elapsed_time(t_end) / a.steps
+    clocks = sampler.stop() if sampler else None
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([step_ms, kernel_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, kernel_ms = float(t[0]), float(t[1])
+
+    # parity spot check of the timed output against the oracle (first rows)
+    out = args[9]
+    e2e = run_e2e(a, w, device) if rank == 0 else None
+    result = {
+        "step_ms": step_ms, "kernel_ms": kernel_ms, "alg_bytes": alg_bytes, "flush": flush,
+        "clocks": clocks, "e2e": e2e, "workload": w, "out": out,
+    }
+    return result
+
+
+def run_e2e(a, w, device) -> dict:
+    """Same metric through the public API with pinned host buffers: each step
+    copies the step's inputs host->device, runs topk_packed, copies the result
+    back.  Timed with CUDA events on the stream doing all three."""
+    from sparse_attention_top_packed_b300 import binding
+
+    steps = max(1, min(a.steps, a.e2e_steps))
+    host = {}
+    for name in ("scores", "seq_lens", "row_starts", "row_to_batch", "page_table"):
+        t = getattr(w, name)
+        if t is not None:
+            host[name] = t.cpu().pin_memory()
+    dev = {n: torch.empty_like(t, device=device) for n, t in host.items()}
+    out_dev = torch.empty((w.num_rows, w.k), dtype=torch.int32, device=device)
+    out_host = torch.empty((w.num_rows, w.k), dtype=torch.int32).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * 4
+
+    def step():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        binding.topk_packed(dev["scores"], w.row_stride, dev["seq_lens"], dev["row_starts"],
+                            dev.get("row_to_batch"), dev["page_table"], w.pt_stride, w.page_size,
+                            w.k, out_dev, w.num_rows, stream=stream)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(device)
+    b = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    b.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(device)
+    ms = b.elapsed_time(e) / steps
+    return {"value": w.num_rows / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
+
+
+def cpu_baseline(w, target_s: float = 12.0, max_rows: int = 4096) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of the workload's rows
+    (windows copied to the host first, outside the timing), all host cores."""
+    from oracle import default_threads, topk_packed_reference
+    from sparse_attention_top_packed_b300.workloads import gather_windows, sample_rows
+
+    cores = default_threads()
+
+    def run_rows(n):
+        rows = sample_rows(w.num_rows, n, seed=1)
+        win, L = gather_windows(w, rows)
+        b = (rows.numpy() if w.row_to_batch is None
+             else w.row_to_batch[rows.to(w.row_to_batch.device)].cpu().numpy()).astype(np.int32)
+        table = w.page_table.reshape(-1).cpu().numpy()
+        t0 = time.perf_counter()
+        topk_packed_reference(win.reshape(-1), win.shape[1], L, np.zeros(len(L), np.int32), b, table,
+                              w.pt_stride, w.page_size, w.k, nthreads=cores)
+        return time.perf_counter() - t0, int(rows.numel())
+
+    n = max(cores, 8)
+    dt, n = run_rows(n)
+    if dt < target_s / 4 and n < w.num_rows:
+        n2 = int(min(w.num_rows, max_rows, n * max(1.0, target_s / max(dt, 1e-3))))
+        if n2 > n:
+            dt, n = run_rows(n2)
+    return {"value": n / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.num_rows} rows (first, last and evenly spread), "
+                      f"{dt:.2f} s on {cores} threads; windows copied to the host beforehand"}
+
+
+def run_reference(a, rank: int, world: int) -> None:
+    """The reference arm: the CPU oracle, timed as it stands on the host cores,
+    on the same workload and metric.  Each step is a bounded sample of rows."""
+    if rank != 0:
+        return
+    from oracle import default_threads, topk_packed_reference
+    from sparse_attention_top_packed_b300.workloads import gather_windows, sample_rows
+
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    w = make_workload(a.workload, device)
+    cores = default_threads()
+    rows_per_step = max(1, min(w.num_rows, cores))
+    steps = []
+    total = a.warmup + a.steps
+    batches = []
+    for s in range(total):
+        rows = sample_rows(w.num_rows, rows_per_step, seed=100 + s)
+        win, L = gather_windows(w, rows)
+        b = (rows.numpy() if w.row_to_batch is None
+             else w.row_to_batch[rows.to(w.row_to_batch.device)].cpu().numpy()).astype(np.int32)
+        batches.append((win, L, b))
+        if len(batches) >= 8:
+            break
+    table = w.page_table.reshape(-1).cpu().numpy()
+    for s in range(total):
+        win, L, b = batches[s % len(batches)]
+        t0 = time.perf_counter()
+        topk_packed_reference(win.reshape(-1), win.shape[1], L, np.zeros(len(L), np.int32), b, table,
+                              w.pt_stride, w.page_size, w.k, nthreads=cores)
+        if s >= a.warmup:
+            steps.append(time.perf_counter() - t0)
+    sec = sum(steps) / len(steps)
+    value = rows_per_step / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(a, w, None),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows per step of {w.num_rows}"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "packed top-k rows/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
+
+
+def config_block(a, w, plan) -> dict:
+    d = {"workload": WORKLOAD_TEXT[a.workload], "rows": w.num_rows, "row_stride": w.row_stride,
+         "k": w.k, "page_size": w.page_size,
+         "window_bytes_per_step": w.window_bytes(), "output_bytes_per_step": w.output_bytes(),
+         "l2": ("inputs larger than L2: each step reads %.2f GB, no flush" % (w.window_bytes() / 1e9))
+         if w.window_bytes() > 4 * L2_BYTES else "L2 flushed (252 MB write) before every timed launch",
+         "parallelism": f"dp{a.gpus} (independent replicas of the batch)"}
+    if plan is not None:
+        d["launch"] = plan
+    return d
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        a.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+        return
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+
+    from sparse_attention_top_packed_b300 import binding
+
+    r = run_ours(a, rank, world, device)
+    w = r["workload"]
+    if rank == 0:
+        peaks = measured_peaks()
+        plan = binding.topk_packed_plan(w.row_stride, w.k, w.num_rows)
+        achieved = r["alg_bytes"] / (r["kernel_ms"] / 1e3) / 1e9
+        value = world * w.num_rows / (r["step_ms"] / 1e3)
+        traffic = profiled_traffic(a.workload)
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": r["step_ms"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) scores, distinct random pages)",
+            "config": config_block(a, w, plan),
+            "achieved_hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peaks["source"] == "measured" else "fallback 6.4 TB/s",
+                         "algorithmic_bytes_per_launch": r["alg_bytes"],
+                         "kernel": "topk_stream_kernel" if plan["path"] == 2 else "topk_multipass_kernel"},
+            "gpu_launches": a.steps,
+            "clocks": r["clocks"],
+            "e2e": r["e2e"],
+        }
+        if world == 1 and not a.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -31,6 +31,12 @@
 
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define TOPK_API __attribute__((visibility("default")))
+#else
+#define TOPK_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -84,7 +90,7 @@ typedef enum {
  * Thread safety: safe to call from several host threads; calls on different
  * streams may run concurrently (they share no device state).
  */
-topk_status_t topk_packed(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                           const int32_t* row_starts, const int32_t* row_to_batch,
                           const int32_t* page_table, int64_t pt_stride, int32_t page_size,
                           int32_t k, int32_t* out, int32_t num_rows, topk_stream_t stream);
@@ -109,7 +115,7 @@ typedef struct {
  * result.  Extra error: TOPK_ERR_INVALID_ARG for an unknown path or a
  * cluster_size other than 0, 1, 2, 4, 8.
  */
-topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+TOPK_API topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                              const int32_t* row_starts, const int32_t* row_to_batch,
                              const int32_t* page_table, int64_t pt_stride, int32_t page_size,
                              int32_t k, int32_t* out, int32_t num_rows,
@@ -120,17 +126,17 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
  * without launching: path, cluster size, grid (in CTAs) and threads per CTA.
  * Any output pointer may be NULL.  Errors as topk_packed_ex (no pointer checks).
  */
-topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
+TOPK_API topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
                                const topk_launch_config_t* config, int32_t* path,
                                int32_t* cluster_size, int32_t* grid_ctas,
                                int32_t* threads_per_cta);
 
 /* Static description of a status code (never NULL). */
-const char* topk_status_string(topk_status_t status);
+TOPK_API const char* topk_status_string(topk_status_t status);
 
 /* The CUDA error code (cudaError_t as int) behind the last TOPK_ERR_LAUNCH or
  * TOPK_ERR_DEVICE returned on the calling host thread, 0 if none. */
-int topk_last_cuda_error(void);
+TOPK_API int topk_last_cuda_error(void);
 
 /*
  * Device-side diagnostics.  Every wait inside the kernels is bounded; a wait
@@ -141,7 +147,7 @@ int topk_last_cuda_error(void);
  * (after the work queued on `stream` so far) and, when `reset` is non-zero,
  * clears them.  It synchronizes `stream`.
  */
-topk_status_t topk_packed_device_flags(uint32_t* flags, int32_t reset, topk_stream_t stream);
+TOPK_API topk_status_t topk_packed_device_flags(uint32_t* flags, int32_t reset, topk_stream_t stream);
 
 #ifdef __cplusplus
 }

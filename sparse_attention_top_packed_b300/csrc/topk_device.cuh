@@ -1,0 +1,624 @@
+// Device building blocks of the packed top-k + page transform (sm_103a).
+//
+// Operation (page "[sglang] [AMD ROCm] GLM-5.x Prefill 성능을 66% 끌어올린 Top-K 커널
+// 최적화 분석", sglang PR #37889): row i reads the window
+//   scores[i * row_stride + row_starts[i] + j], 0 <= j < seq_lens[i]
+// (Intro: packed layout; section 1: TopKPackedParams), selects the k largest
+// (ties to the lower j), and writes the chosen j in ascending order through the
+// page transform of section 1 (get_transform: table row = row_to_batch[i] or i),
+// padding with -1.
+//
+// Selection is an exact radix select on 32-bit order-preserving keys, in three
+// digit levels: bits [20,32) (4096 bins), [10,20) and [0,10) (1024 bins each).
+// After each level the block knows the key prefix T of the k-th largest element
+// under mask M, how many elements lie strictly above it (gt) and how many of the
+// prefix-equal elements are still to be taken (r).  A level stops the descent
+// early when every prefix-equal element is taken.  The emission then keeps, in
+// ascending j, every element with (key & M) > T and the first r with
+// (key & M) == T -- the tie rule.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace topk {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+
+constexpr int kBins1 = 4096;  // level 1: key bits [20, 32)
+constexpr int kShift1 = 20;
+constexpr int kBins23 = 1024;  // levels 2 and 3: bits [10, 20) and [0, 10)
+constexpr int kShift2 = 10;
+constexpr int kShift3 = 0;
+
+// Device-side diagnostic bits (see topk_packed_device_flags).
+constexpr uint32_t kFlagStreamWaitTimeout = 1u;
+constexpr uint32_t kFlagBadOutputPosition = 2u;
+
+// The diagnostic word (the library is one translation unit).
+__device__ uint32_t g_device_flags;
+
+struct Params {
+  const float* scores;
+  int64_t row_stride;
+  const int32_t* seq_lens;
+  const int32_t* row_starts;
+  const int32_t* row_to_batch;  // may be null: identity
+  const int32_t* page_table;
+  int64_t pt_stride;
+  int32_t page_bits;
+  int32_t k;
+  int32_t* out;
+  int32_t num_rows;
+};
+
+// ---------------------------------------------------------------------------
+// Keys.  key(x) orders like x for every non-NaN float; -0.0 is first turned
+// into +0.0 so the two tie (IEEE compares them equal).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t key_of(float x) {
+  uint32_t u = __float_as_uint(x);
+  u = (u == 0x80000000u) ? 0u : u;
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
+// The float whose key is the lower edge of level-1 bin b, so that for every
+// non-NaN x:  x >= edge_float(b)  <=>  key(x) >= (b << 20).  Bin 0 starts at
+// key 0, below every non-NaN key: its edge is -inf.
+__device__ __forceinline__ float edge_float(uint32_t b) {
+  const uint32_t key = b << kShift1;
+  if (b == 0) return __uint_as_float(0xFF800000u);
+  const uint32_t u = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
+  return __uint_as_float(u);
+}
+
+// ---------------------------------------------------------------------------
+// Row addressing (section 1 and section 2 of the page).  The window start is
+// rounded down to a 16-byte boundary of its ABSOLUTE address, so the rounding
+// is right for any row_stride; `head` lanes before the window and the lanes
+// past its end are masked in registers.  The buffer is never written.
+// ---------------------------------------------------------------------------
+struct Row {
+  int32_t L;                // window length, clamped at 0
+  const float4* base4;      // 16-byte aligned, at or before the window start
+  int32_t head;             // window index 0 is element `head` of base4[0]
+  const int32_t* page_row;  // page_table + table_row * pt_stride
+};
+
+__device__ __forceinline__ Row load_row(const Params& p, int32_t row) {
+  Row r;
+  const int32_t L = __ldg(p.seq_lens + row);
+  r.L = L > 0 ? L : 0;
+  const float* w = p.scores + (int64_t)row * p.row_stride + __ldg(p.row_starts + row);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(w);
+  r.head = (int32_t)((a & 15u) >> 2);
+  r.base4 = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
+  const int64_t table_row = p.row_to_batch ? (int64_t)__ldg(p.row_to_batch + row) : (int64_t)row;
+  r.page_row = p.page_table + table_row * p.pt_stride;
+  return r;
+}
+
+// The part of a row one CTA of a cluster owns: quads [q0, q1) of base4, window
+// indices [lo, hi).  Parts are contiguous and in rank order.
+struct Part {
+  int64_t q0, q1;
+  int32_t lo, hi;
+};
+
+__device__ __forceinline__ Part part_of(const Row& r, uint32_t rank, uint32_t parts) {
+  const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
+  const int64_t per = (nq + parts - 1) / parts;
+  Part s;
+  s.q0 = min((int64_t)rank * per, nq);
+  s.q1 = min(s.q0 + per, nq);
+  const int64_t lo = s.q0 * 4 - r.head, hi = s.q1 * 4 - r.head;
+  s.lo = (int32_t)max(lo, (int64_t)0);
+  s.hi = (int32_t)min(hi, (int64_t)r.L);
+  if (s.hi < s.lo) s.hi = s.lo;
+  return s;
+}
+
+// Section 1's transform: page from the high bits of j, offset from the low bits.
+__device__ __forceinline__ int32_t page_slot(const int32_t* page_row, int32_t page_bits, int32_t j) {
+  return __ldg(page_row + (j >> page_bits)) * (1 << page_bits) + (j & ((1 << page_bits) - 1));
+}
+
+// A window no longer than k: every index is taken; slots past L are -1.
+__device__ __forceinline__ void emit_whole_window(const Params& p, int32_t row, const Row& r,
+                                                  uint32_t part, uint32_t parts) {
+  int32_t* o = p.out + (int64_t)row * p.k;
+  for (int32_t t = (int32_t)(part * kThreads + threadIdx.x); t < p.k; t += (int32_t)(parts * kThreads))
+    o[t] = t < r.L ? page_slot(r.page_row, p.page_bits, t) : -1;
+}
+
+// ---------------------------------------------------------------------------
+// PTX helpers: cluster, distributed shared memory, mbarrier, bulk copy.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory word in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+               ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase with the given parity to complete, for at most ~2 s.
+// Returns false when it gave up (the caller records a diagnostic bit).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > 2000000000ull) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// ---------------------------------------------------------------------------
+// Block-wide scans.  Counts travel packed: low 16 bits / high 16 bits, each
+// at most 2048 per call, so the fields never carry into each other.
+// `scratch` holds kWarps words; callers alternate two buffers between calls
+// (every call contains one __syncthreads, which makes two enough).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_incl_suffix(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_down_sync(0xFFFFFFFFu, v, o);
+    if (lane + o < 32) v += n;
+  }
+  return v;
+}
+
+// Exclusive prefix of v over threads in index order; `total` gets the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan(v);
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  const uint32_t wt = lane < kWarps ? scratch[lane] : 0u;
+  const uint32_t wincl = warp_incl_scan(wt);
+  const uint32_t wexcl = __shfl_sync(0xFFFFFFFFu, wincl - wt, warp);
+  total = __shfl_sync(0xFFFFFFFFu, wincl, kWarps - 1);
+  return wexcl + incl - v;
+}
+
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* scratch) {
+  uint32_t total;
+  block_excl_scan(v, scratch, total);
+  return total;
+}
+
+// ---------------------------------------------------------------------------
+// Bucket pick: the largest bin b with sum(hist[b..]) >= r, where hist is this
+// CTA's histogram, or (CLUSTER > 1) the sum of the histograms at the same
+// shared-memory offset in every CTA of the cluster.  Returns, to every thread,
+// the bin, `above` = sum(hist[b+1..]) and `count` = hist[b].  The caller
+// guarantees sum(hist) >= r >= 1.
+// ---------------------------------------------------------------------------
+struct Pick {
+  uint32_t bin, above, count;
+};
+
+template <int NBINS, int CLUSTER>
+__device__ __forceinline__ Pick block_pick(const uint32_t* hist, uint32_t r, uint32_t* scratch,
+                                           Pick* slot) {
+  constexpr int B = NBINS / kThreads;  // bins per thread: 8 or 2
+  static_assert(B == 8 || B == 2, "bins per thread");
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t h[B];
+  if constexpr (CLUSTER == 1) {
+#pragma unroll
+    for (int i = 0; i < B; ++i) h[i] = hist[t * B + i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < B; ++i) h[i] = 0;
+    const uint32_t local = smem_addr(hist + t * B);
+#pragma unroll
+    for (int c = 0; c < CLUSTER; ++c) {
+      const uint32_t a = peer_addr(local, (uint32_t)c);
+      if constexpr (B == 8) {
+        const uint4 v0 = ld_cluster_v4(a), v1 = ld_cluster_v4(a + 16u);
+        h[0] += v0.x; h[1] += v0.y; h[2] += v0.z; h[3] += v0.w;
+        h[4] += v1.x; h[5] += v1.y; h[6] += v1.z; h[7] += v1.w;
+      } else {
+        h[0] += ld_cluster_u32(a);
+        h[1] += ld_cluster_u32(a + 4u);
+      }
+    }
+  }
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < B; ++i) s += h[i];
+  // suffix over threads: sum of s over threads > t
+  const uint32_t incl = warp_incl_suffix(s);
+  if (lane == 0) scratch[warp] = incl;
+  if (t == 0) *slot = Pick{0u, 0u, 0u};
+  __syncthreads();
+  const uint32_t wt = lane < kWarps ? scratch[lane] : 0u;
+  const uint32_t wsuf = warp_incl_suffix(wt);
+  const uint32_t above_warps = __shfl_sync(0xFFFFFFFFu, wsuf - wt, warp);
+  uint32_t run = above_warps + incl - s;  // sum over bins above this thread's bins
+#pragma unroll
+  for (int i = B - 1; i >= 0; --i) {
+    const uint32_t prev = run;
+    run += h[i];
+    if (prev < r && run >= r) *slot = Pick{(uint32_t)(t * B + i), prev, h[i]};
+  }
+  __syncthreads();
+  return *slot;
+}
+
+// Sum of this CTA's own hist[b] for b > bin (only needed with clusters).
+template <int NBINS>
+__device__ __forceinline__ uint32_t own_above(const uint32_t* hist, uint32_t bin, uint32_t* scratch) {
+  constexpr int B = NBINS / kThreads;
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < B; ++i) {
+    const uint32_t b = threadIdx.x * B + i;
+    if (b > bin) s += hist[b];
+  }
+  return block_sum(s, scratch);
+}
+
+// ---------------------------------------------------------------------------
+// Sources of (key, j) pairs for the refinement levels and the emission:
+//   GlobalSrc -- a row part read straight from global memory (16-byte loads,
+//                masked lanes), used by the multipass kernel and as the
+//                streaming kernel's fallback;
+//   CandSrc   -- the streaming kernel's candidate list in shared memory, kept
+//                in ascending j.
+// Both walk "tiles" of kThreads*4 items in ascending j, 4 per thread, for the
+// ordered emission.
+// ---------------------------------------------------------------------------
+struct GlobalSrc {
+  const float4* base4;
+  int64_t q0, q1;
+  int32_t head, lo, hi;
+
+  // hist[(key >> shift) & (nbins-1)] += 1 for every element whose key matches
+  // prefix T under mask M.
+  __device__ __forceinline__ void histogram(uint32_t* hist, uint32_t M, uint32_t T, int shift,
+                                            uint32_t nbins_mask) const {
+    constexpr int U = 4;
+    for (int64_t q = q0 + threadIdx.x; q < q1; q += (int64_t)kThreads * U) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t qq = q + (int64_t)u * kThreads;
+        if (qq < q1) v[u] = __ldg(base4 + qq);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t qq = q + (int64_t)u * kThreads;
+        if (qq < q1) {
+          const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          const int64_t j0 = qq * 4 - head;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t j = j0 + e;
+            const uint32_t key = key_of(x[e]);
+            if (j >= lo && j < hi && (key & M) == T) atomicAdd(hist + ((key >> shift) & nbins_mask), 1u);
+          }
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ int64_t tiles() const { return (q1 - q0 + kThreads - 1) / kThreads; }
+
+  __device__ __forceinline__ void tile(int64_t t, uint32_t key[4], int32_t j[4], bool valid[4]) const {
+    const int64_t q = q0 + t * kThreads + threadIdx.x;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (q < q1) v = __ldg(base4 + q);
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t jj = q * 4 - head + e;
+      valid[e] = q < q1 && jj >= lo && jj < hi;
+      j[e] = (int32_t)jj;
+      key[e] = key_of(x[e]);
+    }
+  }
+};
+
+struct CandSrc {
+  const uint32_t* keys;
+  const int32_t* js;
+  int32_t count;
+
+  __device__ __forceinline__ void histogram(uint32_t* hist, uint32_t M, uint32_t T, int shift,
+                                            uint32_t nbins_mask) const {
+    for (int32_t i = threadIdx.x; i < count; i += kThreads) {
+      const uint32_t key = keys[i];
+      if ((key & M) == T) atomicAdd(hist + ((key >> shift) & nbins_mask), 1u);
+    }
+  }
+
+  __device__ __forceinline__ int64_t tiles() const { return (count + kThreads * 4 - 1) / (kThreads * 4); }
+
+  __device__ __forceinline__ void tile(int64_t t, uint32_t key[4], int32_t j[4], bool valid[4]) const {
+    const int32_t e0 = (int32_t)t * kThreads * 4 + threadIdx.x * 4;
+    if (e0 + 3 < count) {
+      const uint4 k4 = *reinterpret_cast<const uint4*>(keys + e0);
+      const int4 j4 = *reinterpret_cast<const int4*>(js + e0);
+      key[0] = k4.x; key[1] = k4.y; key[2] = k4.z; key[3] = k4.w;
+      j[0] = j4.x; j[1] = j4.y; j[2] = j4.z; j[3] = j4.w;
+      valid[0] = valid[1] = valid[2] = valid[3] = true;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        valid[e] = e0 + e < count;
+        key[e] = valid[e] ? keys[e0 + e] : 0u;
+        j[e] = valid[e] ? js[e0 + e] : 0;
+      }
+    }
+  }
+};
+
+// Per-CTA shared state of the selection.  Everything a peer CTA reads through
+// distributed shared memory sits at the same offset in every CTA.
+struct SelectShared {
+  uint32_t hist1[kBins1];
+  uint32_t hist2[kBins23];
+  uint32_t hist3[kBins23];
+  uint32_t scratch[2][kWarps];
+  Pick pick[2];
+  uint32_t pub_gt;        // published: this CTA's count of elements above the prefix
+  uint32_t pub_eq;        // published: this CTA's count of prefix-equal elements
+  uint32_t pub_overflow;  // published: candidate list overflowed (streaming only)
+  uint32_t pad_;
+};
+
+// Outcome of the selection, identical in every thread of a CTA.
+struct Selection {
+  uint32_t M, T;   // prefix mask and value of the k-th largest key
+  uint32_t quota;  // prefix-equal elements this CTA takes (its first `quota` of them)
+  uint32_t off;    // where this CTA's first output goes inside the row
+};
+
+// Alternating scratch buffers for the block scans and alternating result
+// slots for the bucket picks (two independent counters, so the order in which
+// a call's arguments are evaluated does not matter).
+struct ScanParity {
+  uint32_t p = 0, q = 0;
+  __device__ __forceinline__ uint32_t* next(SelectShared& S) {
+    uint32_t* s = S.scratch[p];
+    p ^= 1u;
+    return s;
+  }
+  __device__ __forceinline__ Pick* next_pick(SelectShared& S) {
+    Pick* s = &S.pick[q];
+    q ^= 1u;
+    return s;
+  }
+};
+
+// Levels 1..3 of the radix select for one row.  On entry hist1 holds, for
+// every bin at or above the row's threshold bin in every CTA of the cluster,
+// the exact number of the CTA's elements in that bin, and a barrier (cluster
+// barrier with clusters) separates its last update from this call.  `k_row`
+// is the number to select (k; the row has more than k elements).
+template <int CLUSTER, class Src>
+__device__ __forceinline__ Selection select_levels(SelectShared& S, const Src& src, uint32_t k_row,
+                                                   ScanParity& par) {
+  Pick pk = block_pick<kBins1, CLUSTER>(S.hist1, k_row, par.next(S), par.next_pick(S));
+  uint32_t r = k_row - pk.above;
+  uint32_t M = 0xFFF00000u, T = pk.bin << kShift1;
+  uint32_t gt = 0, eq = 0;
+  if constexpr (CLUSTER > 1) {
+    gt = own_above<kBins1>(S.hist1, pk.bin, par.next(S));
+    eq = S.hist1[pk.bin];
+  }
+  if (pk.count != r) {
+    // level 2: bits [10, 20) of the keys in bucket T
+    for (int b = threadIdx.x; b < kBins23; b += kThreads) S.hist2[b] = 0u;
+    __syncthreads();
+    src.histogram(S.hist2, M, T, kShift2, kBins23 - 1);
+    __syncthreads();
+    if constexpr (CLUSTER > 1) cluster_sync_all();
+    pk = block_pick<kBins23, CLUSTER>(S.hist2, r, par.next(S), par.next_pick(S));
+    r -= pk.above;
+    M |= 0x000FFC00u;
+    T |= pk.bin << kShift2;
+    if constexpr (CLUSTER > 1) {
+      gt += own_above<kBins23>(S.hist2, pk.bin, par.next(S));
+      eq = S.hist2[pk.bin];
+    }
+    if (pk.count != r) {
+      // level 3: bits [0, 10)
+      for (int b = threadIdx.x; b < kBins23; b += kThreads) S.hist3[b] = 0u;
+      __syncthreads();
+      src.histogram(S.hist3, M, T, kShift3, kBins23 - 1);
+      __syncthreads();
+      if constexpr (CLUSTER > 1) cluster_sync_all();
+      pk = block_pick<kBins23, CLUSTER>(S.hist3, r, par.next(S), par.next_pick(S));
+      r -= pk.above;
+      M = 0xFFFFFFFFu;
+      T |= pk.bin;
+      if constexpr (CLUSTER > 1) {
+        gt += own_above<kBins23>(S.hist3, pk.bin, par.next(S));
+        eq = S.hist3[pk.bin];
+      }
+    }
+  }
+  Selection sel;
+  sel.M = M;
+  sel.T = T;
+  if constexpr (CLUSTER == 1) {
+    sel.quota = r;
+    sel.off = 0;
+  } else {
+    // Tie quota in rank (= window index) order, and each CTA's output offset.
+    if (threadIdx.x == 0) {
+      S.pub_gt = gt;
+      S.pub_eq = eq;
+    }
+    cluster_sync_all();
+    const uint32_t me = cluster_rank();
+    uint32_t eq_before = 0, off = 0, quota = 0;
+    const uint32_t gt_addr = smem_addr(&S.pub_gt), eq_addr = smem_addr(&S.pub_eq);
+    for (uint32_t c = 0; c < (uint32_t)CLUSTER; ++c) {
+      const uint32_t gc = ld_cluster_u32(peer_addr(gt_addr, c));
+      const uint32_t ec = ld_cluster_u32(peer_addr(eq_addr, c));
+      const uint32_t left = r > eq_before ? r - eq_before : 0u;
+      const uint32_t qc = ec < left ? ec : left;
+      if (c == me) quota = qc;
+      if (c < me) off += gc + qc;
+      eq_before += ec;
+    }
+    sel.quota = quota;
+    sel.off = off;
+  }
+  return sel;
+}
+
+// Writes, in ascending j, the elements of `src` selected by `sel` to
+// out_row[sel.off ...] through the page transform.
+template <class Src>
+__device__ __forceinline__ void emit_selected(const Src& src, const Selection& sel, int32_t* out_row,
+                                              uint32_t k_row, const int32_t* page_row,
+                                              int32_t page_bits, SelectShared& S, ScanParity& par) {
+  uint32_t gt_run = 0, eq_run = 0;
+  const int64_t nt = src.tiles();
+  for (int64_t t = 0; t < nt; ++t) {
+    uint32_t key[4];
+    int32_t j[4];
+    bool valid[4];
+    src.tile(t, key, j, valid);
+    uint32_t ngt = 0, neq = 0;
+    bool is_gt[4], is_eq[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t pk = key[e] & sel.M;
+      is_gt[e] = valid[e] && pk > sel.T;
+      is_eq[e] = valid[e] && pk == sel.T;
+      ngt += is_gt[e];
+      neq += is_eq[e];
+    }
+    uint32_t total;
+    const uint32_t ex = block_excl_scan(ngt | (neq << 16), par.next(S), total);
+    uint32_t g = gt_run + (ex & 0xFFFFu), q = eq_run + (ex >> 16);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (is_gt[e] || (is_eq[e] && q < sel.quota)) {
+        const uint32_t pos = sel.off + g + (q < sel.quota ? q : sel.quota);
+        if (pos < k_row)
+          out_row[pos] = page_slot(page_row, page_bits, j[e]);
+        else
+          atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
+      }
+      g += is_gt[e];
+      q += is_eq[e];
+    }
+    gt_run += total & 0xFFFFu;
+    eq_run += total >> 16;
+  }
+}
+
+// A whole row (part) straight from global memory: full level-1 histogram, the
+// refinement levels and the emission.  Used by the multipass kernel and by
+// the streaming kernel when a row's candidates do not fit its list.
+template <int CLUSTER>
+__device__ __forceinline__ void select_from_global(const Params& p, int32_t row, const Row& r,
+                                                   const Part& part, SelectShared& S,
+                                                   ScanParity& par) {
+  const GlobalSrc src{r.base4, part.q0, part.q1, r.head, part.lo, part.hi};
+  for (int b = threadIdx.x; b < kBins1; b += kThreads) S.hist1[b] = 0u;
+  __syncthreads();
+  src.histogram(S.hist1, 0u, 0u, kShift1, kBins1 - 1);
+  __syncthreads();
+  if constexpr (CLUSTER > 1) cluster_sync_all();
+  const Selection sel = select_levels<CLUSTER>(S, src, (uint32_t)p.k, par);
+  emit_selected(src, sel, p.out + (int64_t)row * p.k, (uint32_t)p.k, r.page_row, p.page_bits, S, par);
+}
+
+}  // namespace topk

@@ -1,0 +1,291 @@
+// C ABI of the packed top-k + page transform: argument checks, launch planning
+// and kernel launches.  Declarations and the contract: include/topk_packed.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "topk_kernels.cuh"
+#include "topk_packed.h"
+
+namespace {
+
+using topk::Params;
+
+thread_local int g_last_cuda_error = 0;
+
+topk_status_t cuda_fail(cudaError_t e, topk_status_t s) {
+  g_last_cuda_error = (int)e;
+  return s;
+}
+
+constexpr int kMaxDevices = 64;
+
+// Per-device facts and one-time kernel attributes.
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+  int stream_ctas_per_sm = 0;     // resident stream CTAs per SM (cluster size 1)
+  int stream_clusters[4] = {};    // max resident clusters for sizes 2, 4, 8 (index 1..3)
+  int multipass_ctas_per_sm = 0;
+  cudaError_t error = cudaSuccess;
+};
+
+std::once_flag g_once[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+
+template <int C>
+cudaError_t prepare_stream(int& occupancy_or_clusters, int sms) {
+  const size_t smem = sizeof(topk::StreamShared);
+  cudaError_t e = cudaFuncSetAttribute(topk::topk_stream_kernel<C>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if constexpr (C == 1) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy_or_clusters,
+                                                         topk::topk_stream_kernel<1>, topk::kThreads, smem);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(C * sms), 1, 1);
+    cfg.blockDim = dim3(topk::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(&occupancy_or_clusters, topk::topk_stream_kernel<C>, &cfg);
+  }
+}
+
+void init_device(int dev) {
+  DeviceInfo& d = g_info[dev];
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) {
+    d.error = e;
+    return;
+  }
+  if (prop.major != 10 || prop.minor != 3) {
+    d.error = cudaErrorNoKernelImageForDevice;
+    return;
+  }
+  d.sms = prop.multiProcessorCount;
+  const size_t mp_smem = sizeof(topk::SelectShared);
+  e = cudaFuncSetAttribute(topk::topk_multipass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)mp_smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.multipass_ctas_per_sm, topk::topk_multipass_kernel,
+                                                      topk::kThreads, mp_smem);
+  if (e == cudaSuccess) e = prepare_stream<1>(d.stream_ctas_per_sm, d.sms);
+  if (e == cudaSuccess) e = prepare_stream<2>(d.stream_clusters[1], d.sms);
+  if (e == cudaSuccess) e = prepare_stream<4>(d.stream_clusters[2], d.sms);
+  if (e == cudaSuccess) e = prepare_stream<8>(d.stream_clusters[3], d.sms);
+  if (e != cudaSuccess) {
+    d.error = e;
+    return;
+  }
+  d.ok = d.multipass_ctas_per_sm > 0 && d.stream_ctas_per_sm > 0;
+  if (!d.ok) d.error = cudaErrorInvalidConfiguration;
+}
+
+const DeviceInfo* device_info(topk_status_t& st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    st = cuda_fail(e == cudaSuccess ? cudaErrorInvalidDevice : e, TOPK_ERR_DEVICE);
+    return nullptr;
+  }
+  std::call_once(g_once[dev], init_device, dev);
+  if (!g_info[dev].ok) {
+    st = cuda_fail(g_info[dev].error, TOPK_ERR_DEVICE);
+    return nullptr;
+  }
+  return &g_info[dev];
+}
+
+struct Plan {
+  int32_t path;
+  int32_t cluster;
+  int64_t grid;
+};
+
+int log2_exact(int32_t v) {
+  int b = 0;
+  while ((1 << b) < v) ++b;
+  return b;
+}
+
+topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_size, int32_t k,
+                          int32_t num_rows, const topk_launch_config_t* cfg) {
+  if (num_rows < 0 || k <= 0 || row_stride < 0 || pt_stride < 0) return TOPK_ERR_INVALID_ARG;
+  if (page_size <= 0 || (page_size & (page_size - 1)) != 0) return TOPK_ERR_INVALID_ARG;
+  if (cfg) {
+    if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_STREAM) return TOPK_ERR_INVALID_ARG;
+    const int c = cfg->cluster_size;
+    if (!(c == 0 || c == 1 || c == 2 || c == 4 || c == 8)) return TOPK_ERR_INVALID_ARG;
+    if (cfg->max_ctas < 0) return TOPK_ERR_INVALID_ARG;
+  }
+  if (k > TOPK_K_MAX) return TOPK_ERR_UNSUPPORTED;
+  if (page_size > (1 << 30)) return TOPK_ERR_UNSUPPORTED;
+  return TOPK_OK;
+}
+
+int cluster_index(int c) { return c == 2 ? 1 : c == 4 ? 2 : 3; }
+
+Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t num_rows,
+               const topk_launch_config_t* cfg) {
+  (void)row_stride;
+  Plan pl;
+  const int32_t want = cfg ? cfg->path : TOPK_PATH_AUTO;
+  pl.path = want == TOPK_PATH_AUTO ? TOPK_PATH_STREAM : want;
+  pl.cluster = 1;
+  if (pl.path == TOPK_PATH_MULTIPASS) {
+    const int64_t cap = (int64_t)d.sms * d.multipass_ctas_per_sm * 8;
+    pl.grid = num_rows < cap ? num_rows : cap;
+    if (cfg && cfg->max_ctas > 0 && pl.grid > cfg->max_ctas) pl.grid = cfg->max_ctas;
+    return pl;
+  }
+  pl.cluster = (cfg && cfg->cluster_size > 0) ? cfg->cluster_size : 1;
+  int64_t clusters;
+  if (pl.cluster == 1) {
+    clusters = (int64_t)d.sms * d.stream_ctas_per_sm;
+  } else {
+    clusters = d.stream_clusters[cluster_index(pl.cluster)];
+    if (clusters <= 0) clusters = 1;
+  }
+  if (clusters > num_rows) clusters = num_rows;
+  if (cfg && cfg->max_ctas > 0) {
+    const int64_t lim = cfg->max_ctas / pl.cluster;
+    if (clusters > lim) clusters = lim > 0 ? lim : 1;
+  }
+  pl.grid = clusters * pl.cluster;
+  return pl;
+}
+
+template <int C>
+cudaError_t launch_stream(const Params& prm, int64_t grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(topk::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(topk::StreamShared);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk::topk_stream_kernel<C>, prm);
+}
+
+}  // namespace
+
+extern "C" {
+
+topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                             const int32_t* row_starts, const int32_t* row_to_batch,
+                             const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                             int32_t k, int32_t* out, int32_t num_rows,
+                             const topk_launch_config_t* config, topk_stream_t stream) {
+  g_last_cuda_error = 0;
+  topk_status_t st = check_sizes(row_stride, pt_stride, page_size, k, num_rows, config);
+  if (st != TOPK_OK) return st;
+  if (num_rows == 0) return TOPK_OK;
+  if (!scores || !seq_lens || !row_starts || !page_table || !out) return TOPK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scores) & 3u) != 0) return TOPK_ERR_UNSUPPORTED;
+  const DeviceInfo* d = device_info(st);
+  if (!d) return st;
+
+  Params prm;
+  prm.scores = scores;
+  prm.row_stride = row_stride;
+  prm.seq_lens = seq_lens;
+  prm.row_starts = row_starts;
+  prm.row_to_batch = row_to_batch;
+  prm.page_table = page_table;
+  prm.pt_stride = pt_stride;
+  prm.page_bits = log2_exact(page_size);
+  prm.k = k;
+  prm.out = out;
+  prm.num_rows = num_rows;
+
+  const Plan pl = make_plan(*d, row_stride, num_rows, config);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (pl.path == TOPK_PATH_MULTIPASS) {
+    topk::topk_multipass_kernel<<<(unsigned)pl.grid, topk::kThreads, sizeof(topk::SelectShared), s>>>(prm);
+    e = cudaGetLastError();
+  } else {
+    switch (pl.cluster) {
+      case 1:
+        topk::topk_stream_kernel<1><<<(unsigned)pl.grid, topk::kThreads, sizeof(topk::StreamShared), s>>>(prm);
+        e = cudaGetLastError();
+        break;
+      case 2: e = launch_stream<2>(prm, pl.grid, s); break;
+      case 4: e = launch_stream<4>(prm, pl.grid, s); break;
+      default: e = launch_stream<8>(prm, pl.grid, s); break;
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return cuda_fail(e, TOPK_ERR_LAUNCH);
+  return TOPK_OK;
+}
+
+topk_status_t topk_packed(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                          const int32_t* row_starts, const int32_t* row_to_batch,
+                          const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                          int32_t k, int32_t* out, int32_t num_rows, topk_stream_t stream) {
+  return topk_packed_ex(scores, row_stride, seq_lens, row_starts, row_to_batch, page_table, pt_stride,
+                        page_size, k, out, num_rows, nullptr, stream);
+}
+
+topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
+                               const topk_launch_config_t* config, int32_t* path,
+                               int32_t* cluster_size, int32_t* grid_ctas, int32_t* threads_per_cta) {
+  g_last_cuda_error = 0;
+  topk_status_t st = check_sizes(row_stride, 0, 1, k, num_rows, config);
+  if (st != TOPK_OK) return st;
+  const DeviceInfo* d = device_info(st);
+  if (!d) return st;
+  const Plan pl = make_plan(*d, row_stride, num_rows, config);
+  if (path) *path = pl.path;
+  if (cluster_size) *cluster_size = pl.cluster;
+  if (grid_ctas) *grid_ctas = (int32_t)pl.grid;
+  if (threads_per_cta) *threads_per_cta = topk::kThreads;
+  return TOPK_OK;
+}
+
+const char* topk_status_string(topk_status_t status) {
+  switch (status) {
+    case TOPK_OK: return "success";
+    case TOPK_ERR_INVALID_ARG: return "invalid argument";
+    case TOPK_ERR_UNSUPPORTED: return "unsupported argument for this build";
+    case TOPK_ERR_LAUNCH: return "kernel launch failed";
+    case TOPK_ERR_DEVICE: return "no usable sm_103a device";
+  }
+  return "unknown status";
+}
+
+int topk_last_cuda_error(void) { return g_last_cuda_error; }
+
+topk_status_t topk_packed_device_flags(uint32_t* flags, int32_t reset, topk_stream_t stream) {
+  g_last_cuda_error = 0;
+  if (!flags) return TOPK_ERR_INVALID_ARG;
+  topk_status_t st;
+  if (!device_info(st)) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyFromSymbolAsync(flags, topk::g_device_flags, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && reset) {
+    static const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(topk::g_device_flags, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, TOPK_ERR_DEVICE);
+  return TOPK_OK;
+}
+
+}  // extern "C"

@@ -213,6 +213,42 @@ def named(name: str, device="cpu", **kw) -> Workload:
 
 
 # ---------------------------------------------------------------------------
+# Host copies of windows (for the CPU oracle in tests and the benchmark's
+# CPU-baseline leg).
+# ---------------------------------------------------------------------------
+
+def gather_windows(w: Workload, rows: torch.Tensor, chunk: int = 256):
+    """Host float32 [n, Lmax] windows of `rows` (padded with +inf) and their lengths."""
+    rows = rows.to(torch.int64).to(w.seq_lens.device)
+    L = w.seq_lens[rows].to(torch.int64).clamp_min(0)
+    starts = w.row_starts[rows].to(torch.int64)
+    lmax = max(int(L.max().item()) if rows.numel() else 0, 1)
+    flat = w.scores.reshape(-1)
+    out = np.empty((rows.numel(), lmax), dtype=np.float32)
+    ar = torch.arange(lmax, device=flat.device, dtype=torch.int64)
+    for a in range(0, rows.numel(), chunk):
+        r = rows[a:a + chunk]
+        base = r * w.row_stride + starts[a:a + chunk]
+        valid = ar[None, :] < L[a:a + chunk, None]
+        idx = torch.where(valid, base[:, None] + ar[None, :], torch.zeros_like(base[:, None]))
+        vals = flat[idx]
+        vals = torch.where(valid, vals, torch.full_like(vals, float("inf")))
+        out[a:a + r.numel()] = vals.cpu().numpy()
+    return out, L.cpu().numpy().astype(np.int32)
+
+
+def sample_rows(num_rows: int, n: int, seed: int = 0) -> torch.Tensor:
+    """Deterministic sample: the first and last rows plus evenly spread random ones."""
+    if num_rows <= n:
+        return torch.arange(num_rows)
+    g = torch.Generator().manual_seed(seed)
+    edge = min(32, n // 4)
+    mid = torch.randperm(num_rows - 2 * edge, generator=g)[: n - 2 * edge] + edge
+    return torch.cat([torch.arange(edge), torch.sort(mid).values,
+                      torch.arange(num_rows - edge, num_rows)])
+
+
+# ---------------------------------------------------------------------------
 # Small random problems for parity sweeps and oracle pins (host numpy arrays).
 # ---------------------------------------------------------------------------
 

@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bit-exact int32 equality everywhere (the result is unique).  Small problems are
+compared element by element for every kernel path; the full-size workloads, in
+the launch the benchmark times, are compared row by row on a sample of rows
+and checked on every row for the invariants of the result."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import topk_packed_reference
+from sparse_attention_top_packed_b300 import binding
+from sparse_attention_top_packed_b300 import workloads as wl
+from tests.gpu_helpers import check_invariants_all_rows, oracle_rows, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [dict(path="multipass"), dict(path="stream", cluster_size=1),
+         dict(path="stream", cluster_size=2), dict(path="stream", cluster_size=4),
+         dict(path="stream", cluster_size=8)]
+PATH_IDS = ["multipass", "stream1", "stream2", "stream4", "stream8"]
+
+
+def run(w, **launch):
+    out = torch.full((w.num_rows, w.k), -7, dtype=torch.int32, device=w.scores.device)
+    binding.run_workload(w, out=out, **launch)
+    torch.cuda.synchronize()
+    return out
+
+
+def host_problem_to_device(p, dev):
+    rows = p.num_rows
+    return wl.Workload("random", torch.from_numpy(p.scores).to(dev).reshape(rows, p.row_stride),
+                       p.row_stride, torch.from_numpy(p.seq_lens).to(dev),
+                       torch.from_numpy(p.row_starts).to(dev),
+                       None if p.row_to_batch is None else torch.from_numpy(p.row_to_batch).to(dev),
+                       torch.from_numpy(p.page_table).to(dev), p.pt_stride, p.page_size, p.k, rows)
+
+
+def oracle_host(p):
+    return topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts, p.row_to_batch,
+                                 p.page_table, p.pt_stride, p.page_size, p.k)
+
+
+@pytest.fixture(autouse=True)
+def _flags_stay_clear(cuda_device):
+    binding.topk_packed_device_flags(reset=True)
+    yield
+    assert binding.topk_packed_device_flags() == 0, "a bounded device wait gave up"
+
+
+@pytest.mark.parametrize("launch", PATHS, ids=PATH_IDS)
+def test_tiny(cuda_device, launch):
+    w = wl.tiny(device=cuda_device)
+    out = run(w, **launch)
+    want = oracle_rows(w, torch.arange(w.num_rows))
+    assert np.array_equal(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("launch", PATHS, ids=PATH_IDS)
+def test_decode(cuda_device, launch):
+    w = wl.decode(device=cuda_device)
+    out = run(w, **launch)
+    want = oracle_rows(w, torch.arange(w.num_rows))
+    assert np.array_equal(out.cpu().numpy(), want)
+    check_invariants_all_rows(w, out)
+
+
+CASES = [
+    # values, rows, max_len, k, page_size
+    ("normal", 24, 20000, 2048, 64),
+    ("normal", 40, 9000, 300, 16),
+    ("bf16", 24, 30000, 2048, 64),
+    ("ties", 30, 12000, 777, 1),
+    ("int", 16, 20000, 2048, 64),
+    ("equal", 8, 10000, 2048, 64),
+    ("ascending", 10, 25000, 2048, 64),
+    ("descending", 10, 25000, 2048, 64),
+    ("normal", 20, 5000, 1, 4),
+    ("normal", 12, 70000, 2048, 64),
+    ("bf16", 50, 3000, 32, 64),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-L{c[2]}-k{c[3]}" for c in CASES])
+@pytest.mark.parametrize("launch", PATHS, ids=PATH_IDS)
+def test_random_problems(cuda_device, case, launch):
+    values, rows, max_len, k, page_size = case
+    rng = np.random.default_rng(zlib.crc32(f"{values}-{max_len}-{k}".encode()))
+    p = wl.random_problem(rng, rows=rows, max_len=max_len, k=k, page_size=page_size, values=values,
+                          slack=13)
+    w = host_problem_to_device(p, cuda_device)
+    before = w.scores.clone()
+    out = run(w, **launch)
+    assert torch.equal(before, w.scores), "the score buffer was written"
+    assert np.array_equal(out.cpu().numpy(), oracle_host(p))
+
+
+@pytest.mark.parametrize("launch", PATHS, ids=PATH_IDS)
+def test_edge_lengths_and_offsets(cuda_device, launch):
+    """seq_len in {0, 1, k-1, k, k+1, a tile boundary +-1}, every start offset
+    mod 4, an odd row stride (so absolute alignment differs from row_start % 4),
+    identity map, signed zeros and infinities in the windows."""
+    k = 64
+    lens = [0, 1, k - 1, k, k + 1, 4095, 4096, 4097, 8191, 8193, 2 * 4096 * 8 + 3, -5]
+    rng = np.random.default_rng(3)
+    rows = []
+    for L in lens:
+        for off in range(4):
+            rows.append((L, off))
+    n = len(rows)
+    stride = max(L for L, _ in rows) + 7
+    stride += 1 - stride % 2  # odd: absolute alignment differs from row_start % 4
+    scores = np.full(n * stride, np.inf, dtype=np.float32)
+    seq = np.zeros(n, np.int32)
+    st = np.zeros(n, np.int32)
+    for i, (L, off) in enumerate(rows):
+        Lp = max(L, 0)
+        v = rng.standard_normal(Lp).astype(np.float32)
+        if Lp > 10:
+            v[rng.integers(0, Lp, size=Lp // 10)] = -0.0
+            v[rng.integers(0, Lp, size=Lp // 10)] = 0.0
+            v[rng.integers(0, Lp, size=3)] = np.inf
+            v[rng.integers(0, Lp, size=3)] = -np.inf
+        seq[i] = L
+        st[i] = off + (i % 3)
+        scores[i * stride + st[i]: i * stride + st[i] + Lp] = v
+    pages = -(-stride // 16)
+    table = rng.choice(1 << 24, size=n * pages, replace=False).astype(np.int32)
+    p = wl.HostProblem(scores, stride, seq, st, None, table, pages, 16, k)
+    w = host_problem_to_device(p, cuda_device)
+    out = run(w, **launch)
+    assert np.array_equal(out.cpu().numpy(), oracle_host(p))
+
+
+@pytest.mark.parametrize("k", [1, 2, 31, 512, 2048])
+def test_k_values_against_each_other_and_oracle(cuda_device, k):
+    rng = np.random.default_rng(k)
+    p = wl.random_problem(rng, rows=16, max_len=12000, k=k, page_size=64, values="bf16")
+    w = host_problem_to_device(p, cuda_device)
+    want = oracle_host(p)
+    for launch in PATHS:
+        assert np.array_equal(run(w, **launch).cpu().numpy(), want), launch
+
+
+def test_non_default_stream(cuda_device):
+    w = wl.tiny(device=cuda_device)
+    s = torch.cuda.Stream()
+    out = torch.empty((w.num_rows, w.k), dtype=torch.int32, device=cuda_device)
+    with torch.cuda.stream(s):
+        binding.run_workload(w, out=out, stream=s)
+    s.synchronize()
+    assert np.array_equal(out.cpu().numpy(), oracle_rows(w, torch.arange(w.num_rows)))
+
+
+def test_zero_rows_launches_nothing(cuda_device):
+    w = wl.tiny(device=cuda_device)
+    out = torch.full((1,), 5, dtype=torch.int32, device=cuda_device)
+    binding.topk_packed(w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch,
+                        w.page_table, w.pt_stride, w.page_size, w.k, out, 0)
+    torch.cuda.synchronize()
+    assert out.item() == 5
+
+
+def test_plan_reports_the_launch(cuda_device):
+    plan = binding.topk_packed_plan(140000, 2048, 4096)
+    assert plan["path"] == binding.PATHS["stream"]
+    assert plan["threads_per_cta"] == 512
+    assert plan["grid_ctas"] % plan["cluster_size"] == 0
+    mp = binding.topk_packed_plan(140000, 2048, 4096, path="multipass")
+    assert mp["path"] == binding.PATHS["multipass"]
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, in the launch the benchmark times (topk_packed, auto).
+# ---------------------------------------------------------------------------
+def _full_size(w, sample: int):
+    out = torch.empty((w.num_rows, w.k), dtype=torch.int32, device=w.scores.device)
+    checksum = w.scores.view(torch.int32).sum(dtype=torch.int64)
+    binding.topk_packed(w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch,
+                        w.page_table, w.pt_stride, w.page_size, w.k, out, w.num_rows)
+    torch.cuda.synchronize()
+    assert torch.equal(checksum, w.scores.view(torch.int32).sum(dtype=torch.int64))
+    rows = sample_rows(w.num_rows, sample)
+    want = oracle_rows(w, rows)
+    got = out[rows.to(out.device)].cpu().numpy()
+    bad = np.nonzero((got != want).any(axis=1))[0]
+    assert bad.size == 0, f"rows {rows[bad[:10]].tolist()} differ from the oracle"
+    check_invariants_all_rows(w, out)
+    return out
+
+
+def test_prefill_full_size(cuda_device):
+    w = wl.prefill(device=cuda_device)
+    out = _full_size(w, sample=512)
+    # the cluster path gives the same bits
+    out2 = run(w, path="stream", cluster_size=2)
+    assert torch.equal(out, out2)
+
+
+def test_long_context_full_size(cuda_device):
+    w = wl.long_context(device=cuda_device)
+    out = _full_size(w, sample=160)
+    wi = wl.long_context(device=cuda_device, identity_map=True)
+    out_id = run(wi)
+    assert torch.equal(out, out_id), "row_to_batch=NULL with pt_stride 0 must match the zero map"
+    out4 = run(w, path="stream", cluster_size=4)
+    assert torch.equal(out, out4)
+
+
+def test_mixed_full_size(cuda_device):
+    w = wl.mixed(device=cuda_device)
+    assert int((w.seq_lens < w.k).sum()) > 0, "the mixed batch must hold windows shorter than k"
+    out = _full_size(w, sample=768)
+    out2 = run(w, path="multipass")
+    assert torch.equal(out, out2)
