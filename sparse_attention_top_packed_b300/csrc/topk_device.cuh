@@ -23,8 +23,7 @@
 
 namespace topk {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxWarps = 32;  // largest CTA: 1024 threads
 
 constexpr int kBins1 = 4096;  // level 1: key bits [20, 32)
 constexpr int kShift1 = 20;
@@ -125,10 +124,11 @@ __device__ __forceinline__ int32_t page_slot(const int32_t* page_row, int32_t pa
 }
 
 // A window no longer than k: every index is taken; slots past L are -1.
+template <int NT>
 __device__ __forceinline__ void emit_whole_window(const Params& p, int32_t row, const Row& r,
                                                   uint32_t part, uint32_t parts) {
   int32_t* o = p.out + (int64_t)row * p.k;
-  for (int32_t t = (int32_t)(part * kThreads + threadIdx.x); t < p.k; t += (int32_t)(parts * kThreads))
+  for (int32_t t = (int32_t)(part * NT + threadIdx.x); t < p.k; t += (int32_t)(parts * NT))
     o[t] = t < r.L ? page_slot(r.page_row, p.page_bits, t) : -1;
 }
 
@@ -234,7 +234,7 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 // ---------------------------------------------------------------------------
 // Block-wide scans.  Counts travel packed: low 16 bits / high 16 bits, each
 // at most 2048 per call, so the fields never carry into each other.
-// `scratch` holds kWarps words; callers alternate two buffers between calls
+// `scratch` holds NT/32 words; callers alternate two buffers between calls
 // (every call contains one __syncthreads, which makes two enough).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
@@ -257,22 +257,35 @@ __device__ __forceinline__ uint32_t warp_incl_suffix(uint32_t v) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xFFFFFFFFu, v); }
+
+__device__ __forceinline__ uint32_t warp_max(uint32_t v) { return __reduce_max_sync(0xFFFFFFFFu, v); }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
 // Exclusive prefix of v over threads in index order; `total` gets the sum.
+template <int NT>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t& total) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t incl = warp_incl_scan(v);
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
-  const uint32_t wt = lane < kWarps ? scratch[lane] : 0u;
+  const uint32_t wt = lane < NW ? scratch[lane] : 0u;
   const uint32_t wincl = warp_incl_scan(wt);
   const uint32_t wexcl = __shfl_sync(0xFFFFFFFFu, wincl - wt, warp);
-  total = __shfl_sync(0xFFFFFFFFu, wincl, kWarps - 1);
+  total = __shfl_sync(0xFFFFFFFFu, wincl, NW - 1);
   return wexcl + incl - v;
 }
 
+template <int NT>
 __device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* scratch) {
   uint32_t total;
-  block_excl_scan(v, scratch, total);
+  block_excl_scan<NT>(v, scratch, total);
   return total;
 }
 
@@ -287,11 +300,12 @@ struct Pick {
   uint32_t bin, above, count;
 };
 
-template <int NBINS, int CLUSTER>
+template <int NBINS, int CLUSTER, int NT>
 __device__ __forceinline__ Pick block_pick(const uint32_t* hist, uint32_t r, uint32_t* scratch,
                                            Pick* slot) {
-  constexpr int B = NBINS / kThreads;  // bins per thread: 8 or 2
-  static_assert(B == 8 || B == 2, "bins per thread");
+  constexpr int B = NBINS / NT;  // bins per thread
+  constexpr int NW = NT / 32;
+  static_assert(B == 1 || B == 2 || B == 4 || B == 8, "bins per thread");
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   uint32_t h[B];
   if constexpr (CLUSTER == 1) {
@@ -304,13 +318,15 @@ __device__ __forceinline__ Pick block_pick(const uint32_t* hist, uint32_t r, uin
 #pragma unroll
     for (int c = 0; c < CLUSTER; ++c) {
       const uint32_t a = peer_addr(local, (uint32_t)c);
-      if constexpr (B == 8) {
-        const uint4 v0 = ld_cluster_v4(a), v1 = ld_cluster_v4(a + 16u);
-        h[0] += v0.x; h[1] += v0.y; h[2] += v0.z; h[3] += v0.w;
-        h[4] += v1.x; h[5] += v1.y; h[6] += v1.z; h[7] += v1.w;
+      if constexpr (B >= 4) {
+#pragma unroll
+        for (int i = 0; i < B; i += 4) {
+          const uint4 v = ld_cluster_v4(a + 4u * i);
+          h[i] += v.x; h[i + 1] += v.y; h[i + 2] += v.z; h[i + 3] += v.w;
+        }
       } else {
-        h[0] += ld_cluster_u32(a);
-        h[1] += ld_cluster_u32(a + 4u);
+#pragma unroll
+        for (int i = 0; i < B; ++i) h[i] += ld_cluster_u32(a + 4u * i);
       }
     }
   }
@@ -322,7 +338,7 @@ __device__ __forceinline__ Pick block_pick(const uint32_t* hist, uint32_t r, uin
   if (lane == 0) scratch[warp] = incl;
   if (t == 0) *slot = Pick{0u, 0u, 0u};
   __syncthreads();
-  const uint32_t wt = lane < kWarps ? scratch[lane] : 0u;
+  const uint32_t wt = lane < NW ? scratch[lane] : 0u;
   const uint32_t wsuf = warp_incl_suffix(wt);
   const uint32_t above_warps = __shfl_sync(0xFFFFFFFFu, wsuf - wt, warp);
   uint32_t run = above_warps + incl - s;  // sum over bins above this thread's bins
@@ -337,28 +353,25 @@ __device__ __forceinline__ Pick block_pick(const uint32_t* hist, uint32_t r, uin
 }
 
 // Sum of this CTA's own hist[b] for b > bin (only needed with clusters).
-template <int NBINS>
+template <int NBINS, int NT>
 __device__ __forceinline__ uint32_t own_above(const uint32_t* hist, uint32_t bin, uint32_t* scratch) {
-  constexpr int B = NBINS / kThreads;
+  constexpr int B = NBINS / NT;
   uint32_t s = 0;
 #pragma unroll
   for (int i = 0; i < B; ++i) {
     const uint32_t b = threadIdx.x * B + i;
     if (b > bin) s += hist[b];
   }
-  return block_sum(s, scratch);
+  return block_sum<NT>(s, scratch);
 }
 
 // ---------------------------------------------------------------------------
-// Sources of (key, j) pairs for the refinement levels and the emission:
-//   GlobalSrc -- a row part read straight from global memory (16-byte loads,
-//                masked lanes), used by the multipass kernel and as the
-//                streaming kernel's fallback;
-//   CandSrc   -- the streaming kernel's candidate list in shared memory, kept
-//                in ascending j.
-// Both walk "tiles" of kThreads*4 items in ascending j, 4 per thread, for the
-// ordered emission.
+// A row part read straight from global memory (16-byte loads, masked lanes),
+// as a source of (key, j) pairs: for the multipass kernel and for the
+// streaming kernel's fallback.  The emission walks it in "tiles" of NT*4
+// elements in ascending j, 4 per thread.
 // ---------------------------------------------------------------------------
+template <int NT>
 struct GlobalSrc {
   const float4* base4;
   int64_t q0, q1;
@@ -369,34 +382,33 @@ struct GlobalSrc {
   __device__ __forceinline__ void histogram(uint32_t* hist, uint32_t M, uint32_t T, int shift,
                                             uint32_t nbins_mask) const {
     constexpr int U = 4;
-    for (int64_t q = q0 + threadIdx.x; q < q1; q += (int64_t)kThreads * U) {
+    for (int64_t q = q0 + threadIdx.x; q < q1; q += (int64_t)NT * U) {
       float4 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t qq = q + (int64_t)u * kThreads;
-        if (qq < q1) v[u] = __ldg(base4 + qq);
+        const int64_t qq = q + (int64_t)u * NT;
+        v[u] = qq < q1 ? __ldg(base4 + qq) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t qq = q + (int64_t)u * kThreads;
-        if (qq < q1) {
-          const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-          const int64_t j0 = qq * 4 - head;
+        const int64_t qq = q + (int64_t)u * NT;
+        const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const int64_t j0 = qq * 4 - head;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int64_t j = j0 + e;
-            const uint32_t key = key_of(x[e]);
-            if (j >= lo && j < hi && (key & M) == T) atomicAdd(hist + ((key >> shift) & nbins_mask), 1u);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int64_t j = j0 + e;
+          const uint32_t key = key_of(x[e]);
+          if (qq < q1 && j >= lo && j < hi && (key & M) == T)
+            atomicAdd(hist + ((key >> shift) & nbins_mask), 1u);
         }
       }
     }
   }
 
-  __device__ __forceinline__ int64_t tiles() const { return (q1 - q0 + kThreads - 1) / kThreads; }
+  __device__ __forceinline__ int64_t tiles() const { return (q1 - q0 + NT - 1) / NT; }
 
   __device__ __forceinline__ void tile(int64_t t, uint32_t key[4], int32_t j[4], bool valid[4]) const {
-    const int64_t q = q0 + t * kThreads + threadIdx.x;
+    const int64_t q = q0 + t * NT + threadIdx.x;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (q < q1) v = __ldg(base4 + q);
     const float x[4] = {v.x, v.y, v.z, v.w};
@@ -410,51 +422,17 @@ struct GlobalSrc {
   }
 };
 
-struct CandSrc {
-  const uint32_t* keys;
-  const int32_t* js;
-  int32_t count;
-
-  __device__ __forceinline__ void histogram(uint32_t* hist, uint32_t M, uint32_t T, int shift,
-                                            uint32_t nbins_mask) const {
-    for (int32_t i = threadIdx.x; i < count; i += kThreads) {
-      const uint32_t key = keys[i];
-      if ((key & M) == T) atomicAdd(hist + ((key >> shift) & nbins_mask), 1u);
-    }
-  }
-
-  __device__ __forceinline__ int64_t tiles() const { return (count + kThreads * 4 - 1) / (kThreads * 4); }
-
-  __device__ __forceinline__ void tile(int64_t t, uint32_t key[4], int32_t j[4], bool valid[4]) const {
-    const int32_t e0 = (int32_t)t * kThreads * 4 + threadIdx.x * 4;
-    if (e0 + 3 < count) {
-      const uint4 k4 = *reinterpret_cast<const uint4*>(keys + e0);
-      const int4 j4 = *reinterpret_cast<const int4*>(js + e0);
-      key[0] = k4.x; key[1] = k4.y; key[2] = k4.z; key[3] = k4.w;
-      j[0] = j4.x; j[1] = j4.y; j[2] = j4.z; j[3] = j4.w;
-      valid[0] = valid[1] = valid[2] = valid[3] = true;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        valid[e] = e0 + e < count;
-        key[e] = valid[e] ? keys[e0 + e] : 0u;
-        j[e] = valid[e] ? js[e0 + e] : 0;
-      }
-    }
-  }
-};
-
 // Per-CTA shared state of the selection.  Everything a peer CTA reads through
 // distributed shared memory sits at the same offset in every CTA.
 struct SelectShared {
   uint32_t hist1[kBins1];
   uint32_t hist2[kBins23];
   uint32_t hist3[kBins23];
-  uint32_t scratch[2][kWarps];
+  uint32_t scratch[2][kMaxWarps];
   Pick pick[2];
   uint32_t pub_gt;        // published: this CTA's count of elements above the prefix
   uint32_t pub_eq;        // published: this CTA's count of prefix-equal elements
-  uint32_t pub_overflow;  // published: candidate list overflowed (streaming only)
+  uint32_t pub_overflow;  // published: a candidate list overflowed (streaming only)
   uint32_t pad_;
 };
 
@@ -487,45 +465,45 @@ struct ScanParity {
 // the exact number of the CTA's elements in that bin, and a barrier (cluster
 // barrier with clusters) separates its last update from this call.  `k_row`
 // is the number to select (k; the row has more than k elements).
-template <int CLUSTER, class Src>
+template <int CLUSTER, int NT, class Src>
 __device__ __forceinline__ Selection select_levels(SelectShared& S, const Src& src, uint32_t k_row,
                                                    ScanParity& par) {
-  Pick pk = block_pick<kBins1, CLUSTER>(S.hist1, k_row, par.next(S), par.next_pick(S));
+  Pick pk = block_pick<kBins1, CLUSTER, NT>(S.hist1, k_row, par.next(S), par.next_pick(S));
   uint32_t r = k_row - pk.above;
   uint32_t M = 0xFFF00000u, T = pk.bin << kShift1;
   uint32_t gt = 0, eq = 0;
   if constexpr (CLUSTER > 1) {
-    gt = own_above<kBins1>(S.hist1, pk.bin, par.next(S));
+    gt = own_above<kBins1, NT>(S.hist1, pk.bin, par.next(S));
     eq = S.hist1[pk.bin];
   }
   if (pk.count != r) {
     // level 2: bits [10, 20) of the keys in bucket T
-    for (int b = threadIdx.x; b < kBins23; b += kThreads) S.hist2[b] = 0u;
+    for (int b = threadIdx.x; b < kBins23; b += NT) S.hist2[b] = 0u;
     __syncthreads();
     src.histogram(S.hist2, M, T, kShift2, kBins23 - 1);
     __syncthreads();
     if constexpr (CLUSTER > 1) cluster_sync_all();
-    pk = block_pick<kBins23, CLUSTER>(S.hist2, r, par.next(S), par.next_pick(S));
+    pk = block_pick<kBins23, CLUSTER, NT>(S.hist2, r, par.next(S), par.next_pick(S));
     r -= pk.above;
     M |= 0x000FFC00u;
     T |= pk.bin << kShift2;
     if constexpr (CLUSTER > 1) {
-      gt += own_above<kBins23>(S.hist2, pk.bin, par.next(S));
+      gt += own_above<kBins23, NT>(S.hist2, pk.bin, par.next(S));
       eq = S.hist2[pk.bin];
     }
     if (pk.count != r) {
       // level 3: bits [0, 10)
-      for (int b = threadIdx.x; b < kBins23; b += kThreads) S.hist3[b] = 0u;
+      for (int b = threadIdx.x; b < kBins23; b += NT) S.hist3[b] = 0u;
       __syncthreads();
       src.histogram(S.hist3, M, T, kShift3, kBins23 - 1);
       __syncthreads();
       if constexpr (CLUSTER > 1) cluster_sync_all();
-      pk = block_pick<kBins23, CLUSTER>(S.hist3, r, par.next(S), par.next_pick(S));
+      pk = block_pick<kBins23, CLUSTER, NT>(S.hist3, r, par.next(S), par.next_pick(S));
       r -= pk.above;
       M = 0xFFFFFFFFu;
       T |= pk.bin;
       if constexpr (CLUSTER > 1) {
-        gt += own_above<kBins23>(S.hist3, pk.bin, par.next(S));
+        gt += own_above<kBins23, NT>(S.hist3, pk.bin, par.next(S));
         eq = S.hist3[pk.bin];
       }
     }
@@ -563,7 +541,7 @@ __device__ __forceinline__ Selection select_levels(SelectShared& S, const Src& s
 
 // Writes, in ascending j, the elements of `src` selected by `sel` to
 // out_row[sel.off ...] through the page transform.
-template <class Src>
+template <int NT, class Src>
 __device__ __forceinline__ void emit_selected(const Src& src, const Selection& sel, int32_t* out_row,
                                               uint32_t k_row, const int32_t* page_row,
                                               int32_t page_bits, SelectShared& S, ScanParity& par) {
@@ -585,7 +563,7 @@ __device__ __forceinline__ void emit_selected(const Src& src, const Selection& s
       neq += is_eq[e];
     }
     uint32_t total;
-    const uint32_t ex = block_excl_scan(ngt | (neq << 16), par.next(S), total);
+    const uint32_t ex = block_excl_scan<NT>(ngt | (neq << 16), par.next(S), total);
     uint32_t g = gt_run + (ex & 0xFFFFu), q = eq_run + (ex >> 16);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -606,19 +584,19 @@ __device__ __forceinline__ void emit_selected(const Src& src, const Selection& s
 
 // A whole row (part) straight from global memory: full level-1 histogram, the
 // refinement levels and the emission.  Used by the multipass kernel and by
-// the streaming kernel when a row's candidates do not fit its list.
-template <int CLUSTER>
+// the streaming kernel when a row's candidates do not fit its lists.
+template <int CLUSTER, int NT>
 __device__ __forceinline__ void select_from_global(const Params& p, int32_t row, const Row& r,
                                                    const Part& part, SelectShared& S,
                                                    ScanParity& par) {
-  const GlobalSrc src{r.base4, part.q0, part.q1, r.head, part.lo, part.hi};
-  for (int b = threadIdx.x; b < kBins1; b += kThreads) S.hist1[b] = 0u;
+  const GlobalSrc<NT> src{r.base4, part.q0, part.q1, r.head, part.lo, part.hi};
+  for (int b = threadIdx.x; b < kBins1; b += NT) S.hist1[b] = 0u;
   __syncthreads();
   src.histogram(S.hist1, 0u, 0u, kShift1, kBins1 - 1);
   __syncthreads();
   if constexpr (CLUSTER > 1) cluster_sync_all();
-  const Selection sel = select_levels<CLUSTER>(S, src, (uint32_t)p.k, par);
-  emit_selected(src, sel, p.out + (int64_t)row * p.k, (uint32_t)p.k, r.page_row, p.page_bits, S, par);
+  const Selection sel = select_levels<CLUSTER, NT>(S, src, (uint32_t)p.k, par);
+  emit_selected<NT>(src, sel, p.out + (int64_t)row * p.k, (uint32_t)p.k, r.page_row, p.page_bits, S, par);
 }
 
 }  // namespace topk

@@ -5,16 +5,22 @@
 //                          on the keys that share the chosen prefix, then the
 //                          ordered emission -- every pass straight from global
 //                          memory.  Simple and always exact.
-//   topk_stream_kernel     persistent CTAs (or clusters of CTAs sharing a row)
-//                          that stream every window once from HBM through a
-//                          ring of TMA bulk copies into shared memory.  While
-//                          streaming, a running lower bound on the k-th largest
-//                          key (a histogram bin edge that can only rise) drops
-//                          almost every element at a single compare; the few
-//                          that pass are appended, in window order, to a list
-//                          in shared memory.  The radix select then runs on
-//                          that list.  A row whose list cannot hold its
-//                          candidates falls back to the multipass procedure.
+//   topk_stream_kernel     persistent CTAs (one per SM), or clusters of CTAs
+//                          sharing a row, that read every window once from HBM.
+//                          Each of the 32 warps owns a contiguous slice of the
+//                          row and streams it through its own ring of TMA bulk
+//                          copies into shared memory, with no block-wide
+//                          synchronisation while streaming.  A running lower
+//                          bound on the k-th largest key (a level-1 histogram
+//                          bin edge that only rises, shared by all warps and
+//                          raised lock-free) drops almost every element at one
+//                          compare; the few that pass are appended, in window
+//                          order, to the warp's list in shared memory.  Since
+//                          slices are contiguous and in warp order, the lists
+//                          concatenated in warp order are in window order.  The
+//                          radix select then runs on the lists.  A row whose
+//                          candidates overflow a list falls back to the
+//                          multipass procedure for that row.
 #pragma once
 
 #include "topk_device.cuh"
@@ -26,105 +32,126 @@ __device__ __forceinline__ bool row_is_whole(const Row& r, int32_t k) { return r
 // ---------------------------------------------------------------------------
 // Multipass kernel.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 2) topk_multipass_kernel(Params p) {
+constexpr int kMultipassThreads = 512;
+
+__global__ void __launch_bounds__(kMultipassThreads, 2) topk_multipass_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelectShared& S = *reinterpret_cast<SelectShared*>(smem_raw);
   ScanParity par;
   for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
     const Row r = load_row(p, (int32_t)row);
     if (row_is_whole(r, p.k)) {
-      emit_whole_window(p, (int32_t)row, r, 0u, 1u);
+      emit_whole_window<kMultipassThreads>(p, (int32_t)row, r, 0u, 1u);
       continue;
     }
     const Part part = part_of(r, 0u, 1u);
-    select_from_global<1>(p, (int32_t)row, r, part, S, par);
+    select_from_global<1, kMultipassThreads>(p, (int32_t)row, r, part, S, par);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Streaming kernel.
 // ---------------------------------------------------------------------------
-constexpr int kChunkFloats = kThreads * 8;  // one chunk = one tile: 8 floats per thread
-constexpr int kChunkBytes = kChunkFloats * 4;
-constexpr int kStages = 3;
-constexpr int kCap = 4096;  // candidate list entries (>= k plus the threshold bucket)
+constexpr int kStreamThreads = 1024;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kChunkBytes = 2048;              // one warp chunk: 16 floats per lane
+constexpr int kChunkQuads = kChunkBytes / 16;  // 128
+constexpr int kStages = 2;                     // chunks in flight per warp
+constexpr int kWarpCap = 128;                  // list entries per warp (4096 per CTA)
 
-// Thread 0's position in the chunk sequence (kept in shared memory so that the
-// other 511 threads do not hold it in registers).
-struct ProducerState {
-  int64_t row;
-  int64_t bytes;
-  const char* src;
-  uint64_t policy;
-  int32_t chunk, nchunks;
-  uint32_t issued;
+// The producer of one warp (its lane 0): where the next chunk comes from.
+struct WarpProducer {
+  const char* src;  // next chunk of the current slice
+  int64_t left;     // bytes of the slice not yet issued
+  int64_t row;      // row of the current slice
+  uint32_t issued;  // chunks issued so far
   uint32_t pad_;
 };
 
 struct StreamShared {
-  float4 ring[kStages][kChunkFloats / 4];
-  uint32_t cand_key[kCap];
-  int32_t cand_j[kCap];
+  float4 ring[kStreamWarps][kStages][kChunkQuads];
+  uint32_t list_key[kStreamWarps][kWarpCap];
+  int32_t list_j[kStreamWarps][kWarpCap];
   SelectShared sel;
-  uint64_t full[kStages];
-  ProducerState prod;
-  uint32_t wt[2][kWarps];  // per-warp packed counts of the current tile
-  uint32_t b0;             // running threshold: level-1 bin, only rises
-  uint32_t top;            // highest level-1 bin holding a candidate
+  uint64_t full[kStreamWarps][kStages];
+  WarpProducer prod[kStreamWarps];
+  uint32_t count[kStreamWarps];  // list lengths at the end of the row
+  uint32_t wgt[kStreamWarps];    // per-warp counts for the emission
+  uint32_t weq[kStreamWarps];
+  uint32_t b0;        // running threshold: level-1 bin, only rises
+  uint32_t top;       // highest level-1 bin holding a candidate (may lag)
+  uint32_t overflow;  // a list of this row overflowed
 };
 
-// The producer (thread 0) walks the same sequence of chunks the consumers do:
-// the rows of this CTA (cluster) in order, rows with a window of at most k
-// elements skipped, each row part cut into kChunkBytes pieces from its
-// 16-byte aligned start.
-__device__ __forceinline__ void producer_start(ProducerState& P, int64_t first_row, int32_t ncl) {
-  P.row = first_row - ncl;
-  P.bytes = 0;
-  P.src = nullptr;
-  P.chunk = P.nchunks = 0;
-  P.issued = 0;
-  P.policy = l2_evict_first_policy();
+// Slice of a row part owned by warp w: quads [q0, q1), window indices [lo, hi).
+struct Slice {
+  int64_t q0, q1;
+  int32_t lo, hi;
+};
+
+__device__ __forceinline__ Slice slice_of(const Row& r, const Part& part, int w) {
+  const int64_t nq = part.q1 - part.q0;
+  const int64_t per = (nq + kStreamWarps - 1) / kStreamWarps;
+  Slice s;
+  s.q0 = min(part.q0 + (int64_t)w * per, part.q1);
+  s.q1 = min(s.q0 + per, part.q1);
+  s.lo = (int32_t)min(max(s.q0 * 4 - r.head, (int64_t)0), (int64_t)r.L);
+  s.hi = (int32_t)min(max(s.q1 * 4 - r.head, (int64_t)0), (int64_t)r.L);
+  return s;
 }
 
+// Moves the producer of warp w to the next row (of this CTA / cluster) in
+// which warp w owns a non-empty slice.
 template <int CLUSTER>
-__device__ __forceinline__ bool producer_advance(ProducerState& P, const Params& p, int32_t ncl,
-                                                 uint32_t rank) {
-  while (P.chunk >= P.nchunks) {
+__device__ __noinline__ void producer_next_row(WarpProducer& P, const Params& p, int32_t ncl,
+                                               uint32_t rank, int w) {
+  while (true) {
     P.row += ncl;
-    if (P.row >= p.num_rows) return false;
+    if (P.row >= p.num_rows) {
+      P.left = 0;
+      return;
+    }
     const Row r = load_row(p, (int32_t)P.row);
-    P.chunk = P.nchunks = 0;
     if (row_is_whole(r, p.k)) continue;
-    const Part part = part_of(r, rank, CLUSTER);
-    P.bytes = (part.q1 - part.q0) * 16;
-    P.src = reinterpret_cast<const char*>(r.base4 + part.q0);
-    P.nchunks = (int32_t)((P.bytes + kChunkBytes - 1) / kChunkBytes);
+    const Slice sl = slice_of(r, part_of(r, rank, CLUSTER), w);
+    if (sl.q1 > sl.q0) {
+      P.src = reinterpret_cast<const char*>(r.base4 + sl.q0);
+      P.left = (sl.q1 - sl.q0) * 16;
+      return;
+    }
   }
-  return true;
 }
 
-// Issues the next chunk of the sequence into `slot` (which is issued % kStages).
+// Lane 0 of warp w: issues the next chunk of the warp's sequence into `slot`
+// (= issued % kStages).  The sequence is the slices of the rows in the order
+// the warp consumes them, each cut into kChunkBytes pieces.
 template <int CLUSTER>
-__device__ __noinline__ void producer_issue(StreamShared& S, const Params& p, int32_t ncl, uint32_t rank,
-                                            uint32_t slot) {
-  ProducerState& P = S.prod;
-  fence_proxy_async_smem();  // consumers' reads of the slot precede the async-proxy write
-  if (!producer_advance<CLUSTER>(P, p, ncl, rank)) return;
-  const int64_t off = (int64_t)P.chunk * kChunkBytes;
-  const uint32_t nb = (uint32_t)min((int64_t)kChunkBytes, P.bytes - off);
-  mbar_arrive_expect_tx(&S.full[slot], nb);
-  bulk_copy_g2s(&S.ring[slot][0], P.src + off, nb, &S.full[slot], P.policy);
-  ++P.chunk;
+__device__ __forceinline__ void producer_issue(StreamShared& S, const Params& p, int32_t ncl,
+                                               uint32_t rank, int w, uint32_t slot, uint64_t policy) {
+  WarpProducer& P = S.prod[w];
+  if (P.left == 0) {
+    if (P.row >= p.num_rows) return;
+    producer_next_row<CLUSTER>(P, p, ncl, rank, w);
+    if (P.left == 0) return;
+  }
+  const uint32_t nb = (uint32_t)min((int64_t)kChunkBytes, P.left);
+  fence_proxy_async_smem();  // the warp's reads of the slot precede the async-proxy write
+  mbar_arrive_expect_tx(&S.full[w][slot], nb);
+  bulk_copy_g2s(&S.ring[w][slot][0], P.src, nb, &S.full[w][slot], policy);
+  P.src += nb;
+  P.left -= nb;
   ++P.issued;
 }
 
-// Raises the running threshold: the highest bin b >= b0 such that the list
-// holds at least k candidates in bins >= b.  One warp, top-down over the bins
-// between the highest candidate bin and b0.  Counts read while other warps
-// still add to them can only be low, so the bin found never overshoots.
-__device__ __forceinline__ void warp_raise_threshold(StreamShared& S, uint32_t k) {
+// Raises the running threshold (one warp, lock-free): the highest bin b >= b0
+// such that at least k elements counted so far lie in bins >= b.  Counts read
+// while other warps still add to them can only be low, so the bin found never
+// overshoots the k-th largest key.  Also publishes this warp's highest bin.
+__device__ __forceinline__ void warp_raise_threshold(StreamShared& S, uint32_t k, uint32_t mbin) {
   const int lane = threadIdx.x & 31;
-  // one value for the whole warp, so the loop below stays warp-uniform
+  const uint32_t mb = warp_max(mbin);
+  if (lane == 0) atomicMax(&S.top, mb);
+  __syncwarp();
   const int b0 = __shfl_sync(0xFFFFFFFFu, (int)*reinterpret_cast<volatile uint32_t*>(&S.b0), 0);
   const int top = __shfl_sync(0xFFFFFFFFu, (int)*reinterpret_cast<volatile uint32_t*>(&S.top), 0);
   uint32_t acc = 0;
@@ -142,261 +169,326 @@ __device__ __forceinline__ void warp_raise_threshold(StreamShared& S, uint32_t k
   }
 }
 
-__device__ __forceinline__ uint32_t warp_max(uint32_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  return v;
-}
-
-// Element e (0..7) of thread t in a tile: sub-tile e/4 covers tile elements
-// [0, 2048) or [2048, 4096); thread t holds 4 consecutive ones in each.
-__device__ __forceinline__ int32_t tile_offset(int e) {
-  return (e < 4 ? 0 : kThreads * 4) + (int)threadIdx.x * 4 + (e & 3);
-}
-
-// Writes the flagged elements of the tile at list positions count + their
-// ordered rank (sub-tile 0 before sub-tile 1, threads in order).  `ex` is the
-// exclusive packed prefix of this thread, `total` the tile's packed total.
-__device__ __forceinline__ void write_flagged(StreamShared& S, uint32_t fl, const float x[8],
-                                              int32_t tj0, uint32_t count, uint32_t ex,
-                                              uint32_t total) {
-  uint32_t pos0 = count + (ex & 0xFFFFu);
-  uint32_t pos1 = count + (total & 0xFFFFu) + (ex >> 16);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    if (fl & (1u << e)) {
-      const uint32_t pos = e < 4 ? pos0++ : pos1++;
-      S.cand_key[pos] = key_of(x[e]);
-      S.cand_j[pos] = tj0 + tile_offset(e);
+// Appends the lane's flagged elements (bit e of m = element e of the lane's 16
+// in the slot, element order) at list positions pos, pos+1, ... in ascending e.
+// With COUNT, each one is also counted in the level-1 histogram.
+template <bool COUNT>
+__device__ __forceinline__ void append_flagged(StreamShared& S, int w, const float* xs, uint32_t m,
+                                               uint32_t pos, int32_t jb, uint32_t& mbin) {
+  while (m) {
+    const int e = __ffs(m) - 1;
+    m &= m - 1;
+    const uint32_t key = key_of(xs[e]);
+    if (COUNT) {
+      const uint32_t bin = key >> kShift1;
+      atomicAdd(&S.sel.hist1[bin], 1u);
+      mbin = max(mbin, bin);
     }
+    S.list_key[w][pos] = key;
+    S.list_j[w][pos] = jb + e;
+    ++pos;
   }
 }
 
-// The list is full: raise the threshold with the current tile already counted
-// in the histogram, and drop the listed candidates below it (order kept).
-// Returns the new list length and the new threshold key in *K0.
-__device__ __noinline__ uint32_t compact_list(StreamShared& S, uint32_t count, uint32_t k,
-                                              ScanParity& par, uint32_t* K0_out) {
-  if ((threadIdx.x >> 5) == 0) warp_raise_threshold(S, k);
-  __syncthreads();
-  const uint32_t K0 = S.b0 << kShift1;
-  const int tid = threadIdx.x;
+// The warp's list is full: raise the threshold, drop the listed candidates
+// below it (order kept).  Returns the new length and the threshold bin.
+__device__ __noinline__ uint32_t compact_warp_list(StreamShared& S, int w, uint32_t count, uint32_t k,
+                                                   uint32_t mbin, uint32_t* b0_out) {
+  const int lane = threadIdx.x & 31;
+  warp_raise_threshold(S, k, mbin);
+  const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile uint32_t*>(&S.b0), 0);
+  const uint32_t K0 = b0 << kShift1;
   uint32_t kept = 0;
-  for (uint32_t base = 0; base < count; base += kThreads * 4) {
-    const uint32_t e0 = base + tid * 4;
-    uint32_t kk[4];
-    int32_t jj[4];
-    uint32_t keep = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const bool in = e0 + e < count;
-      kk[e] = in ? S.cand_key[e0 + e] : 0u;
-      jj[e] = in ? S.cand_j[e0 + e] : 0;
-      if (in && kk[e] >= K0) keep |= 1u << e;
+  for (uint32_t i0 = 0; i0 < count; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    const bool in = i < count;
+    const uint32_t key = in ? S.list_key[w][i] : 0u;
+    const int32_t j = in ? S.list_j[w][i] : 0;
+    const bool keep = in && key >= K0;
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, keep);
+    const uint32_t dst = kept + __popc(b & lanemask_lt());
+    __syncwarp();
+    if (keep) {
+      S.list_key[w][dst] = key;
+      S.list_j[w][dst] = j;
     }
-    uint32_t tot;
-    uint32_t pos = kept + block_excl_scan(__popc(keep), par.next(S.sel), tot);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (keep & (1u << e)) {
-        S.cand_key[pos] = kk[e];
-        S.cand_j[pos] = jj[e];
-        ++pos;
-      }
-    }
-    kept += tot;
+    kept += __popc(b);
+    __syncwarp();
   }
-  *K0_out = K0;
+  *b0_out = b0;
   return kept;
 }
 
-// Selection on the candidate list and ordered emission (the usual end of a row).
-template <int CLUSTER>
-__device__ __noinline__ void finish_from_list(const Params& p, int64_t row, const int32_t* page_row,
-                                              StreamShared& S, uint32_t count, ScanParity& par) {
-  const CandSrc src{S.cand_key, S.cand_j, (int32_t)(count < (uint32_t)kCap ? count : (uint32_t)kCap)};
-  const Selection sel = select_levels<CLUSTER>(S.sel, src, (uint32_t)p.k, par);
-  emit_selected(src, sel, p.out + row * p.k, (uint32_t)p.k, page_row, p.page_bits, S.sel, par);
+// Bits of the lane's 16 elements (element order) whose window index jb+e lies
+// in [lo, hi).
+__device__ __forceinline__ uint32_t valid16(int32_t jb, int32_t lo, int32_t hi) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) m |= ((jb + e >= lo && jb + e < hi) ? 1u : 0u) << e;
+  return m;
 }
 
-// A row whose candidates did not fit: every pass from global memory.
+// A lane's 16 elements are the 4 consecutive quads 4*lane .. 4*lane+3 of the
+// chunk.  They are read in the rotated order q -> quad 4*lane + ((q + lane/2) & 3)
+// so that the 8 lanes of each shared-memory phase hit 8 different 16-byte bank
+// groups; x[4q+v] therefore holds element 4*((q + lane/2) & 3) + v.  Masks are
+// computed in that "rotated" order and turned into element order by a rotate.
+__device__ __forceinline__ void load16_rotated(const StreamShared& S, int w, uint32_t slot, int lane,
+                                               float x[16]) {
+  const int s = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = S.ring[w][slot][lane * 4 + ((q + s) & 3)];
+    x[4 * q] = v.x;
+    x[4 * q + 1] = v.y;
+    x[4 * q + 2] = v.z;
+    x[4 * q + 3] = v.w;
+  }
+}
+
+__device__ __forceinline__ uint32_t rotated_to_element_order(uint32_t m, int lane) {
+  const uint32_t s4 = 4u * ((lane >> 1) & 3);
+  return ((m << s4) | (m >> (16u - s4))) & 0xFFFFu;
+}
+
+__device__ __forceinline__ uint32_t element_to_rotated_order(uint32_t m, int lane) {
+  const uint32_t s4 = 4u * ((lane >> 1) & 3);
+  return ((m >> s4) | (m << (16u - s4))) & 0xFFFFu;
+}
+
+// Flags (rotated order) of a lane's 16 elements: bit i set when x[i] >= th.
+__device__ __forceinline__ uint32_t flags16(const float x[16], float th) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m |= (x[i] >= th ? 1u : 0u) << i;
+  return m;
+}
+
+// Histogram of a source made of the warps' lists (refinement levels).
+struct ListSrc {
+  const StreamShared* S;
+  __device__ __forceinline__ void histogram(uint32_t* hist, uint32_t M, uint32_t T, int shift,
+                                            uint32_t nbins_mask) const {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t n = S->count[w];
+    for (uint32_t i = lane; i < n; i += 32) {
+      const uint32_t key = S->list_key[w][i];
+      if ((key & M) == T) atomicAdd(hist + ((key >> shift) & nbins_mask), 1u);
+    }
+  }
+};
+
+// Ordered emission from the lists: warp w's selected entries follow those of
+// warps 0..w-1 (their slices precede w's in the window).
+__device__ __forceinline__ void emit_from_lists(StreamShared& S, const Selection& sel, int32_t* out_row,
+                                                uint32_t k_row, const int32_t* page_row,
+                                                int32_t page_bits) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t n = S.count[w];
+  uint32_t ngt = 0, neq = 0;
+  for (uint32_t i = lane; i < n; i += 32) {
+    const uint32_t pk = S.list_key[w][i] & sel.M;
+    ngt += pk > sel.T;
+    neq += pk == sel.T;
+  }
+  ngt = warp_sum(ngt);
+  neq = warp_sum(neq);
+  if (lane == 0) {
+    S.wgt[w] = ngt;
+    S.weq[w] = neq;
+  }
+  __syncthreads();
+  const uint32_t gv = S.wgt[lane], ev = S.weq[lane];
+  const uint32_t gi = warp_incl_scan(gv), ei = warp_incl_scan(ev);
+  const uint32_t gt_before = __shfl_sync(0xFFFFFFFFu, gi - gv, w);
+  const uint32_t eq_before = __shfl_sync(0xFFFFFFFFu, ei - ev, w);
+  const uint32_t lt = lanemask_lt();
+  uint32_t g = gt_before, q = eq_before;
+  for (uint32_t i0 = 0; i0 < n; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    const bool in = i < n;
+    const uint32_t pk = in ? (S.list_key[w][i] & sel.M) : 0u;
+    const bool is_gt = in && pk > sel.T;
+    const bool is_eq = in && pk == sel.T;
+    const uint32_t bg = __ballot_sync(0xFFFFFFFFu, is_gt), be = __ballot_sync(0xFFFFFFFFu, is_eq);
+    const uint32_t gl = g + __popc(bg & lt), ql = q + __popc(be & lt);
+    if (is_gt || (is_eq && ql < sel.quota)) {
+      const uint32_t pos = sel.off + gl + (ql < sel.quota ? ql : sel.quota);
+      if (pos < k_row)
+        out_row[pos] = page_slot(page_row, page_bits, S.list_j[w][i]);
+      else
+        atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
+    }
+    g += __popc(bg);
+    q += __popc(be);
+  }
+}
+
+template <int CLUSTER>
+__device__ __noinline__ void finish_from_lists(const Params& p, int64_t row, const int32_t* page_row,
+                                               StreamShared& S, ScanParity& par) {
+  const ListSrc src{&S};
+  const Selection sel = select_levels<CLUSTER, kStreamThreads>(S.sel, src, (uint32_t)p.k, par);
+  emit_from_lists(S, sel, p.out + row * p.k, (uint32_t)p.k, page_row, p.page_bits);
+}
+
 template <int CLUSTER>
 __device__ __noinline__ void finish_from_global(const Params& p, int64_t row, const Row& r,
                                                 const Part& part, SelectShared& S, ScanParity& par) {
-  select_from_global<CLUSTER>(p, (int32_t)row, r, part, S, par);
+  select_from_global<CLUSTER, kStreamThreads>(p, (int32_t)row, r, part, S, par);
 }
 
 template <int CLUSTER>
-__global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(Params p) {
+__global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   StreamShared& S = *reinterpret_cast<StreamShared*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0u;
   const int32_t cid = (int32_t)(blockIdx.x / CLUSTER), ncl = (int32_t)(gridDim.x / CLUSTER);
   const uint32_t k = (uint32_t)p.k;
+  const uint64_t policy = l2_evict_first_policy();
 
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&S.full[s], 1);
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&S.full[w][s], 1);
     fence_barrier_init();
+    WarpProducer& P = S.prod[w];
+    P.row = (int64_t)cid - ncl;
+    P.left = 0;
+    P.src = nullptr;
+    P.issued = 0;
+    for (uint32_t s = 0; s < (uint32_t)kStages; ++s) producer_issue<CLUSTER>(S, p, ncl, rank, w, s, policy);
   }
   __syncthreads();
   if constexpr (CLUSTER > 1) cluster_sync_all();
 
-  if (tid == 0) {
-    producer_start(S.prod, cid, ncl);
-    for (uint32_t s = 0; s < (uint32_t)kStages; ++s) producer_issue<CLUSTER>(S, p, ncl, rank, s);
-  }
-
   ScanParity par;
-  uint32_t g = 0, wtpar = 0;
+  uint32_t g = 0;  // chunks this warp consumed
   bool timed_out = false;
 
   for (int64_t row = cid; row < p.num_rows; row += ncl) {
     const Row r = load_row(p, (int32_t)row);
     if (row_is_whole(r, p.k)) {
-      emit_whole_window(p, (int32_t)row, r, rank, (uint32_t)CLUSTER);
+      emit_whole_window<kStreamThreads>(p, (int32_t)row, r, rank, (uint32_t)CLUSTER);
       continue;
     }
     const Part part = part_of(r, rank, (uint32_t)CLUSTER);
-    const int64_t bytes = (part.q1 - part.q0) * 16;
-    const int32_t nchunks = (int32_t)((bytes + kChunkBytes - 1) / kChunkBytes);
+    const Slice sl = slice_of(r, part, w);
+    const int32_t nch = (int32_t)(((sl.q1 - sl.q0) * 16 + kChunkBytes - 1) / kChunkBytes);
 
-    for (int b = tid; b < kBins1; b += kThreads) S.sel.hist1[b] = 0u;
+    for (int b = tid; b < kBins1; b += kStreamThreads) S.sel.hist1[b] = 0u;
     if (tid == 0) {
       S.b0 = 0u;
       S.top = 0u;
+      S.overflow = 0u;
     }
     __syncthreads();
-    uint32_t count = 0;
-    bool overflow = false;
 
-    for (int32_t c = 0; c < nchunks; ++c) {
-      const uint32_t slot = g % kStages, parity = (g / kStages) & 1u;
+    uint32_t count = 0, mbin = 0;
+    bool over = false;
+
+    // ---- chunk 0 of every warp: histogram only, then one block-wide pick of
+    // the first threshold, then the chunk's survivors go to the lists.
+    uint32_t slot = 0, m = 0;
+    int32_t jb = 0;
+    float x[16];
+    if (nch > 0) {
+      slot = g % kStages;
+      if (!timed_out && !mbar_wait_bounded(&S.full[w][slot], (g / kStages) & 1u)) timed_out = true;
       ++g;
-      // After one wait has given up, wait no more: the kernel only finishes its
-      // control flow (results unspecified, diagnostic bit set).
-      if (!timed_out && !mbar_wait_bounded(&S.full[slot], parity)) timed_out = true;
-      const int32_t tj0 = (int32_t)((part.q0 + (int64_t)c * (kChunkFloats / 4)) * 4 - r.head);
-
-      if (overflow) {  // the row already goes to the fallback: only keep the ring moving
-        __syncthreads();
-        if (tid == 0) producer_issue<CLUSTER>(S, p, ncl, rank, slot);
-        continue;
-      }
-
-      const float4 va = S.ring[slot][tid], vb = S.ring[slot][kThreads + tid];
-      const float x[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-      uint32_t validm = 0xFFu;
-      if (!(tj0 >= part.lo && tj0 + kChunkFloats <= part.hi)) {
-        validm = 0u;
+      load16_rotated(S, w, slot, lane, x);
+      jb = (int32_t)(sl.q0 * 4 - r.head) + 16 * lane;
+      m = element_to_rotated_order(valid16(jb, sl.lo, sl.hi), lane);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int32_t j = tj0 + tile_offset(e);
-          if (j >= part.lo && j < part.hi) validm |= 1u << e;
+      for (int i = 0; i < 16; ++i) {
+        if (m & (1u << i)) {
+          const uint32_t bin = key_of(x[i]) >> kShift1;
+          atomicAdd(&S.sel.hist1[bin], 1u);
+          mbin = max(mbin, bin);
         }
-      }
-
-      if (c == 0) {
-        // First tile of the row: histogram every element, pick the bin of the
-        // k-th largest among them, keep only what reaches that bin.
-        uint32_t maxbin = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (validm & (1u << e)) {
-            const uint32_t bin = key_of(x[e]) >> kShift1;
-            atomicAdd(&S.sel.hist1[bin], 1u);
-            maxbin = max(maxbin, bin);
-          }
-        }
-        const uint32_t mb = warp_max(maxbin);
-        if (lane == 0 && mb > 0) atomicMax(&S.top, mb);
-        __syncthreads();
-        if (tid == 0) producer_issue<CLUSTER>(S, p, ncl, rank, slot);
-        const int32_t nvalid = max(0, min(part.hi, tj0 + kChunkFloats) - max(part.lo, tj0));
-        uint32_t b0 = 0;
-        if ((uint32_t)nvalid >= k) {
-          const Pick pk = block_pick<kBins1, 1>(S.sel.hist1, k, par.next(S.sel), par.next_pick(S.sel));
-          b0 = pk.bin;
-          if (tid == 0) S.b0 = b0;
-        }
-        const uint32_t K0 = b0 << kShift1;
-        uint32_t fl = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if ((validm & (1u << e)) && key_of(x[e]) >= K0) fl |= 1u << e;
-        const uint32_t packed = __popc(fl & 0xFu) | ((uint32_t)__popc(fl >> 4) << 16);
-        uint32_t total;
-        const uint32_t ex = block_excl_scan(packed, par.next(S.sel), total);
-        write_flagged(S, fl, x, tj0, 0u, ex, total);
-        count = (total & 0xFFFFu) + (total >> 16);
-        continue;
-      }
-
-      const float th = edge_float(*reinterpret_cast<volatile uint32_t*>(&S.b0));
-      uint32_t fl = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (x[e] >= th) fl |= 1u << e;
-      fl &= validm;
-      const uint32_t packed = __popc(fl & 0xFu) | ((uint32_t)__popc(fl >> 4) << 16);
-      uint32_t maxbin = 0;
-      if (fl) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (fl & (1u << e)) {
-            const uint32_t bin = key_of(x[e]) >> kShift1;
-            atomicAdd(&S.sel.hist1[bin], 1u);
-            maxbin = max(maxbin, bin);
-          }
-        }
-      }
-      const uint32_t incl = warp_incl_scan(packed);
-      uint32_t* wt = S.wt[wtpar];
-      wtpar ^= 1u;
-      if (lane == 31) wt[warp] = incl;
-      const uint32_t mb = warp_max(maxbin);
-      if (lane == 0 && mb > 0) atomicMax(&S.top, mb);
-      __syncthreads();
-      if (tid == 0) producer_issue<CLUSTER>(S, p, ncl, rank, slot);
-      const uint32_t w = lane < kWarps ? wt[lane] : 0u;
-      const uint32_t wincl = warp_incl_scan(w);
-      const uint32_t wbase = __shfl_sync(0xFFFFFFFFu, wincl - w, warp);
-      const uint32_t total = __shfl_sync(0xFFFFFFFFu, wincl, kWarps - 1);
-      const uint32_t tcount = (total & 0xFFFFu) + (total >> 16);
-
-      if (count + tcount <= (uint32_t)kCap) {
-        write_flagged(S, fl, x, tj0, count, wbase + incl - packed, total);
-        count += tcount;
-        if (warp == (c & (kWarps - 1))) warp_raise_threshold(S, k);
-        continue;
-      }
-
-      // The list is full: raise the threshold with this tile counted, drop the
-      // listed candidates below it (order kept), then add the tile's survivors.
-      uint32_t K0;
-      const uint32_t kept = compact_list(S, count, k, par, &K0);
-      uint32_t fl2 = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if ((fl & (1u << e)) && key_of(x[e]) >= K0) fl2 |= 1u << e;
-      uint32_t total2;
-      const uint32_t ex2 = block_excl_scan(__popc(fl2 & 0xFu) | ((uint32_t)__popc(fl2 >> 4) << 16),
-                                           par.next(S.sel), total2);
-      const uint32_t t2 = (total2 & 0xFFFFu) + (total2 >> 16);
-      if (kept + t2 <= (uint32_t)kCap) {
-        write_flagged(S, fl2, x, tj0, kept, ex2, total2);
-        count = kept + t2;
-      } else {
-        overflow = true;
-        count = kept;
       }
     }
-
-    // ---- end of the row's stream: select on the list (or fall back) ----
+    {
+      const uint32_t mb = warp_max(mbin);
+      if (lane == 0) atomicMax(&S.top, mb);
+    }
     __syncthreads();
-    bool any_over = overflow;
+    // Pick{0,...} (threshold -inf) when the first chunks hold fewer than k elements
+    const Pick pk0 = block_pick<kBins1, 1, kStreamThreads>(S.sel.hist1, k, par.next(S.sel),
+                                                           par.next_pick(S.sel));
+    if (tid == 0) S.b0 = pk0.bin;
+    if (nch > 0) {
+      const uint32_t K0 = pk0.bin << kShift1;
+      uint32_t f = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f |= ((m & (1u << i)) && key_of(x[i]) >= K0 ? 1u : 0u) << i;
+      f = rotated_to_element_order(f, lane);
+      const uint32_t cnt = __popc(f);
+      const uint32_t incl = warp_incl_scan(cnt);
+      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      if (total <= (uint32_t)kWarpCap) {
+        append_flagged<false>(S, w, reinterpret_cast<const float*>(&S.ring[w][slot][lane * 4]), f,
+                              incl - cnt, jb, mbin);
+        count = total;
+      } else {
+        over = true;  // more than kWarpCap of 512 elements reach the first threshold
+        if (lane == 0) S.overflow = 1u;
+      }
+      __syncwarp();
+      if (lane == 0) producer_issue<CLUSTER>(S, p, ncl, rank, w, slot, policy);
+    }
+
+    // ---- the rest of the slice: one compare per element against the running
+    // threshold; survivors appended in order; no block-wide synchronisation.
+    for (int32_t c = 1; c < nch; ++c) {
+      slot = g % kStages;
+      if (!timed_out && !mbar_wait_bounded(&S.full[w][slot], (g / kStages) & 1u)) timed_out = true;
+      ++g;
+      load16_rotated(S, w, slot, lane, x);
+      jb = (int32_t)((sl.q0 + (int64_t)c * kChunkQuads) * 4 - r.head) + 16 * lane;
+      if (!over) {
+        const float th = edge_float(max(*reinterpret_cast<volatile uint32_t*>(&S.b0), pk0.bin));
+        m = rotated_to_element_order(flags16(x, th), lane);
+        if (c == nch - 1) m &= valid16(jb, sl.lo, sl.hi);
+        uint32_t cnt = __popc(m);
+        uint32_t incl = warp_incl_scan(cnt);
+        uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const float* xs = reinterpret_cast<const float*>(&S.ring[w][slot][lane * 4]);
+        if (total != 0) {
+          if (count + total > (uint32_t)kWarpCap) {
+            uint32_t b0;
+            count = compact_warp_list(S, w, count, k, mbin, &b0);
+            const float th2 = edge_float(b0);
+            uint32_t m2 = 0;
+            for (uint32_t mm = m; mm; mm &= mm - 1) {
+              const int e = __ffs(mm) - 1;
+              if (xs[e] >= th2) m2 |= 1u << e;
+            }
+            m = m2;
+            cnt = __popc(m);
+            incl = warp_incl_scan(cnt);
+            total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            if (count + total > (uint32_t)kWarpCap) {
+              over = true;
+              if (lane == 0) S.overflow = 1u;
+            }
+          }
+          if (!over) {
+            append_flagged<true>(S, w, xs, m, count + incl - cnt, jb, mbin);
+            count += total;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) producer_issue<CLUSTER>(S, p, ncl, rank, w, slot, policy);
+      if (!over && (c <= 3 || (c & 3) == 0)) warp_raise_threshold(S, k, mbin);
+    }
+    if (lane == 0) S.count[w] = over ? 0u : count;
+
+    // ---- end of the row's stream: select on the lists (or fall back) ----
+    __syncthreads();
+    bool any_over = S.overflow != 0u;
     if constexpr (CLUSTER > 1) {
-      if (tid == 0) S.sel.pub_overflow = overflow ? 1u : 0u;
+      if (tid == 0) S.sel.pub_overflow = S.overflow;
       cluster_sync_all();
       const uint32_t a = smem_addr(&S.sel.pub_overflow);
       uint32_t o = 0;
@@ -406,17 +498,17 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(Params p) {
     if (any_over)
       finish_from_global<CLUSTER>(p, row, r, part, S.sel, par);
     else
-      finish_from_list<CLUSTER>(p, row, r.page_row, S, count, par);
+      finish_from_lists<CLUSTER>(p, row, r.page_row, S, par);
   }
 
   // Every issued chunk was waited for, so nothing is in flight -- unless a
   // wait gave up; then wait (bounded) for the copies still outstanding.
   if (__syncthreads_or(timed_out ? 1 : 0)) {
-    if (tid == 0) {
+    if (lane == 0) {
       atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
-      const uint32_t issued = S.prod.issued;
+      const uint32_t issued = S.prod[w].issued;
       for (uint32_t n = (issued > (uint32_t)kStages ? issued - kStages : 0u); n < issued; ++n)
-        mbar_wait_bounded(&S.full[n % kStages], (n / kStages) & 1u);
+        mbar_wait_bounded(&S.full[w][n % kStages], (n / kStages) & 1u);
     }
     __syncthreads();
   }

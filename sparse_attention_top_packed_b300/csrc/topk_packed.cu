@@ -42,11 +42,11 @@ cudaError_t prepare_stream(int& occupancy_or_clusters, int sms) {
   if (e != cudaSuccess) return e;
   if constexpr (C == 1) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy_or_clusters,
-                                                         topk::topk_stream_kernel<1>, topk::kThreads, smem);
+                                                         topk::topk_stream_kernel<1>, topk::kStreamThreads, smem);
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(C * sms), 1, 1);
-    cfg.blockDim = dim3(topk::kThreads, 1, 1);
+    cfg.blockDim = dim3(topk::kStreamThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -77,7 +77,7 @@ void init_device(int dev) {
                            (int)mp_smem);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.multipass_ctas_per_sm, topk::topk_multipass_kernel,
-                                                      topk::kThreads, mp_smem);
+                                                      topk::kMultipassThreads, mp_smem);
   if (e == cudaSuccess) e = prepare_stream<1>(d.stream_ctas_per_sm, d.sms);
   if (e == cudaSuccess) e = prepare_stream<2>(d.stream_clusters[1], d.sms);
   if (e == cudaSuccess) e = prepare_stream<4>(d.stream_clusters[2], d.sms);
@@ -168,7 +168,7 @@ template <int C>
 cudaError_t launch_stream(const Params& prm, int64_t grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(topk::kThreads, 1, 1);
+  cfg.blockDim = dim3(topk::kStreamThreads, 1, 1);
   cfg.dynamicSmemBytes = sizeof(topk::StreamShared);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -216,12 +216,12 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl.path == TOPK_PATH_MULTIPASS) {
-    topk::topk_multipass_kernel<<<(unsigned)pl.grid, topk::kThreads, sizeof(topk::SelectShared), s>>>(prm);
+    topk::topk_multipass_kernel<<<(unsigned)pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), s>>>(prm);
     e = cudaGetLastError();
   } else {
     switch (pl.cluster) {
       case 1:
-        topk::topk_stream_kernel<1><<<(unsigned)pl.grid, topk::kThreads, sizeof(topk::StreamShared), s>>>(prm);
+        topk::topk_stream_kernel<1><<<(unsigned)pl.grid, topk::kStreamThreads, sizeof(topk::StreamShared), s>>>(prm);
         e = cudaGetLastError();
         break;
       case 2: e = launch_stream<2>(prm, pl.grid, s); break;
@@ -254,7 +254,8 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
   if (path) *path = pl.path;
   if (cluster_size) *cluster_size = pl.cluster;
   if (grid_ctas) *grid_ctas = (int32_t)pl.grid;
-  if (threads_per_cta) *threads_per_cta = topk::kThreads;
+  if (threads_per_cta)
+    *threads_per_cta = pl.path == TOPK_PATH_MULTIPASS ? topk::kMultipassThreads : topk::kStreamThreads;
   return TOPK_OK;
 }
 

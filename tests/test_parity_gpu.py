@@ -167,7 +167,7 @@ def test_zero_rows_launches_nothing(cuda_device):
 def test_plan_reports_the_launch(cuda_device):
     plan = binding.topk_packed_plan(140000, 2048, 4096)
     assert plan["path"] == binding.PATHS["stream"]
-    assert plan["threads_per_cta"] == 512
+    assert plan["threads_per_cta"] == 1024
     assert plan["grid_ctas"] % plan["cluster_size"] == 0
     mp = binding.topk_packed_plan(140000, 2048, 4096, path="multipass")
     assert mp["path"] == binding.PATHS["multipass"]
