@@ -146,10 +146,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_workload(name: str, device):
+def make_workload(name: str, device, rows: int = 0):
     from sparse_attention_top_packed_b300 import workloads
 
-    return workloads.named(name, device=device)
+    w = workloads.named(name, device=device)
+    return w.head(rows) if rows else w
 
 
 def l2_flush_buffer(device):
@@ -179,7 +180,7 @@ def run_ours(a, rank: int, world: int, device) -> dict:
     from sparse_attention_top_packed_b300 import binding
 
     torch.cuda.set_device(device)
-    w = make_workload(a.workload, device)
+    w = make_workload(a.workload, device, a.rows)
     torch.cuda.synchronize(device)
     alg_bytes = w.algorithmic_bytes()
     big = w.window_bytes() > 4 * L2_BYTES
@@ -311,7 +312,7 @@ def run_reference(a, rank: int, world: int) -> None:
     from sparse_attention_top_packed_b300.workloads import gather_windows, sample_rows
 
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    w = make_workload(a.workload, device)
+    w = make_workload(a.workload, device, a.rows)
     cores = default_threads()
     rows_per_step = max(1, min(w.num_rows, cores))
     steps = []
@@ -370,6 +371,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="keep only the first N rows of the workload (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
     if a.warmup < 3:

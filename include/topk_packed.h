@@ -97,16 +97,18 @@ TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, cons
 
 /* Kernel families behind topk_packed_ex. */
 typedef enum {
-  TOPK_PATH_AUTO = 0,      /* what topk_packed uses */
+  TOPK_PATH_AUTO = 0,      /* what topk_packed uses (currently TOPK_PATH_PIPE) */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
-  TOPK_PATH_STREAM = 2     /* persistent CTAs (or clusters): TMA ring + running threshold */
+  TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
+  TOPK_PATH_PIPE = 3       /* persistent CTAs, two per SM: one TMA ring per CTA, candidate buffer
+                              with a threshold carried from row to row, bitmap-ordered emission */
 } topk_path_t;
 
 /* Launch choices; zero fields mean "choose automatically". */
 typedef struct {
   int32_t path;         /* topk_path_t */
   int32_t cluster_size; /* STREAM: CTAs that share one row (1, 2, 4 or 8); 0 = auto */
-  int32_t max_ctas;     /* STREAM: upper bound on the persistent grid; 0 = auto */
+  int32_t max_ctas;     /* STREAM, PIPE, MULTIPASS: upper bound on the grid; 0 = auto */
 } topk_launch_config_t;
 
 /*

@@ -62,15 +62,21 @@ __device__ __forceinline__ uint32_t key_of(float x) {
   return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
-// The float whose key is the lower edge of level-1 bin b, so that for every
-// non-NaN x:  x >= edge_float(b)  <=>  key(x) >= (b << 20).  Bin 0 starts at
-// key 0, below every non-NaN key: its edge is -inf.
-__device__ __forceinline__ float edge_float(uint32_t b) {
-  const uint32_t key = b << kShift1;
-  if (b == 0) return __uint_as_float(0xFF800000u);
+// A float f with, for every non-NaN x:  x >= f  <=>  key(x) >= key.
+// The smallest non-NaN key is key(-inf) = 0x007FFFFF; every key at or below
+// it maps to -inf (decoding those bit patterns would give a NaN, which no x
+// reaches).  Above it the decoded float is exact: key 0x7FFFFFFF (no float
+// has it, -0.0 being folded into +0.0) decodes to -0.0, and x >= -0.0 holds
+// exactly for the x whose key is at least key(+0.0) = 0x80000000.
+__device__ __forceinline__ float key_floor_float(uint32_t key) {
+  if (key <= 0x007FFFFFu) return __uint_as_float(0xFF800000u);
   const uint32_t u = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
   return __uint_as_float(u);
 }
+
+// The float at the lower edge of level-1 bin b:
+//   x >= edge_float(b)  <=>  key(x) >= (b << 20)   for every non-NaN x.
+__device__ __forceinline__ float edge_float(uint32_t b) { return key_floor_float(b << kShift1); }
 
 // ---------------------------------------------------------------------------
 // Row addressing (section 1 and section 2 of the page).  The window start is
@@ -186,6 +192,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
                ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// Plain arrival (release): the caller's earlier shared-memory reads of the
+// guarded data are done before the phase can complete.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {

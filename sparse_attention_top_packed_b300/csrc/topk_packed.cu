@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "topk_kernels.cuh"
+#include "topk_pipe.cuh"
 #include "topk_packed.h"
 
 namespace {
@@ -28,6 +29,7 @@ struct DeviceInfo {
   int stream_ctas_per_sm = 0;     // resident stream CTAs per SM (cluster size 1)
   int stream_clusters[4] = {};    // max resident clusters for sizes 2, 4, 8 (index 1..3)
   int multipass_ctas_per_sm = 0;
+  int pipe_ctas_per_sm = 0;
   cudaError_t error = cudaSuccess;
 };
 
@@ -78,6 +80,13 @@ void init_device(int dev) {
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.multipass_ctas_per_sm, topk::topk_multipass_kernel,
                                                       topk::kMultipassThreads, mp_smem);
+  const size_t pipe_smem = sizeof(topk::pipe::Shared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(topk::pipe::topk_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pipe_smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.pipe_ctas_per_sm, topk::pipe::topk_pipe_kernel,
+                                                      topk::pipe::kThreads, pipe_smem);
   if (e == cudaSuccess) e = prepare_stream<1>(d.stream_ctas_per_sm, d.sms);
   if (e == cudaSuccess) e = prepare_stream<2>(d.stream_clusters[1], d.sms);
   if (e == cudaSuccess) e = prepare_stream<4>(d.stream_clusters[2], d.sms);
@@ -86,7 +95,7 @@ void init_device(int dev) {
     d.error = e;
     return;
   }
-  d.ok = d.multipass_ctas_per_sm > 0 && d.stream_ctas_per_sm > 0;
+  d.ok = d.multipass_ctas_per_sm > 0 && d.stream_ctas_per_sm > 0 && d.pipe_ctas_per_sm > 0;
   if (!d.ok) d.error = cudaErrorInvalidConfiguration;
 }
 
@@ -122,7 +131,7 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
   if (num_rows < 0 || k <= 0 || row_stride < 0 || pt_stride < 0) return TOPK_ERR_INVALID_ARG;
   if (page_size <= 0 || (page_size & (page_size - 1)) != 0) return TOPK_ERR_INVALID_ARG;
   if (cfg) {
-    if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_STREAM) return TOPK_ERR_INVALID_ARG;
+    if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_PIPE) return TOPK_ERR_INVALID_ARG;
     const int c = cfg->cluster_size;
     if (!(c == 0 || c == 1 || c == 2 || c == 4 || c == 8)) return TOPK_ERR_INVALID_ARG;
     if (cfg->max_ctas < 0) return TOPK_ERR_INVALID_ARG;
@@ -139,8 +148,14 @@ Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t num_rows,
   (void)row_stride;
   Plan pl;
   const int32_t want = cfg ? cfg->path : TOPK_PATH_AUTO;
-  pl.path = want == TOPK_PATH_AUTO ? TOPK_PATH_STREAM : want;
+  pl.path = want == TOPK_PATH_AUTO ? TOPK_PATH_PIPE : want;
   pl.cluster = 1;
+  if (pl.path == TOPK_PATH_PIPE) {
+    const int64_t cap = (int64_t)d.sms * d.pipe_ctas_per_sm;
+    pl.grid = num_rows < cap ? num_rows : cap;
+    if (cfg && cfg->max_ctas > 0 && pl.grid > cfg->max_ctas) pl.grid = cfg->max_ctas;
+    return pl;
+  }
   if (pl.path == TOPK_PATH_MULTIPASS) {
     const int64_t cap = (int64_t)d.sms * d.multipass_ctas_per_sm * 8;
     pl.grid = num_rows < cap ? num_rows : cap;
@@ -181,6 +196,8 @@ cudaError_t launch_stream(const Params& prm, int64_t grid, cudaStream_t stream) 
   return cudaLaunchKernelEx(&cfg, topk::topk_stream_kernel<C>, prm);
 }
 
+static_assert(topk::pipe::kKMax == TOPK_K_MAX, "the pipelined kernel is sized for TOPK_K_MAX");
+
 }  // namespace
 
 extern "C" {
@@ -215,7 +232,10 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   const Plan pl = make_plan(*d, row_stride, num_rows, config);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (pl.path == TOPK_PATH_MULTIPASS) {
+  if (pl.path == TOPK_PATH_PIPE) {
+    topk::pipe::topk_pipe_kernel<<<(unsigned)pl.grid, topk::pipe::kThreads, sizeof(topk::pipe::Shared), s>>>(prm);
+    e = cudaGetLastError();
+  } else if (pl.path == TOPK_PATH_MULTIPASS) {
     topk::topk_multipass_kernel<<<(unsigned)pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), s>>>(prm);
     e = cudaGetLastError();
   } else {
@@ -255,7 +275,9 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
   if (cluster_size) *cluster_size = pl.cluster;
   if (grid_ctas) *grid_ctas = (int32_t)pl.grid;
   if (threads_per_cta)
-    *threads_per_cta = pl.path == TOPK_PATH_MULTIPASS ? topk::kMultipassThreads : topk::kStreamThreads;
+    *threads_per_cta = pl.path == TOPK_PATH_PIPE        ? topk::pipe::kThreads
+                       : pl.path == TOPK_PATH_MULTIPASS ? topk::kMultipassThreads
+                                                        : topk::kStreamThreads;
   return TOPK_OK;
 }
 

@@ -1,0 +1,681 @@
+// Pipelined single-pass kernel of the packed top-k + page transform (sm_103a).
+//
+// Operation (page "[sglang] [AMD ROCm] GLM-5.x Prefill 성능을 66% 끌어올린 Top-K 커널
+// 최적화 분석", sglang PR #37889, Intro and sections 1-2): row i's window is
+//   scores[i * row_stride + row_starts[i] + j], 0 <= j < seq_lens[i];
+// the k largest are kept (a tie goes to the lower j), listed in ascending j and
+// mapped through the row's page-table row; -1 pads windows shorter than k.
+//
+// Design (one CTA per row at a time, two CTAs per SM, rows strided over the
+// persistent grid):
+//
+//  * Load.  The CTA's windows, row after row, stream through a ring of
+//    kStages shared-memory stages filled by 1-D TMA bulk copies (8 KB each,
+//    L2 evict-first: every byte is read once).  A window is copied from its
+//    start rounded down to 16 bytes; lanes before the start and past the end
+//    are masked in registers (section 2 of the page, without writing the
+//    buffer).  Each stage has a "full" barrier (the copy landed) and an
+//    "empty" barrier (all 8 warps took the chunk into registers).  Thread 0,
+//    after taking chunk g, refills the stage of chunk g-1 with chunk
+//    g + kStages - 1, which may belong to a later row: the next row's first
+//    chunks are in flight while a row is finished.
+//
+//  * Admission.  Each thread takes 8 floats of a chunk and keeps those at or
+//    above the admission threshold, a lower bound on the row's k-th largest
+//    key: one float compare per element.  Kept elements (order-preserving
+//    key, window index) go to one candidate buffer of kCap entries, at
+//    positions reserved by one shared-memory atomic per warp, and are counted
+//    in a 4096-bin histogram of the key's top 12 bits.
+//
+//  * Threshold.  When the CTA's previous row gives a hint -- the key prefix
+//    that about 1.25 k of its candidates reach, scaled to the new row's
+//    length -- the row streams with that fixed threshold and no block-wide
+//    synchronisation ("fast" mode).  If that admits fewer than k elements or
+//    overflows the buffer, the row is streamed again from global memory in
+//    "exact" mode.  Without a hint (first row of a CTA, a much shorter row)
+//    the row streams in exact mode from the ring: the threshold starts at
+//    -inf and, whenever the buffer would overflow, rises to the histogram bin
+//    of the k-th largest buffered key, or to the exact k-th largest (key,
+//    index) pair.  Any threshold at or below the k-th largest key of the
+//    elements seen so far is safe, so no selected element is ever dropped.
+//
+//  * Selection.  A radix select on the buffer orders candidates by the
+//    64-bit pair (key, ~j): larger key first, then lower j.  Level 1 uses the
+//    histogram kept while streaming; levels 2-3 refine the key (10 bits each);
+//    levels 4-6 (only for equal keys) refine ~j.  Pairs are unique, so the
+//    result is exactly k candidates, whatever the ties.
+//
+//  * Emission.  The selected window indices are set in a bitmap of the window
+//    (reusing the histogram's shared memory, 131072 indices per segment); a
+//    block scan of the word popcounts puts the indices, in ascending j, into a
+//    staging row; then every thread maps k / 256 of them through the page
+//    transform of section 1 (independent loads) and the row leaves with
+//    coalesced stores.
+#pragma once
+
+#include "topk_device.cuh"
+
+namespace topk {
+namespace pipe {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunkBytes = 8192;
+constexpr int kChunkQuads = kChunkBytes / 16;  // 512
+constexpr int kChunkElems = kChunkBytes / 4;   // 2048
+constexpr int kStages = 6;
+constexpr int kAhead = kStages - 1;            // chunks in flight ahead of the one being taken
+constexpr int kKMax = 2048;
+constexpr int kCap = 4096;                 // candidate buffer entries
+constexpr int kBins1 = 4096;               // key bits [20, 32)
+constexpr int kBins2 = 2048;               // refinement levels (<= 11 bits)
+constexpr int kSegBits = kBins1 * 32;      // bitmap indices per emission segment
+constexpr uint32_t kMaskBin = 0xFFF00000u;  // key bits of a level-1 bin
+constexpr uint32_t kMaskSub = 0xFFFFFC00u;  // key bits of a level-2 sub-bin
+
+static_assert(kChunkQuads == 2 * kThreads, "each thread takes two quads of a chunk");
+// After an exact compaction the buffer holds k entries; a whole chunk must fit.
+static_assert(kCap - kKMax >= kChunkElems, "candidate buffer too small for k + one chunk");
+static_assert(kBins2 >= kKMax, "the output staging row reuses the level-2 histogram");
+
+// Admission / selection rule on the pair (key, nj = ~j): an element passes
+// iff (key & mk, nj & mj) >= (tk, tj) lexicographically.  tf is a float with
+// x >= tf <=> key(x) >= tk (tk has no bits outside mk), the fast first test.
+struct Rule {
+  uint32_t mk, tk, mj, tj;
+  float tf;
+  uint32_t exact;  // the pair test can reject an element that passed x >= tf
+};
+
+__device__ __forceinline__ Rule rule_prefix(uint32_t mk, uint32_t tk) {
+  Rule a;
+  a.mk = mk; a.tk = tk & mk; a.mj = 0u; a.tj = 0u;
+  a.tf = key_floor_float(a.tk);
+  a.exact = 0u;
+  return a;
+}
+
+__device__ __forceinline__ Rule rule_all() { return rule_prefix(0u, 0u); }
+
+__device__ __forceinline__ Rule rule_bin(uint32_t bin) { return rule_prefix(kMaskBin, bin << 20); }
+
+__device__ __forceinline__ bool rule_pass(const Rule& a, uint32_t key, int32_t j) {
+  const uint32_t kk = key & a.mk;
+  return kk > a.tk || (kk == a.tk && ((~(uint32_t)j) & a.mj) >= a.tj);
+}
+
+// Lowest level-1 bin that can hold an admitted key under rule a.
+__device__ __forceinline__ uint32_t rule_low_bin(const Rule& a) { return (a.mk & kMaskBin) ? a.tk >> 20 : 0u; }
+
+struct PickOut {
+  uint32_t bin, above, count;  // first target: bin holding rank r, count above it, its count
+  uint32_t bin2, has2;         // second target (optional)
+  uint32_t total;
+};
+
+struct Shared {
+  float4 ring[kStages][kChunkQuads];
+  uint32_t bkey[kCap];
+  int32_t bj[kCap];
+  uint32_t hist1[kBins1];  // also the emission bitmap
+  uint32_t hist2[kBins2];  // also the output staging row
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint32_t scratch[2][kWarps];
+  PickOut pick[2];
+  uint32_t wtot[kWarps];
+  uint32_t count;
+  uint32_t overflow;  // fast mode: a reservation did not fit
+  Rule rule;          // admission rule of the current row
+  Rule hint;          // admission rule proposed for the next row
+  uint32_t hint_valid;
+  uint32_t hint_rank;  // rank the next row's hint should reach in this row (0: none)
+  int32_t next_len;    // window length of the CTA's next row that needs a selection
+  uint32_t pad_;
+};
+
+// Thread 0's cursor over the CTA's chunk sequence: the windows of rows
+// blockIdx.x, blockIdx.x + gridDim.x, ... (rows with seq_len <= k have none),
+// each cut into kChunkBytes pieces.
+struct Cursor {
+  const char* src;
+  int64_t left;
+  int64_t row;
+  uint32_t issued;
+};
+
+struct Par {
+  uint32_t p = 0, q = 0;
+  __device__ __forceinline__ uint32_t* scratch(Shared& S) {
+    uint32_t* s = S.scratch[p];
+    p ^= 1u;
+    return s;
+  }
+  __device__ __forceinline__ PickOut* slot(Shared& S) {
+    PickOut* s = &S.pick[q];
+    q ^= 1u;
+    return s;
+  }
+};
+
+// Thread 0: issues chunk number cur.issued of the sequence into its stage,
+// after the stage's previous chunk was taken by every warp.  Returns false
+// past the last chunk.
+__device__ __forceinline__ bool issue_next(Shared& S, Cursor& cur, const Params& p, uint64_t policy,
+                                           bool& timed_out) {
+  while (cur.left == 0) {
+    if (cur.row >= p.num_rows) return false;
+    cur.row += gridDim.x;
+    if (cur.row >= p.num_rows) return false;
+    const Row r = load_row(p, (int32_t)cur.row);
+    if (r.L <= p.k) continue;
+    cur.src = reinterpret_cast<const char*>(r.base4);
+    cur.left = (((int64_t)r.L + r.head + 3) >> 2) * 16;
+  }
+  const uint32_t c = cur.issued, s = c % kStages;
+  if (c >= (uint32_t)kStages) {
+    const uint32_t prev = c - kStages;
+    if (!timed_out && !mbar_wait_bounded(&S.empty[s], (prev / kStages) & 1u)) timed_out = true;
+  }
+  const uint32_t nb = (uint32_t)min((int64_t)kChunkBytes, cur.left);
+  mbar_arrive_expect_tx(&S.full[s], nb);
+  bulk_copy_g2s(&S.ring[s][0], cur.src, nb, &S.full[s], policy);
+  cur.src += nb;
+  cur.left -= nb;
+  ++cur.issued;
+  return true;
+}
+
+// Block-wide bucket pick over NB bins (bins below `lo` count as empty): the
+// bin where the count from the top first reaches r (and r2 when r2 > 0).
+template <int NB>
+__device__ __forceinline__ PickOut pick_bins(const uint32_t* hist, uint32_t lo, uint32_t r, uint32_t r2,
+                                             Shared& S, Par& par) {
+  constexpr int B = NB / kThreads;
+  static_assert(B >= 1 && NB % kThreads == 0, "bins per thread");
+  uint32_t* scratch = par.scratch(S);
+  PickOut* slot = par.slot(S);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t h[B];
+  if constexpr (B % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < B; i += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(hist + t * B + i);
+      h[i] = v.x; h[i + 1] = v.y; h[i + 2] = v.z; h[i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < B; ++i) h[i] = hist[t * B + i];
+  }
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < B; ++i) {
+    if ((uint32_t)(t * B + i) < lo) h[i] = 0u;
+    s += h[i];
+  }
+  const uint32_t incl = warp_incl_suffix(s);
+  if (lane == 0) scratch[warp] = incl;
+  if (t == 0) *slot = PickOut{0u, 0u, 0u, 0u, 0u, 0u};
+  __syncthreads();
+  const uint32_t wt = lane < kWarps ? scratch[lane] : 0u;
+  const uint32_t wsuf = warp_incl_suffix(wt);
+  const uint32_t above_warps = __shfl_sync(0xFFFFFFFFu, wsuf - wt, warp);
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, wsuf, 0);
+  uint32_t run = above_warps + incl - s;  // bins owned by higher threads
+#pragma unroll
+  for (int i = B - 1; i >= 0; --i) {
+    const uint32_t prev = run;
+    run += h[i];
+    if (prev < r && run >= r) {
+      slot->bin = (uint32_t)(t * B + i);
+      slot->above = prev;
+      slot->count = h[i];
+    }
+    if (r2 != 0u && prev < r2 && run >= r2) {
+      slot->bin2 = (uint32_t)(t * B + i);
+      slot->has2 = 1u;
+    }
+  }
+  if (t == 0) slot->total = total;
+  __syncthreads();
+  return *slot;
+}
+
+// Keeps the buffer entries i < n that pass `rule` (any order); returns the
+// new count, also stored in S.count.  Starts and ends with a barrier.
+__device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule rule, Par& par) {
+  constexpr int E = kCap / kThreads;
+  const int t = threadIdx.x;
+  uint32_t key[E];
+  int32_t jj[E];
+  uint32_t keep = 0, c = 0;
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const uint32_t i = (uint32_t)(t * E + e);
+    key[e] = 0u;
+    jj[e] = 0;
+    if (i < n) {
+      key[e] = S.bkey[i];
+      jj[e] = S.bj[i];
+      if (rule_pass(rule, key[e], jj[e])) {
+        keep |= 1u << e;
+        ++c;
+      }
+    }
+  }
+  uint32_t total;
+  uint32_t pos = block_excl_scan<kThreads>(c, par.scratch(S), total);  // contains a barrier
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (keep & (1u << e)) {
+      S.bkey[pos] = key[e];
+      S.bj[pos] = jj[e];
+      ++pos;
+    }
+  }
+  if (t == 0) S.count = total;
+  __syncthreads();
+  return total;
+}
+
+// Exact rule that selects the r largest pairs (key, ~j) of the n buffer
+// entries (r <= n).  Level 1 reads hist1, which must count every buffered
+// key exactly in bins >= lo (all buffered keys lie there).
+//
+// With r2 > 0 it also proposes a prefix threshold that about r2 entries reach
+// (the next row's hint): the level-2 sub-bin holding rank r2 when rank r2
+// falls in the level-1 bin of rank r and level 2 runs, else the level-1 bin of
+// rank r2.  *hint_ok is 0 when fewer than r2 entries are buffered.
+__device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, uint32_t lo, uint32_t r2,
+                                           Rule* hint, uint32_t* hint_ok, Par& par) {
+  const int t = threadIdx.x;
+  __syncthreads();
+  const PickOut p1 = pick_bins<kBins1>(S.hist1, lo, r, r2, S, par);
+  if (hint_ok) {
+    *hint_ok = p1.has2;
+    *hint = rule_bin(p1.bin2);
+  }
+  Rule a;
+  a.mk = kMaskBin;
+  a.tk = p1.bin << 20;
+  a.mj = 0u;
+  a.tj = 0u;
+  uint32_t rem = r - p1.above, cnt = p1.count;
+  // (on key or ~j, shift, bits) of the refinement levels
+  const int kLevels = 5;
+  const uint32_t on_key[kLevels] = {1u, 1u, 0u, 0u, 0u};
+  const int shift[kLevels] = {10, 0, 20, 10, 0};
+  const int bits[kLevels] = {10, 10, 11, 10, 10};
+  for (int l = 0; l < kLevels && cnt != rem; ++l) {
+    const uint32_t nb = 1u << bits[l];
+    for (uint32_t b = t; b < nb; b += kThreads) S.hist2[b] = 0u;
+    __syncthreads();
+    for (uint32_t i = t; i < n; i += kThreads) {
+      const uint32_t key = S.bkey[i];
+      const uint32_t nj = ~(uint32_t)S.bj[i];
+      if ((key & a.mk) == a.tk && (nj & a.mj) == a.tj) {
+        const uint32_t d = ((on_key[l] ? key : nj) >> shift[l]) & (nb - 1u);
+        atomicAdd(&S.hist2[d], 1u);
+      }
+    }
+    __syncthreads();
+    const bool hint_here = l == 0 && hint_ok && p1.has2 && p1.bin2 == p1.bin;
+    const uint32_t r2l = hint_here ? r2 - p1.above : 0u;
+    const PickOut pl = (bits[l] == 11) ? pick_bins<2048>(S.hist2, 0u, rem, 0u, S, par)
+                                       : pick_bins<1024>(S.hist2, 0u, rem, r2l, S, par);
+    if (hint_here && pl.has2) *hint = rule_prefix(kMaskSub, (p1.bin << 20) | (pl.bin2 << 10));
+    const uint32_t m = (nb - 1u) << shift[l];
+    if (on_key[l]) {
+      a.mk |= m;
+      a.tk |= pl.bin << shift[l];
+    } else {
+      a.mj |= m;
+      a.tj |= pl.bin << shift[l];
+    }
+    rem -= pl.above;
+    cnt = pl.count;
+  }
+  a.tf = key_floor_float(a.tk);
+  a.exact = (a.mk != kMaskBin) || (a.mj != 0u) ? 1u : 0u;
+  return a;
+}
+
+// The buffer would overflow: raise the threshold.  attempt 0 moves it to the
+// level-1 bin of the k-th largest buffered key; attempt 1 (or when that does
+// not rise) to the exact k-th largest pair.  n > k entries are buffered.
+__device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int attempt, Par& par) {
+  const Rule cur = S.rule;  // read before filter_buffer's first barrier; written after it
+  const uint32_t lo = rule_low_bin(cur);
+  if (attempt == 0 && !cur.exact) {
+    __syncthreads();
+    const PickOut p1 = pick_bins<kBins1>(S.hist1, lo, k, 0u, S, par);
+    if (p1.bin > lo || cur.mk == 0u) {
+      const Rule a = rule_bin(p1.bin);
+      filter_buffer(S, n, a, par);
+      if (threadIdx.x == 0) S.rule = a;
+      __syncthreads();
+      return;
+    }
+  }
+  const Rule a = select_buffer(S, n, k, lo, 0u, nullptr, nullptr, par);
+  const uint32_t kept = filter_buffer(S, n, a, par);
+  // hist1 must count the buffer exactly again (the bin of the threshold lost entries)
+  for (int b = threadIdx.x; b < kBins1; b += kThreads) S.hist1[b] = 0u;
+  if (threadIdx.x == 0) S.rule = a;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < kept; i += kThreads) atomicAdd(&S.hist1[S.bkey[i] >> 20], 1u);
+  __syncthreads();
+}
+
+// Takes this thread's 8 floats of the row's chunk c: from ring chunk g (then
+// marks the stage taken and, on thread 0, issues the next chunk), or straight
+// from global memory.
+template <bool kRing>
+__device__ __forceinline__ void take_chunk(Shared& S, const Params& p, const Row& r, int64_t nq, int64_t q0,
+                                           uint32_t g, Cursor& cur, uint64_t policy, bool& timed_out,
+                                           float x[8]) {
+  float4 v0, v1;
+  if constexpr (kRing) {
+    const uint32_t s = g % kStages;
+    if (!timed_out && !mbar_wait_bounded(&S.full[s], (g / kStages) & 1u)) timed_out = true;
+    v0 = S.ring[s][threadIdx.x];
+    v1 = S.ring[s][threadIdx.x + kThreads];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&S.empty[s]);
+    if (threadIdx.x == 0) issue_next(S, cur, p, policy, timed_out);
+  } else {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    v0 = q0 < nq ? __ldg(r.base4 + q0) : z;
+    v1 = q0 + kThreads < nq ? __ldg(r.base4 + q0 + kThreads) : z;
+  }
+  x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+  x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+}
+
+// Bit e set when element e of the thread's 8 passes `rule` and lies in the window.
+__device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8], int64_t jb0, int64_t jb1,
+                                               bool edge, int32_t L) {
+  uint32_t m = 0u;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m |= (x[e] >= rule.tf ? 1u : 0u) << e;
+  if (edge) {
+    uint32_t valid = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int64_t j = (e < 4 ? jb0 + e : jb1 + (e - 4));
+      valid |= (j >= 0 && j < L ? 1u : 0u) << e;
+    }
+    m &= valid;
+  }
+  if (rule.exact && m) {
+    for (uint32_t mm = m; mm; mm &= mm - 1u) {
+      const int e = __ffs(mm) - 1;
+      const int32_t j = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
+      if (!rule_pass(rule, key_of(x[e]), j)) m &= ~(1u << e);
+    }
+  }
+  return m;
+}
+
+__device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, uint32_t pos, int64_t jb0,
+                                       int64_t jb1) {
+  for (uint32_t mm = m; mm; mm &= mm - 1u) {
+    const int e = __ffs(mm) - 1;
+    const int32_t j = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
+    const uint32_t key = key_of(x[e]);
+    S.bkey[pos] = key;
+    S.bj[pos] = j;
+    ++pos;
+    atomicAdd(&S.hist1[key >> 20], 1u);
+  }
+}
+
+// Fast mode: the row's window through the ring with the fixed rule S.rule and
+// no block-wide synchronisation.  A reservation that does not fit sets
+// S.overflow (the row is then done again in exact mode).
+__device__ __forceinline__ void stream_row_fast(Shared& S, const Params& p, const Row& r, int64_t nq,
+                                                uint32_t& g, Cursor& cur, uint64_t policy, bool& timed_out) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
+  const Rule rule = S.rule;
+  for (int64_t c = 0; c < nch; ++c, ++g) {
+    const int64_t q0 = c * kChunkQuads + tid;
+    float x[8];
+    take_chunk<true>(S, p, r, nq, q0, g, cur, policy, timed_out, x);
+    const int64_t jb0 = q0 * 4 - r.head, jb1 = jb0 + 4 * (int64_t)kThreads;
+    const uint32_t m = admit_mask(rule, x, jb0, jb1, c == 0 || c == nch - 1, r.L);
+    if (__any_sync(0xFFFFFFFFu, m != 0u)) {
+      const uint32_t n = __popc(m);
+      const uint32_t incl = warp_incl_scan(n);
+      const uint32_t wsum = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      uint32_t base = 0u;
+      if (lane == 31) base = atomicAdd(&S.count, wsum);
+      base = __shfl_sync(0xFFFFFFFFu, base, 31);
+      if (base + wsum <= (uint32_t)kCap)
+        append(S, x, m, base + incl - n, jb0, jb1);
+      else if (lane == 0)
+        S.overflow = 1u;
+    }
+  }
+}
+
+// Exact mode: the row's window (from the ring, or from global memory) with a
+// rising threshold; the buffer is compacted whenever a chunk would overflow
+// it.  One block-wide vote per chunk.
+template <bool kRing>
+__device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, const Row& r, int64_t nq,
+                                                 uint32_t& g, Cursor& cur, uint64_t policy, bool& timed_out,
+                                                 Par& par) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const uint32_t k = (uint32_t)p.k;
+  const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
+  Rule rule = S.rule;
+  for (int64_t c = 0; c < nch; ++c) {
+    const int64_t q0 = c * kChunkQuads + tid;
+    float x[8];
+    take_chunk<kRing>(S, p, r, nq, q0, g, cur, policy, timed_out, x);
+    if constexpr (kRing) ++g;
+    const int64_t jb0 = q0 * 4 - r.head, jb1 = jb0 + 4 * (int64_t)kThreads;
+    uint32_t m = admit_mask(rule, x, jb0, jb1, c == 0 || c == nch - 1, r.L);
+    uint32_t pos;
+    for (int attempt = 0;; ++attempt) {
+      const uint32_t n = __popc(m);
+      const uint32_t incl = warp_incl_scan(n);
+      const uint32_t wsum = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      uint32_t base = 0u;
+      if (lane == 31) {
+        if (wsum) base = atomicAdd(&S.count, wsum);
+        S.wtot[w] = wsum;
+      }
+      base = __shfl_sync(0xFFFFFFFFu, base, 31);
+      pos = base + incl - n;
+      const bool ovf = __syncthreads_or(wsum != 0u && base + wsum > (uint32_t)kCap) != 0;
+      if (!ovf) break;
+      // roll back this chunk's reservations and raise the threshold
+      uint32_t added = 0;
+#pragma unroll
+      for (int i = 0; i < kWarps; ++i) added += S.wtot[i];
+      const uint32_t held = S.count - added;
+      compact(S, held, k, attempt, par);
+      rule = S.rule;
+      for (uint32_t mm = m; mm; mm &= mm - 1u) {
+        const int e = __ffs(mm) - 1;
+        const int32_t j = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
+        if (!rule_pass(rule, key_of(x[e]), j)) m &= ~(1u << e);
+      }
+    }
+    append(S, x, m, pos, jb0, jb1);
+  }
+}
+
+// Writes the buffer entries that pass `sel` (exactly k of them) in ascending
+// window index, through the page transform, to out_row[0, k).
+__device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row,
+                                              const Rule sel, uint32_t n, Par& par) {
+  const int t = threadIdx.x;
+  uint32_t* bm = S.hist1;
+  int32_t* stage = reinterpret_cast<int32_t*>(S.hist2);
+  const uint32_t k = (uint32_t)p.k;
+  uint32_t out_base = 0;
+  for (int64_t seg = 0; seg < r.L; seg += kSegBits) {
+    const int32_t seg_lo = (int32_t)seg;
+    const int32_t span = (int32_t)min((int64_t)kSegBits, (int64_t)r.L - seg);
+    const int32_t nw = (span + 31) >> 5;
+    __syncthreads();  // previous users of the bitmap are done
+    for (int i = t; i < nw; i += kThreads) bm[i] = 0u;
+    __syncthreads();
+    for (uint32_t i = t; i < n; i += kThreads) {
+      const int32_t j = S.bj[i];
+      if (j >= seg_lo && j - seg_lo < span && rule_pass(sel, S.bkey[i], j))
+        atomicOr(&bm[(j - seg_lo) >> 5], 1u << ((j - seg_lo) & 31));
+    }
+    __syncthreads();
+    const int32_t wpt = (nw + kThreads - 1) / kThreads;
+    const int32_t w0 = min(t * wpt, nw), w1 = min(w0 + wpt, nw);
+    uint32_t cnt = 0;
+    for (int32_t i = w0; i < w1; ++i) cnt += __popc(bm[i]);
+    uint32_t total;
+    uint32_t pos = out_base + block_excl_scan<kThreads>(cnt, par.scratch(S), total);
+    for (int32_t i = w0; i < w1; ++i) {
+      for (uint32_t b = bm[i]; b; b &= b - 1u) {
+        if (pos < k)
+          stage[pos] = seg_lo + i * 32 + (__ffs(b) - 1);
+        else
+          atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
+        ++pos;
+      }
+    }
+    out_base += total;
+  }
+  __syncthreads();
+  int32_t* o = p.out + row * p.k;
+  constexpr int U = 4;
+  for (int i0 = t; i0 < p.k; i0 += kThreads * U) {
+    int32_t j[U], pg[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kThreads;
+      j[u] = i < p.k ? stage[i] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) pg[u] = i0 + u * kThreads < p.k ? __ldg(r.page_row + (j[u] >> p.page_bits)) : 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kThreads;
+      if (i < p.k) o[i] = pg[u] * (1 << p.page_bits) + (j[u] & ((1 << p.page_bits) - 1));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) topk_pipe_kernel(Params p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Shared& S = *reinterpret_cast<Shared*>(smem_raw);
+  const int tid = threadIdx.x;
+  const uint32_t k = (uint32_t)p.k;
+  const uint64_t policy = l2_evict_first_policy();
+  bool timed_out = false;
+  Cursor cur;
+  cur.src = nullptr;
+  cur.left = 0;
+  cur.row = (int64_t)blockIdx.x - gridDim.x;
+  cur.issued = 0;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kWarps);
+    }
+    fence_barrier_init();
+    for (int s = 0; s < kAhead; ++s) issue_next(S, cur, p, policy, timed_out);
+    S.hint_valid = 0u;
+  }
+  __syncthreads();
+
+  Par par;
+  uint32_t g = 0;  // chunks taken from the ring
+
+  for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
+    const Row r = load_row(p, (int32_t)row);
+    if (r.L <= p.k) {
+      emit_whole_window<kThreads>(p, (int32_t)row, r, 0u, 1u);
+      continue;
+    }
+    const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
+    // ---- row set-up: empty buffer and histogram, threshold from the hint
+    {
+      uint4* h4 = reinterpret_cast<uint4*>(S.hist1);
+      for (int b = tid; b < kBins1 / 4; b += kThreads) h4[b] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const bool fast = S.hint_valid != 0u;  // read by every thread before thread 0 rewrites it below
+    __syncthreads();
+    if (tid == 0) {
+      S.count = 0u;
+      S.overflow = 0u;
+      S.rule = fast ? S.hint : rule_all();
+      S.hint_valid = 0u;
+      // the CTA's next row that needs a selection, for the hint
+      int32_t nl = 0;
+      for (int64_t rr = row + gridDim.x; rr < p.num_rows; rr += gridDim.x) {
+        const int32_t l = __ldg(p.seq_lens + rr);
+        if (l > p.k) {
+          nl = l;
+          break;
+        }
+      }
+      S.next_len = nl;
+      // rank of about 1.25 k in a row of the next row's length
+      S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
+    }
+    __syncthreads();
+    if (fast)
+      stream_row_fast(S, p, r, nq, g, cur, policy, timed_out);
+    else
+      stream_row_exact<true>(S, p, r, nq, g, cur, policy, timed_out, par);
+    __syncthreads();
+    uint32_t n = S.count;
+    if (n < k || S.overflow) {
+      // the hint was off: stream the row again, from global memory, exactly
+      for (int b = tid; b < kBins1; b += kThreads) S.hist1[b] = 0u;
+      __syncthreads();
+      if (tid == 0) {
+        S.count = 0u;
+        S.overflow = 0u;
+        S.rule = rule_all();
+      }
+      __syncthreads();
+      stream_row_exact<false>(S, p, r, nq, g, cur, policy, timed_out, par);
+      __syncthreads();
+      n = S.count;
+    }
+    // ---- selection, next row's hint, emission
+    Rule hint;
+    uint32_t hint_ok = 0u;
+    const uint32_t hr = S.hint_rank;
+    const Rule sel = select_buffer(S, n, k, rule_low_bin(S.rule), hr, &hint, &hint_ok, par);
+    if (tid == 0 && hr != 0u) {
+      if (hint_ok) {
+        S.hint = hint;
+        S.hint_valid = 1u;
+      } else if ((uint64_t)n * (uint64_t)S.next_len * 5u >= (uint64_t)6u * k * (uint64_t)r.L) {
+        // too few candidates for the rank, but the admitted ones scale to
+        // at least 1.2 k in the next row: keep this row's threshold
+        S.hint = rule_prefix(S.rule.mk, S.rule.tk);
+        S.hint_valid = 1u;
+      }
+    }
+    emit_selected(S, p, r, row, sel, n, par);
+  }
+
+  // Every issued chunk was taken, so no copy is in flight -- unless a wait
+  // gave up; then wait (bounded) for the copies that may still be landing.
+  if (__syncthreads_or(timed_out ? 1 : 0)) {
+    if (tid == 0) {
+      atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
+      for (uint32_t c = g; c < cur.issued; ++c) mbar_wait_bounded(&S.full[c % kStages], (c / kStages) & 1u);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace pipe
+}  // namespace topk

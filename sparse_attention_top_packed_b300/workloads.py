@@ -80,6 +80,15 @@ class Workload:
                         mv(self.row_starts), mv(self.row_to_batch), mv(self.page_table),
                         self.pt_stride, self.page_size, self.k, self.num_rows)
 
+    def head(self, n: int) -> "Workload":
+        """The first n query rows, with a copy of only the buffer rows they read
+        (so the full buffer can be freed)."""
+        n = min(int(n), self.num_rows)
+        cut = lambda t: None if t is None else t[:n].clone()
+        return Workload(self.name, self.scores[:n].clone(), self.row_stride, cut(self.seq_lens),
+                        cut(self.row_starts), cut(self.row_to_batch), self.page_table,
+                        self.pt_stride, self.page_size, self.k, n)
+
     def table_rows(self) -> torch.Tensor:
         """Table row of each query row (materialises the identity map)."""
         if self.row_to_batch is None:

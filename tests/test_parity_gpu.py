@@ -17,10 +17,10 @@ from tests.gpu_helpers import check_invariants_all_rows, oracle_rows, sample_row
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [dict(path="multipass"), dict(path="stream", cluster_size=1),
+PATHS = [dict(path="pipe"), dict(path="multipass"), dict(path="stream", cluster_size=1),
          dict(path="stream", cluster_size=2), dict(path="stream", cluster_size=4),
          dict(path="stream", cluster_size=8)]
-PATH_IDS = ["multipass", "stream1", "stream2", "stream4", "stream8"]
+PATH_IDS = ["pipe", "multipass", "stream1", "stream2", "stream4", "stream8"]
 
 
 def run(w, **launch):
@@ -166,9 +166,14 @@ def test_zero_rows_launches_nothing(cuda_device):
 
 def test_plan_reports_the_launch(cuda_device):
     plan = binding.topk_packed_plan(140000, 2048, 4096)
-    assert plan["path"] == binding.PATHS["stream"]
-    assert plan["threads_per_cta"] == 1024
-    assert plan["grid_ctas"] % plan["cluster_size"] == 0
+    assert plan["path"] == binding.PATHS["pipe"]
+    assert plan["threads_per_cta"] == 256
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan["grid_ctas"] == 2 * sms, "two pipelined CTAs per SM"
+    assert binding.topk_packed_plan(140000, 2048, 7)["grid_ctas"] == 7
+    st = binding.topk_packed_plan(140000, 2048, 4096, path="stream")
+    assert st["threads_per_cta"] == 1024
+    assert st["grid_ctas"] % st["cluster_size"] == 0
     mp = binding.topk_packed_plan(140000, 2048, 4096, path="multipass")
     assert mp["path"] == binding.PATHS["multipass"]
 
@@ -216,3 +221,64 @@ def test_mixed_full_size(cuda_device):
     out = _full_size(w, sample=768)
     out2 = run(w, path="multipass")
     assert torch.equal(out, out2)
+
+
+# ---------------------------------------------------------------------------
+# The pipelined kernel carries an admission threshold from one row of a CTA to
+# the next.  With one or two CTAs every row follows another in the same CTA,
+# so these sequences drive each branch: a hint above the next row's k-th key
+# (the row is streamed again), a hint far below it (the candidate buffer is
+# compacted), ties across the threshold (exact compaction on (key, index)),
+# rows much shorter or longer than the previous one, and rows whose k-th
+# largest score is -inf.
+# ---------------------------------------------------------------------------
+def _sequence_problem(rng, kind, rows=12, L=20000, k=2048, page_size=64):
+    stride = L + 37
+    scores = np.full(rows * stride, np.inf, dtype=np.float32)
+    seq = np.zeros(rows, np.int32)
+    st = np.zeros(rows, np.int32)
+    for i in range(rows):
+        n = L
+        if kind == "lengths":
+            n = [L, L // 6, L, 3000, L, 2100, L // 2, L][i % 8]
+        base = rng.standard_normal(n).astype(np.float32)
+        if kind == "falling":      # each row's scores sit below the previous row's
+            v = base - 0.5 * i
+        elif kind == "rising":     # each row's scores sit above the previous row's
+            v = base + 0.75 * i
+        elif kind == "ties":       # few distinct values: big tie groups at every threshold
+            v = np.round(base * 2.0) / 2.0
+        elif kind == "neg_inf":    # most of the window is -inf: the k-th largest is -inf
+            v = base.copy()
+            v[rng.random(n) < 0.97] = -np.inf
+        elif kind == "ramp":       # ascending windows: every chunk beats everything before it
+            v = np.sort(base)
+        else:
+            v = base
+        seq[i] = n
+        st[i] = int(rng.integers(0, stride - n + 1))
+        scores[i * stride + st[i]: i * stride + st[i] + n] = v.astype(np.float32)
+    pages = -(-stride // page_size)
+    table = rng.choice(1 << 24, size=2 * pages, replace=False).astype(np.int32)
+    rtb = (np.arange(rows) % 2).astype(np.int32)
+    return wl.HostProblem(scores, stride, seq, st, rtb, table, pages, page_size, k)
+
+
+@pytest.mark.parametrize("kind", ["falling", "rising", "ties", "neg_inf", "ramp", "lengths"])
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_pipe_threshold_carried_between_rows(cuda_device, kind, ctas):
+    rng = np.random.default_rng(zlib.crc32(kind.encode()))
+    p = _sequence_problem(rng, kind)
+    w = host_problem_to_device(p, cuda_device)
+    want = oracle_host(p)
+    got = run(w, path="pipe", max_ctas=ctas).cpu().numpy()
+    bad = np.nonzero((got != want).any(axis=1))[0]
+    assert bad.size == 0, f"rows {bad.tolist()} differ"
+
+
+@pytest.mark.parametrize("launch", PATHS, ids=PATH_IDS)
+def test_kth_largest_is_negative_infinity(cuda_device, launch):
+    rng = np.random.default_rng(11)
+    p = _sequence_problem(rng, "neg_inf", rows=6, L=9000, k=512)
+    w = host_problem_to_device(p, cuda_device)
+    assert np.array_equal(run(w, **launch).cpu().numpy(), oracle_host(p))
