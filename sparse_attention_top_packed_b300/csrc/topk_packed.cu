@@ -86,7 +86,7 @@ void init_device(int dev) {
                              (int)pipe_smem);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.pipe_ctas_per_sm, topk::pipe::topk_pipe_kernel,
-                                                      topk::pipe::kThreads, pipe_smem);
+                                                      topk::pipe::kBlock, pipe_smem);
   if (e == cudaSuccess) e = prepare_stream<1>(d.stream_ctas_per_sm, d.sms);
   if (e == cudaSuccess) e = prepare_stream<2>(d.stream_clusters[1], d.sms);
   if (e == cudaSuccess) e = prepare_stream<4>(d.stream_clusters[2], d.sms);
@@ -233,7 +233,7 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl.path == TOPK_PATH_PIPE) {
-    topk::pipe::topk_pipe_kernel<<<(unsigned)pl.grid, topk::pipe::kThreads, sizeof(topk::pipe::Shared), s>>>(prm);
+    topk::pipe::topk_pipe_kernel<<<(unsigned)pl.grid, topk::pipe::kBlock, sizeof(topk::pipe::Shared), s>>>(prm);
     e = cudaGetLastError();
   } else if (pl.path == TOPK_PATH_MULTIPASS) {
     topk::topk_multipass_kernel<<<(unsigned)pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), s>>>(prm);
@@ -275,7 +275,7 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
   if (cluster_size) *cluster_size = pl.cluster;
   if (grid_ctas) *grid_ctas = (int32_t)pl.grid;
   if (threads_per_cta)
-    *threads_per_cta = pl.path == TOPK_PATH_PIPE        ? topk::pipe::kThreads
+    *threads_per_cta = pl.path == TOPK_PATH_PIPE        ? topk::pipe::kBlock
                        : pl.path == TOPK_PATH_MULTIPASS ? topk::kMultipassThreads
                                                         : topk::kStreamThreads;
   return TOPK_OK;

@@ -15,10 +15,11 @@
 //    start rounded down to 16 bytes; lanes before the start and past the end
 //    are masked in registers (section 2 of the page, without writing the
 //    buffer).  Each stage has a "full" barrier (the copy landed) and an
-//    "empty" barrier (all 8 warps took the chunk into registers).  Thread 0,
-//    after taking chunk g, refills the stage of chunk g-1 with chunk
-//    g + kStages - 1, which may belong to a later row: the next row's first
-//    chunks are in flight while a row is finished.
+//    "empty" barrier (all 8 consumer warps took the chunk into registers).
+//    A ninth warp only produces: it refills each stage as soon as it is
+//    empty, running ahead across rows, so the next row's first chunks are in
+//    flight while a row is finished.  The consumer warps synchronise among
+//    themselves with named barrier 1, never with the producer.
 //
 //  * Admission.  Each thread takes 8 floats of a chunk and keeps those at or
 //    above the admission threshold, a lower bound on the row's k-th largest
@@ -58,13 +59,13 @@
 namespace topk {
 namespace pipe {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;              // consumer threads (warps 0-7)
 constexpr int kWarps = kThreads / 32;
+constexpr int kBlock = kThreads + 32;      // + the producer warp
 constexpr int kChunkBytes = 8192;
 constexpr int kChunkQuads = kChunkBytes / 16;  // 512
 constexpr int kChunkElems = kChunkBytes / 4;   // 2048
 constexpr int kStages = 6;
-constexpr int kAhead = kStages - 1;            // chunks in flight ahead of the one being taken
 constexpr int kKMax = 2048;
 constexpr int kCap = 4096;                 // candidate buffer entries
 constexpr int kBins1 = 4096;               // key bits [20, 32)
@@ -158,8 +159,34 @@ struct Par {
   }
 };
 
-// Thread 0: issues chunk number cur.issued of the sequence into its stage,
-// after the stage's previous chunk was taken by every warp.  Returns false
+// Barriers among the consumer warps only (named barrier 1).
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+__device__ __forceinline__ bool cbar_or(bool v) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\t"
+               "setp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.or.pred q, 1, %2, p;\n\t"
+               "selp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(r) : "r"(v ? 1u : 0u), "n"(kThreads) : "memory");
+  return r != 0u;
+}
+
+// Exclusive prefix of v over the consumer threads; `total` gets the sum.
+__device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* scratch, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan(v);
+  if (lane == 31) scratch[warp] = incl;
+  cbar();
+  const uint32_t wt = lane < kWarps ? scratch[lane] : 0u;
+  const uint32_t wincl = warp_incl_scan(wt);
+  const uint32_t wexcl = __shfl_sync(0xFFFFFFFFu, wincl - wt, warp);
+  total = __shfl_sync(0xFFFFFFFFu, wincl, kWarps - 1);
+  return wexcl + incl - v;
+}
+
+// The producer lane: issues chunk number cur.issued of the sequence into its stage,
+// after the stage's previous chunk was taken by every consumer warp.  Returns false
 // past the last chunk.
 __device__ __forceinline__ bool issue_next(Shared& S, Cursor& cur, const Params& p, uint64_t policy,
                                            bool& timed_out) {
@@ -216,7 +243,7 @@ __device__ __forceinline__ PickOut pick_bins(const uint32_t* hist, uint32_t lo, 
   const uint32_t incl = warp_incl_suffix(s);
   if (lane == 0) scratch[warp] = incl;
   if (t == 0) *slot = PickOut{0u, 0u, 0u, 0u, 0u, 0u};
-  __syncthreads();
+  cbar();
   const uint32_t wt = lane < kWarps ? scratch[lane] : 0u;
   const uint32_t wsuf = warp_incl_suffix(wt);
   const uint32_t above_warps = __shfl_sync(0xFFFFFFFFu, wsuf - wt, warp);
@@ -237,7 +264,7 @@ __device__ __forceinline__ PickOut pick_bins(const uint32_t* hist, uint32_t lo, 
     }
   }
   if (t == 0) slot->total = total;
-  __syncthreads();
+  cbar();
   return *slot;
 }
 
@@ -249,7 +276,7 @@ __device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule
   uint32_t key[E];
   int32_t jj[E];
   uint32_t keep = 0, c = 0;
-  __syncthreads();
+  cbar();
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const uint32_t i = (uint32_t)(t * E + e);
@@ -265,7 +292,7 @@ __device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule
     }
   }
   uint32_t total;
-  uint32_t pos = block_excl_scan<kThreads>(c, par.scratch(S), total);  // contains a barrier
+  uint32_t pos = cta_excl_scan(c, par.scratch(S), total);  // contains a barrier
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     if (keep & (1u << e)) {
@@ -275,7 +302,7 @@ __device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule
     }
   }
   if (t == 0) S.count = total;
-  __syncthreads();
+  cbar();
   return total;
 }
 
@@ -290,7 +317,7 @@ __device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule
 __device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, uint32_t lo, uint32_t r2,
                                            Rule* hint, uint32_t* hint_ok, Par& par) {
   const int t = threadIdx.x;
-  __syncthreads();
+  cbar();
   const PickOut p1 = pick_bins<kBins1>(S.hist1, lo, r, r2, S, par);
   if (hint_ok) {
     *hint_ok = p1.has2;
@@ -310,7 +337,7 @@ __device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, ui
   for (int l = 0; l < kLevels && cnt != rem; ++l) {
     const uint32_t nb = 1u << bits[l];
     for (uint32_t b = t; b < nb; b += kThreads) S.hist2[b] = 0u;
-    __syncthreads();
+    cbar();
     for (uint32_t i = t; i < n; i += kThreads) {
       const uint32_t key = S.bkey[i];
       const uint32_t nj = ~(uint32_t)S.bj[i];
@@ -319,7 +346,7 @@ __device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, ui
         atomicAdd(&S.hist2[d], 1u);
       }
     }
-    __syncthreads();
+    cbar();
     const bool hint_here = l == 0 && hint_ok && p1.has2 && p1.bin2 == p1.bin;
     const uint32_t r2l = hint_here ? r2 - p1.above : 0u;
     const PickOut pl = (bits[l] == 11) ? pick_bins<2048>(S.hist2, 0u, rem, 0u, S, par)
@@ -348,13 +375,13 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   const Rule cur = S.rule;  // read before filter_buffer's first barrier; written after it
   const uint32_t lo = rule_low_bin(cur);
   if (attempt == 0 && !cur.exact) {
-    __syncthreads();
+    cbar();
     const PickOut p1 = pick_bins<kBins1>(S.hist1, lo, k, 0u, S, par);
     if (p1.bin > lo || cur.mk == 0u) {
       const Rule a = rule_bin(p1.bin);
       filter_buffer(S, n, a, par);
       if (threadIdx.x == 0) S.rule = a;
-      __syncthreads();
+      cbar();
       return;
     }
   }
@@ -363,27 +390,23 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   // hist1 must count the buffer exactly again (the bin of the threshold lost entries)
   for (int b = threadIdx.x; b < kBins1; b += kThreads) S.hist1[b] = 0u;
   if (threadIdx.x == 0) S.rule = a;
-  __syncthreads();
+  cbar();
   for (uint32_t i = threadIdx.x; i < kept; i += kThreads) atomicAdd(&S.hist1[S.bkey[i] >> 20], 1u);
-  __syncthreads();
+  cbar();
 }
 
-// Takes this thread's 8 floats of the row's chunk c: from ring chunk g (then
-// marks the stage taken and, on thread 0, issues the next chunk), or straight
-// from global memory.
+// Takes this thread's 8 floats of the row's chunk c: from ring chunk g, or
+// straight from global memory.  A ring stage must then be given back with
+// release_chunk once the values have been used.
 template <bool kRing>
-__device__ __forceinline__ void take_chunk(Shared& S, const Params& p, const Row& r, int64_t nq, int64_t q0,
-                                           uint32_t g, Cursor& cur, uint64_t policy, bool& timed_out,
-                                           float x[8]) {
+__device__ __forceinline__ void take_chunk(Shared& S, const Row& r, int64_t nq, int64_t q0, uint32_t g,
+                                           bool& timed_out, float x[8]) {
   float4 v0, v1;
   if constexpr (kRing) {
     const uint32_t s = g % kStages;
     if (!timed_out && !mbar_wait_bounded(&S.full[s], (g / kStages) & 1u)) timed_out = true;
     v0 = S.ring[s][threadIdx.x];
     v1 = S.ring[s][threadIdx.x + kThreads];
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&S.empty[s]);
-    if (threadIdx.x == 0) issue_next(S, cur, p, policy, timed_out);
   } else {
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     v0 = q0 < nq ? __ldg(r.base4 + q0) : z;
@@ -391,6 +414,17 @@ __device__ __forceinline__ void take_chunk(Shared& S, const Params& p, const Row
   }
   x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
   x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+}
+
+// Gives ring stage g % kStages back to the producer.  The stage's next
+// content is written by a TMA copy (the async proxy) while these reads were
+// plain shared-memory loads (the generic proxy): each thread orders its reads
+// before that write with a proxy fence, after the loaded values have been
+// used, and the warp then arrives on the stage's "empty" barrier.
+__device__ __forceinline__ void release_chunk(Shared& S, uint32_t g) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&S.empty[g % kStages]);
 }
 
 // Bit e set when element e of the thread's 8 passes `rule` and lies in the window.
@@ -434,17 +468,18 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
 // Fast mode: the row's window through the ring with the fixed rule S.rule and
 // no block-wide synchronisation.  A reservation that does not fit sets
 // S.overflow (the row is then done again in exact mode).
-__device__ __forceinline__ void stream_row_fast(Shared& S, const Params& p, const Row& r, int64_t nq,
-                                                uint32_t& g, Cursor& cur, uint64_t policy, bool& timed_out) {
+__device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t nq, uint32_t& g,
+                                                bool& timed_out) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
   const Rule rule = S.rule;
   for (int64_t c = 0; c < nch; ++c, ++g) {
     const int64_t q0 = c * kChunkQuads + tid;
     float x[8];
-    take_chunk<true>(S, p, r, nq, q0, g, cur, policy, timed_out, x);
+    take_chunk<true>(S, r, nq, q0, g, timed_out, x);
     const int64_t jb0 = q0 * 4 - r.head, jb1 = jb0 + 4 * (int64_t)kThreads;
     const uint32_t m = admit_mask(rule, x, jb0, jb1, c == 0 || c == nch - 1, r.L);
+    release_chunk(S, g);
     if (__any_sync(0xFFFFFFFFu, m != 0u)) {
       const uint32_t n = __popc(m);
       const uint32_t incl = warp_incl_scan(n);
@@ -465,8 +500,7 @@ __device__ __forceinline__ void stream_row_fast(Shared& S, const Params& p, cons
 // it.  One block-wide vote per chunk.
 template <bool kRing>
 __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, const Row& r, int64_t nq,
-                                                 uint32_t& g, Cursor& cur, uint64_t policy, bool& timed_out,
-                                                 Par& par) {
+                                                 uint32_t& g, bool& timed_out, Par& par) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t k = (uint32_t)p.k;
   const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
@@ -474,10 +508,13 @@ __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, con
   for (int64_t c = 0; c < nch; ++c) {
     const int64_t q0 = c * kChunkQuads + tid;
     float x[8];
-    take_chunk<kRing>(S, p, r, nq, q0, g, cur, policy, timed_out, x);
-    if constexpr (kRing) ++g;
+    take_chunk<kRing>(S, r, nq, q0, g, timed_out, x);
     const int64_t jb0 = q0 * 4 - r.head, jb1 = jb0 + 4 * (int64_t)kThreads;
     uint32_t m = admit_mask(rule, x, jb0, jb1, c == 0 || c == nch - 1, r.L);
+    if constexpr (kRing) {
+      release_chunk(S, g);
+      ++g;
+    }
     uint32_t pos;
     for (int attempt = 0;; ++attempt) {
       const uint32_t n = __popc(m);
@@ -490,7 +527,7 @@ __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, con
       }
       base = __shfl_sync(0xFFFFFFFFu, base, 31);
       pos = base + incl - n;
-      const bool ovf = __syncthreads_or(wsum != 0u && base + wsum > (uint32_t)kCap) != 0;
+      const bool ovf = cbar_or(wsum != 0u && base + wsum > (uint32_t)kCap);
       if (!ovf) break;
       // roll back this chunk's reservations and raise the threshold
       uint32_t added = 0;
@@ -522,21 +559,21 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
     const int32_t seg_lo = (int32_t)seg;
     const int32_t span = (int32_t)min((int64_t)kSegBits, (int64_t)r.L - seg);
     const int32_t nw = (span + 31) >> 5;
-    __syncthreads();  // previous users of the bitmap are done
+    cbar();  // previous users of the bitmap are done
     for (int i = t; i < nw; i += kThreads) bm[i] = 0u;
-    __syncthreads();
+    cbar();
     for (uint32_t i = t; i < n; i += kThreads) {
       const int32_t j = S.bj[i];
       if (j >= seg_lo && j - seg_lo < span && rule_pass(sel, S.bkey[i], j))
         atomicOr(&bm[(j - seg_lo) >> 5], 1u << ((j - seg_lo) & 31));
     }
-    __syncthreads();
+    cbar();
     const int32_t wpt = (nw + kThreads - 1) / kThreads;
     const int32_t w0 = min(t * wpt, nw), w1 = min(w0 + wpt, nw);
     uint32_t cnt = 0;
     for (int32_t i = w0; i < w1; ++i) cnt += __popc(bm[i]);
     uint32_t total;
-    uint32_t pos = out_base + block_excl_scan<kThreads>(cnt, par.scratch(S), total);
+    uint32_t pos = out_base + cta_excl_scan(cnt, par.scratch(S), total);
     for (int32_t i = w0; i < w1; ++i) {
       for (uint32_t b = bm[i]; b; b &= b - 1u) {
         if (pos < k)
@@ -548,7 +585,7 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
     }
     out_base += total;
   }
-  __syncthreads();
+  cbar();
   int32_t* o = p.out + row * p.k;
   constexpr int U = 4;
   for (int i0 = t; i0 < p.k; i0 += kThreads * U) {
@@ -568,28 +605,44 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) topk_pipe_kernel(Params p) {
+__global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Shared& S = *reinterpret_cast<Shared*>(smem_raw);
   const int tid = threadIdx.x;
   const uint32_t k = (uint32_t)p.k;
   const uint64_t policy = l2_evict_first_policy();
   bool timed_out = false;
-  Cursor cur;
-  cur.src = nullptr;
-  cur.left = 0;
-  cur.row = (int64_t)blockIdx.x - gridDim.x;
-  cur.issued = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], kWarps);
     }
     fence_barrier_init();
-    for (int s = 0; s < kAhead; ++s) issue_next(S, cur, p, policy, timed_out);
     S.hint_valid = 0u;
   }
   __syncthreads();
+
+  if (tid >= kThreads) {
+    // ---- producer warp: one lane streams every chunk of the CTA's rows
+    Cursor cur;
+    cur.src = nullptr;
+    cur.left = 0;
+    cur.row = (int64_t)blockIdx.x - gridDim.x;
+    cur.issued = 0;
+    if (tid == kThreads) {
+      while (issue_next(S, cur, p, policy, timed_out)) {
+      }
+    }
+    // Every issued chunk is taken by the consumers before they finish, so no
+    // copy is in flight at exit -- unless a wait gave up; then wait (bounded)
+    // for the last chunks issued.
+    if (__syncthreads_or(timed_out ? 1 : 0) && tid == kThreads) {
+      atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
+      const uint32_t first = cur.issued > (uint32_t)kStages ? cur.issued - kStages : 0u;
+      for (uint32_t c = first; c < cur.issued; ++c) mbar_wait_bounded(&S.full[c % kStages], (c / kStages) & 1u);
+    }
+    return;
+  }
 
   Par par;
   uint32_t g = 0;  // chunks taken from the ring
@@ -607,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_pipe_kernel(Params p) {
       for (int b = tid; b < kBins1 / 4; b += kThreads) h4[b] = make_uint4(0u, 0u, 0u, 0u);
     }
     const bool fast = S.hint_valid != 0u;  // read by every thread before thread 0 rewrites it below
-    __syncthreads();
+    cbar();
     if (tid == 0) {
       S.count = 0u;
       S.overflow = 0u;
@@ -626,25 +679,25 @@ __global__ void __launch_bounds__(kThreads, 2) topk_pipe_kernel(Params p) {
       // rank of about 1.25 k in a row of the next row's length
       S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
     }
-    __syncthreads();
+    cbar();
     if (fast)
-      stream_row_fast(S, p, r, nq, g, cur, policy, timed_out);
+      stream_row_fast(S, r, nq, g, timed_out);
     else
-      stream_row_exact<true>(S, p, r, nq, g, cur, policy, timed_out, par);
-    __syncthreads();
+      stream_row_exact<true>(S, p, r, nq, g, timed_out, par);
+    cbar();
     uint32_t n = S.count;
     if (n < k || S.overflow) {
       // the hint was off: stream the row again, from global memory, exactly
       for (int b = tid; b < kBins1; b += kThreads) S.hist1[b] = 0u;
-      __syncthreads();
+      cbar();
       if (tid == 0) {
         S.count = 0u;
         S.overflow = 0u;
         S.rule = rule_all();
       }
-      __syncthreads();
-      stream_row_exact<false>(S, p, r, nq, g, cur, policy, timed_out, par);
-      __syncthreads();
+      cbar();
+      stream_row_exact<false>(S, p, r, nq, g, timed_out, par);
+      cbar();
       n = S.count;
     }
     // ---- selection, next row's hint, emission
@@ -666,15 +719,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_pipe_kernel(Params p) {
     emit_selected(S, p, r, row, sel, n, par);
   }
 
-  // Every issued chunk was taken, so no copy is in flight -- unless a wait
-  // gave up; then wait (bounded) for the copies that may still be landing.
-  if (__syncthreads_or(timed_out ? 1 : 0)) {
-    if (tid == 0) {
-      atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
-      for (uint32_t c = g; c < cur.issued; ++c) mbar_wait_bounded(&S.full[c % kStages], (c / kStages) & 1u);
-    }
-    __syncthreads();
-  }
+  // (the producer warp joins this last block-wide vote)
+  if (__syncthreads_or(timed_out ? 1 : 0) && tid == 0) atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
 }
 
 }  // namespace pipe
