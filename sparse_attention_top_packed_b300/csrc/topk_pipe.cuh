@@ -24,27 +24,30 @@
 //  * Admission.  Each thread takes 8 floats of a chunk and keeps those at or
 //    above the admission threshold, a lower bound on the row's k-th largest
 //    key: one float compare per element.  Kept elements (order-preserving
-//    key, window index) go to one candidate buffer of kCap entries, at
-//    positions reserved by one shared-memory atomic per warp, and are counted
-//    in a 4096-bin histogram of the key's top 12 bits.
+//    key, window index) go to a candidate buffer of kCap entries.
 //
 //  * Threshold.  When the CTA's previous row gives a hint -- the key prefix
 //    that about 1.25 k of its candidates reach, scaled to the new row's
 //    length -- the row streams with that fixed threshold and no block-wide
-//    synchronisation ("fast" mode).  If that admits fewer than k elements or
-//    overflows the buffer, the row is streamed again from global memory in
-//    "exact" mode.  Without a hint (first row of a CTA, a much shorter row)
-//    the row streams in exact mode from the ring: the threshold starts at
-//    -inf and, whenever the buffer would overflow, rises to the histogram bin
-//    of the k-th largest buffered key, or to the exact k-th largest (key,
-//    index) pair.  Any threshold at or below the k-th largest key of the
-//    elements seen so far is safe, so no selected element is ever dropped.
+//    synchronisation ("fast" mode): each warp appends to its own region of
+//    the buffer at positions from warp ballots, with no shared atomics.  If
+//    that admits fewer than k elements or overflows a region, the row is
+//    streamed again from global memory in "exact" mode.  Without a hint
+//    (first row of a CTA, a much shorter row) the row streams in exact mode
+//    from the ring: one shared buffer, a 4096-bin histogram of the key's top
+//    12 bits kept as elements arrive, and a threshold that starts at -inf and,
+//    whenever a chunk would overflow the buffer, rises to the histogram bin of
+//    the k-th largest buffered key, or to the exact k-th largest (key, index)
+//    pair.  Any threshold at or below the k-th largest key of the elements
+//    seen so far is safe, so no selected element is ever dropped.
 //
 //  * Selection.  A radix select on the buffer orders candidates by the
-//    64-bit pair (key, ~j): larger key first, then lower j.  Level 1 uses the
-//    histogram kept while streaming; levels 2-3 refine the key (10 bits each);
-//    levels 4-6 (only for equal keys) refine ~j.  Pairs are unique, so the
-//    result is exactly k candidates, whatever the ties.
+//    64-bit pair (key, ~j): larger key first, then lower j.  The candidates'
+//    keys share a prefix (the bits where the smallest and largest agree); the
+//    digits, 11 bits each, start right below it, so the first level already
+//    spreads the candidates over up to 2048 bins.  Levels go on into ~j only
+//    for equal keys.  Pairs are unique, so the result is exactly k
+//    candidates, whatever the ties.
 //
 //  * Emission.  The selected window indices are set in a bitmap of the window
 //    (reusing the histogram's shared memory, 131072 indices per segment); a
@@ -68,6 +71,7 @@ constexpr int kChunkElems = kChunkBytes / 4;   // 2048
 constexpr int kStages = 6;
 constexpr int kKMax = 2048;
 constexpr int kCap = 4096;                 // candidate buffer entries
+constexpr int kRegion = kCap / kWarps;     // fast mode: one region of the buffer per warp
 constexpr int kBins1 = 4096;               // key bits [20, 32)
 constexpr int kBins2 = 2048;               // refinement levels (<= 11 bits)
 constexpr int kSegBits = kBins1 * 32;      // bitmap indices per emission segment
@@ -125,6 +129,8 @@ struct Shared {
   uint32_t scratch[2][kWarps];
   PickOut pick[2];
   uint32_t wtot[kWarps];
+  uint32_t rbase[kWarps], rcnt[kWarps];  // the buffer, as one region per warp (see set_regions_*)
+  uint32_t wmin[kWarps], wmax[kWarps];
   uint32_t count;
   uint32_t overflow;  // fast mode: a reservation did not fit
   Rule rule;          // admission rule of the current row
@@ -306,66 +312,100 @@ __device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule
   return total;
 }
 
-// Exact rule that selects the r largest pairs (key, ~j) of the n buffer
-// entries (r <= n).  Level 1 reads hist1, which must count every buffered
-// key exactly in bins >= lo (all buffered keys lie there).
-//
-// With r2 > 0 it also proposes a prefix threshold that about r2 entries reach
-// (the next row's hint): the level-2 sub-bin holding rank r2 when rank r2
-// falls in the level-1 bin of rank r and level 2 runs, else the level-1 bin of
-// rank r2.  *hint_ok is 0 when fewer than r2 entries are buffered.
-__device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, uint32_t lo, uint32_t r2,
-                                           Rule* hint, uint32_t* hint_ok, Par& par) {
-  const int t = threadIdx.x;
-  cbar();
-  const PickOut p1 = pick_bins<kBins1>(S.hist1, lo, r, r2, S, par);
-  if (hint_ok) {
-    *hint_ok = p1.has2;
-    *hint = rule_bin(p1.bin2);
+// The buffer as kWarps regions, each scanned by one warp: entries
+// [rbase[w], rbase[w] + rcnt[w]).  Each warp's lane 0 writes its own pair;
+// a consumer barrier must follow before other warps read them.
+__device__ __forceinline__ void set_regions_contiguous(Shared& S, uint32_t n) {
+  const uint32_t per = (n + kWarps - 1) / kWarps, w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t b = min(w * per, n);
+    S.rbase[w] = b;
+    S.rcnt[w] = min(per, n - b);
   }
+}
+
+__device__ __forceinline__ uint64_t pair_of(uint32_t key, int32_t j) {
+  return ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)j);
+}
+
+__device__ __forceinline__ Rule rule_of_pair_prefix(uint64_t M, uint64_t T) {
   Rule a;
-  a.mk = kMaskBin;
-  a.tk = p1.bin << 20;
-  a.mj = 0u;
-  a.tj = 0u;
-  uint32_t rem = r - p1.above, cnt = p1.count;
-  // (on key or ~j, shift, bits) of the refinement levels
-  const int kLevels = 5;
-  const uint32_t on_key[kLevels] = {1u, 1u, 0u, 0u, 0u};
-  const int shift[kLevels] = {10, 0, 20, 10, 0};
-  const int bits[kLevels] = {10, 10, 11, 10, 10};
-  for (int l = 0; l < kLevels && cnt != rem; ++l) {
-    const uint32_t nb = 1u << bits[l];
-    for (uint32_t b = t; b < nb; b += kThreads) S.hist2[b] = 0u;
-    cbar();
-    for (uint32_t i = t; i < n; i += kThreads) {
-      const uint32_t key = S.bkey[i];
-      const uint32_t nj = ~(uint32_t)S.bj[i];
-      if ((key & a.mk) == a.tk && (nj & a.mj) == a.tj) {
-        const uint32_t d = ((on_key[l] ? key : nj) >> shift[l]) & (nb - 1u);
-        atomicAdd(&S.hist2[d], 1u);
-      }
-    }
-    cbar();
-    const bool hint_here = l == 0 && hint_ok && p1.has2 && p1.bin2 == p1.bin;
-    const uint32_t r2l = hint_here ? r2 - p1.above : 0u;
-    const PickOut pl = (bits[l] == 11) ? pick_bins<2048>(S.hist2, 0u, rem, 0u, S, par)
-                                       : pick_bins<1024>(S.hist2, 0u, rem, r2l, S, par);
-    if (hint_here && pl.has2) *hint = rule_prefix(kMaskSub, (p1.bin << 20) | (pl.bin2 << 10));
-    const uint32_t m = (nb - 1u) << shift[l];
-    if (on_key[l]) {
-      a.mk |= m;
-      a.tk |= pl.bin << shift[l];
-    } else {
-      a.mj |= m;
-      a.tj |= pl.bin << shift[l];
-    }
-    rem -= pl.above;
-    cnt = pl.count;
-  }
+  a.mk = (uint32_t)(M >> 32);
+  a.tk = (uint32_t)(T >> 32);
+  a.mj = (uint32_t)M;
+  a.tj = (uint32_t)T;
   a.tf = key_floor_float(a.tk);
-  a.exact = (a.mk != kMaskBin) || (a.mj != 0u) ? 1u : 0u;
+  a.exact = a.mj != 0u ? 1u : 0u;
   return a;
+}
+
+// Exact rule that selects the r largest pairs (key, ~j) among the n buffered
+// entries (r <= n; regions set).  The selected entries are those whose pair,
+// under the returned prefix mask, is at least the returned prefix.
+//
+// With r2 > 0 it also proposes a key-prefix threshold that at least r2
+// entries reach (the next row's hint): the deepest prefix, at most two digits
+// below the common one, whose bin holds rank r2.  *hint_ok is 0 when fewer
+// than r2 entries are buffered.
+__device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, uint32_t r2, Rule* hint,
+                                           uint32_t* hint_ok, Par& par) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
+  // common prefix of the buffered keys
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (uint32_t i = lane; i < cnt; i += 32) {
+    const uint32_t key = S.bkey[base + i];
+    mn = min(mn, key);
+    mx = max(mx, key);
+  }
+  mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  if (lane == 0) {
+    S.wmin[w] = mn;
+    S.wmax[w] = mx;
+  }
+  cbar();
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) {
+    mn = min(mn, S.wmin[i]);
+    mx = max(mx, S.wmax[i]);
+  }
+  const int P = mn == mx ? 32 : __clz(mn ^ mx);
+  uint64_t M = P ? (~0ull << (64 - P)) : 0ull;
+  uint64_t T = ((uint64_t)mn << 32) & M;
+  int pos = 64 - P;
+  uint32_t rem = r, hr = r2;
+  bool track = r2 != 0u && r2 <= n;
+  uint64_t HM = M, HT = T;
+  for (int level = 0; pos > 0; ++level) {
+    const int wd = pos < 11 ? pos : 11, sh = pos - wd;
+    const uint32_t nb = 1u << wd;
+    for (uint32_t b = threadIdx.x; b < (uint32_t)kBins2; b += kThreads) S.hist2[b] = 0u;
+    cbar();
+    for (uint32_t i = lane; i < cnt; i += 32) {
+      const uint64_t c = pair_of(S.bkey[base + i], S.bj[base + i]);
+      if ((c & M) == T) atomicAdd(&S.hist2[(uint32_t)(c >> sh) & (nb - 1u)], 1u);
+    }
+    cbar();
+    const PickOut pk = pick_bins<kBins2>(S.hist2, 0u, rem, track ? hr : 0u, S, par);
+    const uint64_t dm = (uint64_t)(nb - 1u) << sh;
+    if (track && pk.has2) {
+      HM = M | dm;
+      HT = T | ((uint64_t)pk.bin2 << sh);
+    }
+    track = track && pk.has2 && pk.bin2 == pk.bin && level < 1;
+    if (track) hr -= pk.above;
+    M |= dm;
+    T |= (uint64_t)pk.bin << sh;
+    rem -= pk.above;
+    pos = sh;
+    if (pk.count == rem) break;
+  }
+  if (hint_ok) {
+    *hint_ok = (r2 != 0u && r2 <= n) ? 1u : 0u;
+    *hint = rule_prefix((uint32_t)(HM >> 32), (uint32_t)(HT >> 32));  // the key part: never higher
+  }
+  return rule_of_pair_prefix(M, T);
 }
 
 // The buffer would overflow: raise the threshold.  attempt 0 moves it to the
@@ -385,7 +425,9 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
       return;
     }
   }
-  const Rule a = select_buffer(S, n, k, lo, 0u, nullptr, nullptr, par);
+  set_regions_contiguous(S, n);
+  cbar();
+  const Rule a = select_buffer(S, n, k, 0u, nullptr, nullptr, par);
   const uint32_t kept = filter_buffer(S, n, a, par);
   // hist1 must count the buffer exactly again (the bin of the threshold lost entries)
   for (int b = threadIdx.x; b < kBins1; b += kThreads) S.hist1[b] = 0u;
@@ -466,13 +508,19 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
 }
 
 // Fast mode: the row's window through the ring with the fixed rule S.rule and
-// no block-wide synchronisation.  A reservation that does not fit sets
-// S.overflow (the row is then done again in exact mode).
+// no block-wide synchronisation.  Warp w appends to region w of the buffer
+// (kRegion entries), at positions from its ballots; a region that would
+// overflow sets S.overflow (the row is then done again in exact mode).
 __device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t nq, uint32_t& g,
                                                 bool& timed_out) {
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
   const Rule rule = S.rule;
+  const uint32_t lt = lanemask_lt();
+  uint32_t* rkey = S.bkey + w * kRegion;
+  int32_t* rj = S.bj + w * kRegion;
+  uint32_t wcnt = 0;
+  bool full = false;
   for (int64_t c = 0; c < nch; ++c, ++g) {
     const int64_t q0 = c * kChunkQuads + tid;
     float x[8];
@@ -480,18 +528,32 @@ __device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t
     const int64_t jb0 = q0 * 4 - r.head, jb1 = jb0 + 4 * (int64_t)kThreads;
     const uint32_t m = admit_mask(rule, x, jb0, jb1, c == 0 || c == nch - 1, r.L);
     release_chunk(S, g);
-    if (__any_sync(0xFFFFFFFFu, m != 0u)) {
-      const uint32_t n = __popc(m);
-      const uint32_t incl = warp_incl_scan(n);
-      const uint32_t wsum = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      uint32_t base = 0u;
-      if (lane == 31) base = atomicAdd(&S.count, wsum);
-      base = __shfl_sync(0xFFFFFFFFu, base, 31);
-      if (base + wsum <= (uint32_t)kCap)
-        append(S, x, m, base + incl - n, jb0, jb1);
-      else if (lane == 0)
-        S.overflow = 1u;
+    if (full || !__any_sync(0xFFFFFFFFu, m != 0u)) continue;
+    uint32_t b[8], before[8], tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      b[e] = __ballot_sync(0xFFFFFFFFu, (m >> e) & 1u);
+      before[e] = tot;
+      tot += __popc(b[e]);
     }
+    if (wcnt + tot > (uint32_t)kRegion) {
+      full = true;
+      if (lane == 0) S.overflow = 1u;
+      continue;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if ((m >> e) & 1u) {
+        const uint32_t pos = wcnt + before[e] + __popc(b[e] & lt);
+        rkey[pos] = key_of(x[e]);
+        rj[pos] = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
+      }
+    }
+    wcnt += tot;
+  }
+  if (lane == 0) {
+    S.rbase[w] = (uint32_t)(w * kRegion);
+    S.rcnt[w] = wcnt;
   }
 }
 
@@ -549,8 +611,9 @@ __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, con
 // Writes the buffer entries that pass `sel` (exactly k of them) in ascending
 // window index, through the page transform, to out_row[0, k).
 __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row,
-                                              const Rule sel, uint32_t n, Par& par) {
-  const int t = threadIdx.x;
+                                              const Rule sel, Par& par) {
+  const int t = threadIdx.x, lane = t & 31;
+  const uint32_t rbase = S.rbase[t >> 5], rcnt = S.rcnt[t >> 5];
   uint32_t* bm = S.hist1;
   int32_t* stage = reinterpret_cast<int32_t*>(S.hist2);
   const uint32_t k = (uint32_t)p.k;
@@ -562,9 +625,9 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
     cbar();  // previous users of the bitmap are done
     for (int i = t; i < nw; i += kThreads) bm[i] = 0u;
     cbar();
-    for (uint32_t i = t; i < n; i += kThreads) {
-      const int32_t j = S.bj[i];
-      if (j >= seg_lo && j - seg_lo < span && rule_pass(sel, S.bkey[i], j))
+    for (uint32_t i = lane; i < rcnt; i += 32) {
+      const int32_t j = S.bj[rbase + i];
+      if (j >= seg_lo && j - seg_lo < span && rule_pass(sel, S.bkey[rbase + i], j))
         atomicOr(&bm[(j - seg_lo) >> 5], 1u << ((j - seg_lo) & 31));
     }
     cbar();
@@ -680,12 +743,17 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
     }
     cbar();
-    if (fast)
+    if (fast) {
       stream_row_fast(S, r, nq, g, timed_out);
-    else
+    } else {
       stream_row_exact<true>(S, p, r, nq, g, timed_out, par);
+      cbar();
+      set_regions_contiguous(S, S.count);
+    }
     cbar();
-    uint32_t n = S.count;
+    uint32_t n = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) n += S.rcnt[i];
     if (n < k || S.overflow) {
       // the hint was off: stream the row again, from global memory, exactly
       for (int b = tid; b < kBins1; b += kThreads) S.hist1[b] = 0u;
@@ -699,12 +767,14 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       stream_row_exact<false>(S, p, r, nq, g, timed_out, par);
       cbar();
       n = S.count;
+      set_regions_contiguous(S, n);
+      cbar();
     }
     // ---- selection, next row's hint, emission
     Rule hint;
     uint32_t hint_ok = 0u;
     const uint32_t hr = S.hint_rank;
-    const Rule sel = select_buffer(S, n, k, rule_low_bin(S.rule), hr, &hint, &hint_ok, par);
+    const Rule sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par);
     if (tid == 0 && hr != 0u) {
       if (hint_ok) {
         S.hint = hint;
@@ -716,7 +786,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
         S.hint_valid = 1u;
       }
     }
-    emit_selected(S, p, r, row, sel, n, par);
+    emit_selected(S, p, r, row, sel, par);
   }
 
   // (the producer warp joins this last block-wide vote)
