@@ -348,6 +348,7 @@ def run_reference(a, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+KERNEL_NAMES = {1: "topk_multipass_kernel", 2: "topk_stream_kernel", 3: "topk_pipe_kernel"}
 METRIC = "packed top-k rows/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
 
 
@@ -411,7 +412,7 @@ def main():
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
                          if peaks["source"] == "measured" else "fallback 6.4 TB/s",
                          "algorithmic_bytes_per_launch": r["alg_bytes"],
-                         "kernel": "topk_stream_kernel" if plan["path"] == 2 else "topk_multipass_kernel"},
+                         "kernel": KERNEL_NAMES.get(plan["path"], "?")},
             "gpu_launches": a.steps,
             "clocks": r["clocks"],
             "e2e": r["e2e"],

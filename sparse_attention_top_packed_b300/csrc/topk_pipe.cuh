@@ -10,7 +10,7 @@
 // persistent grid):
 //
 //  * Load.  The CTA's windows, row after row, stream through a ring of
-//    kStages shared-memory stages filled by 1-D TMA bulk copies (8 KB each,
+//    kStages shared-memory stages filled by 1-D TMA bulk copies (16 KB each,
 //    L2 evict-first: every byte is read once).  A window is copied from its
 //    start rounded down to 16 bytes; lanes before the start and past the end
 //    are masked in registers (section 2 of the page, without writing the
@@ -21,7 +21,7 @@
 //    flight while a row is finished.  The consumer warps synchronise among
 //    themselves with named barrier 1, never with the producer.
 //
-//  * Admission.  Each thread takes 8 floats of a chunk and keeps those at or
+//  * Admission.  Each thread takes 16 floats of a chunk and keeps those at or
 //    above the admission threshold, a lower bound on the row's k-th largest
 //    key: one float compare per element.  Kept elements (order-preserving
 //    key, window index) go to a candidate buffer of kCap entries.
@@ -65,10 +65,11 @@ namespace pipe {
 constexpr int kThreads = 256;              // consumer threads (warps 0-7)
 constexpr int kWarps = kThreads / 32;
 constexpr int kBlock = kThreads + 32;      // + the producer warp
-constexpr int kChunkBytes = 8192;
-constexpr int kChunkQuads = kChunkBytes / 16;  // 512
-constexpr int kChunkElems = kChunkBytes / 4;   // 2048
-constexpr int kStages = 6;
+constexpr int kChunkBytes = 16384;
+constexpr int kChunkQuads = kChunkBytes / 16;  // 1024
+constexpr int kQuadsPerThread = kChunkQuads / kThreads;  // 4: quads tid + u * kThreads
+constexpr int kHalfElems = kChunkQuads * 2;    // exact mode admits a chunk in two halves of 2048
+constexpr int kStages = 3;
 constexpr int kKMax = 2048;
 constexpr int kCap = 4096;                 // candidate buffer entries
 constexpr int kRegion = kCap / kWarps;     // fast mode: one region of the buffer per warp
@@ -78,9 +79,9 @@ constexpr int kSegBits = kBins1 * 32;      // bitmap indices per emission segmen
 constexpr uint32_t kMaskBin = 0xFFF00000u;  // key bits of a level-1 bin
 constexpr uint32_t kMaskSub = 0xFFFFFC00u;  // key bits of a level-2 sub-bin
 
-static_assert(kChunkQuads == 2 * kThreads, "each thread takes two quads of a chunk");
-// After an exact compaction the buffer holds k entries; a whole chunk must fit.
-static_assert(kCap - kKMax >= kChunkElems, "candidate buffer too small for k + one chunk");
+static_assert(kQuadsPerThread == 4, "each thread takes four quads of a chunk");
+// After an exact compaction the buffer holds k entries; a half chunk must fit.
+static_assert(kCap - kKMax >= kHalfElems, "candidate buffer too small for k + half a chunk");
 static_assert(kBins2 >= kKMax, "the output staging row reuses the level-2 histogram");
 
 // Admission / selection rule on the pair (key, nj = ~j): an element passes
@@ -437,25 +438,80 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   cbar();
 }
 
-// Takes this thread's 8 floats of the row's chunk c: from ring chunk g, or
-// straight from global memory.  A ring stage must then be given back with
+// Takes this thread's 16 floats of the row's chunk (quads cq + tid + u * kThreads,
+// u < 4; x[4u + v] is element v of quad u): from ring chunk g, or straight
+// from global memory.  A ring stage must then be given back with
 // release_chunk once the values have been used.
 template <bool kRing>
-__device__ __forceinline__ void take_chunk(Shared& S, const Row& r, int64_t nq, int64_t q0, uint32_t g,
-                                           bool& timed_out, float x[8]) {
-  float4 v0, v1;
+__device__ __forceinline__ void take_chunk(Shared& S, const Row& r, int64_t nq, int64_t cq, uint32_t g,
+                                           bool& timed_out, float x[16]) {
+  float4 v[kQuadsPerThread];
   if constexpr (kRing) {
     const uint32_t s = g % kStages;
     if (!timed_out && !mbar_wait_bounded(&S.full[s], (g / kStages) & 1u)) timed_out = true;
-    v0 = S.ring[s][threadIdx.x];
-    v1 = S.ring[s][threadIdx.x + kThreads];
+#pragma unroll
+    for (int u = 0; u < kQuadsPerThread; ++u) v[u] = S.ring[s][threadIdx.x + u * kThreads];
   } else {
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    v0 = q0 < nq ? __ldg(r.base4 + q0) : z;
-    v1 = q0 + kThreads < nq ? __ldg(r.base4 + q0 + kThreads) : z;
+#pragma unroll
+    for (int u = 0; u < kQuadsPerThread; ++u) {
+      const int64_t q = cq + threadIdx.x + u * kThreads;
+      v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
-  x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
-  x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+#pragma unroll
+  for (int u = 0; u < kQuadsPerThread; ++u) {
+    x[4 * u] = v[u].x;
+    x[4 * u + 1] = v[u].y;
+    x[4 * u + 2] = v[u].z;
+    x[4 * u + 3] = v[u].w;
+  }
+}
+
+// Exact mode's view of a chunk: the thread's quads 2h and 2h + 1 (8 floats)
+// of half h, read from the ring stage of chunk g (already waited for) or from
+// global memory.
+template <bool kRing>
+__device__ __forceinline__ void take_half(const Shared& S, const Row& r, int64_t nq, int64_t cq, uint32_t g,
+                                          int h, float x[8]) {
+  float4 v[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int qi = threadIdx.x + (2 * h + u) * kThreads;
+    if constexpr (kRing) {
+      v[u] = S.ring[g % kStages][qi];
+    } else {
+      const int64_t q = cq + qi;
+      v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  x[0] = v[0].x; x[1] = v[0].y; x[2] = v[0].z; x[3] = v[0].w;
+  x[4] = v[1].x; x[5] = v[1].y; x[6] = v[1].z; x[7] = v[1].w;
+}
+
+// x[e] for a run-time e in [0, 8), as a tree of selects (indexing the array
+// with a run-time value would move it to local memory).
+__device__ __forceinline__ float pick8(const float x[8], int e) {
+  const float a = (e & 1) ? x[1] : x[0], b = (e & 1) ? x[3] : x[2];
+  const float c = (e & 1) ? x[5] : x[4], d = (e & 1) ? x[7] : x[6];
+  const float lo = (e & 2) ? b : a, hi = (e & 2) ? d : c;
+  return (e & 4) ? hi : lo;
+}
+
+__device__ __forceinline__ float pick16(const float x[16], int e) {
+  const float lo = pick8(x, e & 7), hi = pick8(x + 8, e & 7);
+  return (e & 8) ? hi : lo;
+}
+
+// Window index of element e of 8 consecutive x whose first element has index
+// jb0: elements 0-3 are one quad (index jb0 + e), elements 4-7 the quad
+// kThreads further on (index jb0 + 4 * kThreads + e - 4).  index16 extends
+// this to the thread's four quads.
+__device__ __forceinline__ int32_t index8(int64_t jb0, int e) {
+  return (int32_t)(jb0 + (e & 3) + ((e & 4) ? 4 * kThreads : 0));
+}
+
+__device__ __forceinline__ int32_t index16(int64_t jb0, int e) {
+  return (int32_t)(jb0 + (e & 3) + (int64_t)(e >> 2) * 4 * kThreads);
 }
 
 // Gives ring stage g % kStages back to the producer.  The stage's next
@@ -469,9 +525,10 @@ __device__ __forceinline__ void release_chunk(Shared& S, uint32_t g) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(&S.empty[g % kStages]);
 }
 
-// Bit e set when element e of the thread's 8 passes `rule` and lies in the window.
-__device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8], int64_t jb0, int64_t jb1,
-                                               bool edge, int32_t L) {
+// Bit e set when element e of 8 consecutive x (laid out as index8) passes
+// `rule` and lies in the window [0, L).
+__device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8], int64_t jb0, bool edge,
+                                               int32_t L) {
   uint32_t m = 0u;
 #pragma unroll
   for (int e = 0; e < 8; ++e) m |= (x[e] >= rule.tf ? 1u : 0u) << e;
@@ -479,7 +536,7 @@ __device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8
     uint32_t valid = 0u;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int64_t j = (e < 4 ? jb0 + e : jb1 + (e - 4));
+      const int64_t j = jb0 + (e & 3) + ((e & 4) ? 4 * kThreads : 0);
       valid |= (j >= 0 && j < L ? 1u : 0u) << e;
     }
     m &= valid;
@@ -487,21 +544,20 @@ __device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8
   if (rule.exact && m) {
     for (uint32_t mm = m; mm; mm &= mm - 1u) {
       const int e = __ffs(mm) - 1;
-      const int32_t j = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
-      if (!rule_pass(rule, key_of(x[e]), j)) m &= ~(1u << e);
+      if (!rule_pass(rule, key_of(pick8(x, e)), index8(jb0, e))) m &= ~(1u << e);
     }
   }
   return m;
 }
 
-__device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, uint32_t pos, int64_t jb0,
-                                       int64_t jb1) {
+// Exact mode: appends the flagged elements (8 consecutive x) at pos, pos+1, ...
+// and counts them in hist1.
+__device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, uint32_t pos, int64_t jb0) {
   for (uint32_t mm = m; mm; mm &= mm - 1u) {
     const int e = __ffs(mm) - 1;
-    const int32_t j = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
-    const uint32_t key = key_of(x[e]);
+    const uint32_t key = key_of(pick8(x, e));
     S.bkey[pos] = key;
-    S.bj[pos] = j;
+    S.bj[pos] = index8(jb0, e);
     ++pos;
     atomicAdd(&S.hist1[key >> 20], 1u);
   }
@@ -509,8 +565,9 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
 
 // Fast mode: the row's window through the ring with the fixed rule S.rule and
 // no block-wide synchronisation.  Warp w appends to region w of the buffer
-// (kRegion entries), at positions from its ballots; a region that would
-// overflow sets S.overflow (the row is then done again in exact mode).
+// (kRegion entries): in rounds, every lane with a flagged element left writes
+// one, at a position from the round's ballot.  A region that would overflow
+// sets S.overflow (the row is then done again in exact mode).
 __device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t nq, uint32_t& g,
                                                 bool& timed_out) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -522,34 +579,35 @@ __device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t
   uint32_t wcnt = 0;
   bool full = false;
   for (int64_t c = 0; c < nch; ++c, ++g) {
-    const int64_t q0 = c * kChunkQuads + tid;
-    float x[8];
-    take_chunk<true>(S, r, nq, q0, g, timed_out, x);
-    const int64_t jb0 = q0 * 4 - r.head, jb1 = jb0 + 4 * (int64_t)kThreads;
-    const uint32_t m = admit_mask(rule, x, jb0, jb1, c == 0 || c == nch - 1, r.L);
+    const int64_t cq = c * kChunkQuads;
+    float x[16];
+    take_chunk<true>(S, r, nq, cq, g, timed_out, x);
+    const int64_t jb0 = (cq + tid) * 4 - r.head;  // element 0; element e at index16(jb0, e)
+    const bool edge = c == 0 || c == nch - 1;
+    const uint32_t m = admit_mask(rule, x, jb0, edge, r.L) |
+                       (admit_mask(rule, x + 8, jb0 + 8 * kThreads, edge, r.L) << 8);
     release_chunk(S, g);
-    if (full || !__any_sync(0xFFFFFFFFu, m != 0u)) continue;
-    uint32_t b[8], before[8], tot = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      b[e] = __ballot_sync(0xFFFFFFFFu, (m >> e) & 1u);
-      before[e] = tot;
-      tot += __popc(b[e]);
-    }
-    if (wcnt + tot > (uint32_t)kRegion) {
-      full = true;
-      if (lane == 0) S.overflow = 1u;
-      continue;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if ((m >> e) & 1u) {
-        const uint32_t pos = wcnt + before[e] + __popc(b[e] & lt);
-        rkey[pos] = key_of(x[e]);
-        rj[pos] = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
+    if (full) continue;
+    uint32_t mm = m;
+    while (true) {
+      const bool has = mm != 0u;
+      const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
+      if (b == 0u) break;
+      const uint32_t nb = __popc(b);
+      if (wcnt + nb > (uint32_t)kRegion) {
+        full = true;
+        if (lane == 0) S.overflow = 1u;
+        break;
       }
+      if (has) {
+        const int e = __ffs(mm) - 1;
+        mm &= mm - 1u;
+        const uint32_t pos = wcnt + __popc(b & lt);
+        rkey[pos] = key_of(pick16(x, e));
+        rj[pos] = index16(jb0, e);
+      }
+      wcnt += nb;
     }
-    wcnt += tot;
   }
   if (lane == 0) {
     S.rbase[w] = (uint32_t)(w * kRegion);
@@ -558,8 +616,8 @@ __device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t
 }
 
 // Exact mode: the row's window (from the ring, or from global memory) with a
-// rising threshold; the buffer is compacted whenever a chunk would overflow
-// it.  One block-wide vote per chunk.
+// rising threshold; the buffer is compacted whenever a half chunk would
+// overflow it.  One block-wide vote per half chunk.
 template <bool kRing>
 __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, const Row& r, int64_t nq,
                                                  uint32_t& g, bool& timed_out, Par& par) {
@@ -568,43 +626,49 @@ __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, con
   const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
   Rule rule = S.rule;
   for (int64_t c = 0; c < nch; ++c) {
-    const int64_t q0 = c * kChunkQuads + tid;
-    float x[8];
-    take_chunk<kRing>(S, r, nq, q0, g, timed_out, x);
-    const int64_t jb0 = q0 * 4 - r.head, jb1 = jb0 + 4 * (int64_t)kThreads;
-    uint32_t m = admit_mask(rule, x, jb0, jb1, c == 0 || c == nch - 1, r.L);
+    const int64_t cq = c * kChunkQuads;
+    if constexpr (kRing) {
+      if (!timed_out && !mbar_wait_bounded(&S.full[g % kStages], (g / kStages) & 1u)) timed_out = true;
+    }
+    const bool edge = c == 0 || c == nch - 1;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      float xh[8];
+      take_half<kRing>(S, r, nq, cq, g, h, xh);
+      const int64_t jb0 = (cq + tid) * 4 - r.head + (int64_t)h * 8 * kThreads;
+      uint32_t m = admit_mask(rule, xh, jb0, edge, r.L);
+      uint32_t pos;
+      for (int attempt = 0;; ++attempt) {
+        const uint32_t n = __popc(m);
+        const uint32_t incl = warp_incl_scan(n);
+        const uint32_t wsum = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t base = 0u;
+        if (lane == 31) {
+          if (wsum) base = atomicAdd(&S.count, wsum);
+          S.wtot[w] = wsum;
+        }
+        base = __shfl_sync(0xFFFFFFFFu, base, 31);
+        pos = base + incl - n;
+        const bool ovf = cbar_or(wsum != 0u && base + wsum > (uint32_t)kCap);
+        if (!ovf) break;
+        // roll back this half chunk's reservations and raise the threshold
+        uint32_t added = 0;
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i) added += S.wtot[i];
+        const uint32_t held = S.count - added;
+        compact(S, held, k, attempt, par);
+        rule = S.rule;
+        for (uint32_t mm = m; mm; mm &= mm - 1u) {
+          const int e = __ffs(mm) - 1;
+          if (!rule_pass(rule, key_of(pick8(xh, e)), index8(jb0, e))) m &= ~(1u << e);
+        }
+      }
+      append(S, xh, m, pos, jb0);
+    }
     if constexpr (kRing) {
       release_chunk(S, g);
       ++g;
     }
-    uint32_t pos;
-    for (int attempt = 0;; ++attempt) {
-      const uint32_t n = __popc(m);
-      const uint32_t incl = warp_incl_scan(n);
-      const uint32_t wsum = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      uint32_t base = 0u;
-      if (lane == 31) {
-        if (wsum) base = atomicAdd(&S.count, wsum);
-        S.wtot[w] = wsum;
-      }
-      base = __shfl_sync(0xFFFFFFFFu, base, 31);
-      pos = base + incl - n;
-      const bool ovf = cbar_or(wsum != 0u && base + wsum > (uint32_t)kCap);
-      if (!ovf) break;
-      // roll back this chunk's reservations and raise the threshold
-      uint32_t added = 0;
-#pragma unroll
-      for (int i = 0; i < kWarps; ++i) added += S.wtot[i];
-      const uint32_t held = S.count - added;
-      compact(S, held, k, attempt, par);
-      rule = S.rule;
-      for (uint32_t mm = m; mm; mm &= mm - 1u) {
-        const int e = __ffs(mm) - 1;
-        const int32_t j = (int32_t)(e < 4 ? jb0 + e : jb1 + (e - 4));
-        if (!rule_pass(rule, key_of(x[e]), j)) m &= ~(1u << e);
-      }
-    }
-    append(S, x, m, pos, jb0, jb1);
   }
 }
 
