@@ -672,6 +672,44 @@ __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, con
   }
 }
 
+// A row without a hint takes its threshold from kSamples of its own elements:
+// kSamples / 4 quads spread evenly over the window, read from global memory
+// (the same bytes stream through the ring right after).  The threshold is the
+// key prefix of the sample's rank-R element, R = 1.4 k * kSamples / L, so
+// that about 1.4 k of the row's elements reach it.  It is only a guess: if it
+// admits fewer than k elements or overflows the buffer, the row is done
+// again in exact mode.  Windows of at least kSampleMinLen elements only (the
+// sampled quads are then distinct).
+constexpr int kSamples = 4096;
+constexpr int kSampleMinLen = 16384;
+static_assert(kSamples <= kCap, "the sample is ranked in the candidate buffer");
+
+__device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const Row& r, int64_t nq, Par& par) {
+  constexpr int kSampleQuads = kSamples / 4;
+#pragma unroll
+  for (int u = 0; u < kSampleQuads / kThreads; ++u) {
+    const int s = threadIdx.x + u * kThreads;
+    const int64_t q = ((2 * (int64_t)s + 1) * nq) / (2 * kSampleQuads);
+    const float4 v = __ldg(r.base4 + q);
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t j = q * 4 - r.head + e;
+      const bool in = j >= 0 && j < r.L;
+      S.bkey[4 * s + e] = in ? key_of(f[e]) : 0u;  // below every real key
+      S.bj[4 * s + e] = in ? (int32_t)j : 0;
+    }
+  }
+  set_regions_contiguous(S, kSamples);
+  cbar();
+  const int64_t want = (7 * (int64_t)p.k * kSamples) / (5 * (int64_t)r.L) + 1;
+  const uint32_t rank = (uint32_t)min(want, (int64_t)kSamples);
+  const Rule sel = select_buffer(S, kSamples, rank, 0u, nullptr, nullptr, par);
+  cbar();
+  if (threadIdx.x == 0) S.rule = rule_prefix(sel.mk, sel.tk);
+  cbar();
+}
+
 // Writes the buffer entries that pass `sel` (exactly k of them) in ascending
 // window index, through the page transform, to out_row[0, k).
 __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row,
@@ -687,7 +725,7 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
     const int32_t span = (int32_t)min((int64_t)kSegBits, (int64_t)r.L - seg);
     const int32_t nw = (span + 31) >> 5;
     cbar();  // previous users of the bitmap are done
-    for (int i = t; i < nw; i += kThreads) bm[i] = 0u;
+    for (int i = 4 * t; i < nw; i += 4 * kThreads) *reinterpret_cast<uint4*>(bm + i) = make_uint4(0u, 0u, 0u, 0u);
     cbar();
     for (uint32_t i = lane; i < rcnt; i += 32) {
       const int32_t j = S.bj[rbase + i];
@@ -695,7 +733,9 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
         atomicOr(&bm[(j - seg_lo) >> 5], 1u << ((j - seg_lo) & 31));
     }
     cbar();
-    const int32_t wpt = (nw + kThreads - 1) / kThreads;
+    // each thread scans a run of wpt consecutive words; an odd run length
+    // keeps the threads of a warp on different banks
+    const int32_t wpt = ((nw + kThreads - 1) / kThreads) | 1;
     const int32_t w0 = min(t * wpt, nw), w1 = min(w0 + wpt, nw);
     uint32_t cnt = 0;
     for (int32_t i = w0; i < w1; ++i) cnt += __popc(bm[i]);
@@ -786,7 +826,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       uint4* h4 = reinterpret_cast<uint4*>(S.hist1);
       for (int b = tid; b < kBins1 / 4; b += kThreads) h4[b] = make_uint4(0u, 0u, 0u, 0u);
     }
-    const bool fast = S.hint_valid != 0u;  // read by every thread before thread 0 rewrites it below
+    bool fast = S.hint_valid != 0u;  // read by every thread before thread 0 rewrites it below
     cbar();
     if (tid == 0) {
       S.count = 0u;
@@ -807,6 +847,11 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
     }
     cbar();
+    if (!fast && r.L >= kSampleMinLen) {
+      // no hint: estimate a threshold from a sample of the row itself
+      sample_threshold(S, p, r, nq, par);
+      fast = true;
+    }
     if (fast) {
       stream_row_fast(S, r, nq, g, timed_out);
     } else {
