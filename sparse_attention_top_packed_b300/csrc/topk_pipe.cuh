@@ -131,6 +131,7 @@ struct Shared {
   PickOut pick[2];
   uint32_t wtot[kWarps];
   uint32_t rbase[kWarps], rcnt[kWarps];  // the buffer, as one region per warp (see set_regions_*)
+  uint32_t qlist[kWarps][4 * 32];        // fast mode: a warp's quads that may hold candidates
   uint32_t wmin[kWarps], wmax[kWarps];
   uint32_t count;
   uint32_t overflow;  // fast mode: a reservation did not fit
@@ -348,24 +349,29 @@ __device__ __forceinline__ Rule rule_of_pair_prefix(uint64_t M, uint64_t T) {
 // entries reach (the next row's hint): the deepest prefix, at most two digits
 // below the common one, whose bin holds rank r2.  *hint_ok is 0 when fewer
 // than r2 entries are buffered.
+//
+// `ready`: hist2 is all zero and S.wmin / S.wmax hold every region's key
+// range (the fast stream leaves both so); otherwise they are made here.
 __device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, uint32_t r2, Rule* hint,
-                                           uint32_t* hint_ok, Par& par) {
+                                           uint32_t* hint_ok, Par& par, bool ready = false) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
-  // common prefix of the buffered keys
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-  for (uint32_t i = lane; i < cnt; i += 32) {
-    const uint32_t key = S.bkey[base + i];
-    mn = min(mn, key);
-    mx = max(mx, key);
+  if (!ready) {
+    // common prefix of the buffered keys
+    for (uint32_t i = lane; i < cnt; i += 32) {
+      const uint32_t key = S.bkey[base + i];
+      mn = min(mn, key);
+      mx = max(mx, key);
+    }
+    mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if (lane == 0) {
+      S.wmin[w] = mn;
+      S.wmax[w] = mx;
+    }
+    cbar();
   }
-  mn = __reduce_min_sync(0xFFFFFFFFu, mn);
-  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-  if (lane == 0) {
-    S.wmin[w] = mn;
-    S.wmax[w] = mx;
-  }
-  cbar();
 #pragma unroll
   for (int i = 0; i < kWarps; ++i) {
     mn = min(mn, S.wmin[i]);
@@ -381,8 +387,10 @@ __device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, ui
   for (int level = 0; pos > 0; ++level) {
     const int wd = pos < 11 ? pos : 11, sh = pos - wd;
     const uint32_t nb = 1u << wd;
-    for (uint32_t b = threadIdx.x; b < (uint32_t)kBins2; b += kThreads) S.hist2[b] = 0u;
-    cbar();
+    if (level > 0 || !ready) {
+      for (uint32_t b = threadIdx.x; b < (uint32_t)kBins2; b += kThreads) S.hist2[b] = 0u;
+      cbar();
+    }
     for (uint32_t i = lane; i < cnt; i += 32) {
       const uint64_t c = pair_of(S.bkey[base + i], S.bj[base + i]);
       if ((c & M) == T) atomicAdd(&S.hist2[(uint32_t)(c >> sh) & (nb - 1u)], 1u);
@@ -563,55 +571,113 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
   }
 }
 
-// Fast mode: the row's window through the ring with the fixed rule S.rule and
-// no block-wide synchronisation.  Warp w appends to region w of the buffer
-// (kRegion entries): in rounds, every lane with a flagged element left writes
-// one, at a position from the round's ballot.  A region that would overflow
-// sets S.overflow (the row is then done again in exact mode).
+// Fast mode: the row's window through the ring with the fixed rule S.rule
+// (a key prefix: x >= rule.tf decides) and no block-wide synchronisation.
+// Per chunk each thread compares the maximum of each of its 4 quads with the
+// threshold; the warp lists its passing quads (about 1 in 7) in qlist, and
+// then each lane takes one listed quad from the stage and appends its
+// passing elements to the warp's region of the buffer (kRegion entries) at
+// positions from the warp's ballots.  A region that would overflow sets
+// S.overflow (the row is then done again in exact mode).
 __device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t nq, uint32_t& g,
                                                 bool& timed_out) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
-  const Rule rule = S.rule;
+  const float tf = S.rule.tf;
   const uint32_t lt = lanemask_lt();
   uint32_t* rkey = S.bkey + w * kRegion;
   int32_t* rj = S.bj + w * kRegion;
-  uint32_t wcnt = 0;
+  uint32_t* ql = S.qlist[w];
+  const float qnan = __uint_as_float(0x7FC00000u);  // fails every comparison
+  uint32_t wcnt = 0, kmin = 0xFFFFFFFFu, kmax = 0u;
   bool full = false;
-  for (int64_t c = 0; c < nch; ++c, ++g) {
+  uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+  for (int64_t c = 0; c < nch; ++c) {
     const int64_t cq = c * kChunkQuads;
-    float x[16];
-    take_chunk<true>(S, r, nq, cq, g, timed_out, x);
-    const int64_t jb0 = (cq + tid) * 4 - r.head;  // element 0; element e at index16(jb0, e)
+    if (!mbar_try_wait(&S.full[s], ph) && !timed_out && !mbar_wait_bounded(&S.full[s], ph)) timed_out = true;
+    const float4* st = S.ring[s];
     const bool edge = c == 0 || c == nch - 1;
-    const uint32_t m = admit_mask(rule, x, jb0, edge, r.L) |
-                       (admit_mask(rule, x + 8, jb0 + 8 * kThreads, edge, r.L) << 8);
-    release_chunk(S, g);
-    if (full) continue;
-    uint32_t mm = m;
-    while (true) {
-      const bool has = mm != 0u;
-      const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
-      if (b == 0u) break;
-      const uint32_t nb = __popc(b);
-      if (wcnt + nb > (uint32_t)kRegion) {
-        full = true;
-        if (lane == 0) S.overflow = 1u;
-        break;
+    uint32_t B[kQuadsPerThread];
+    bool pass[kQuadsPerThread];
+#pragma unroll
+    for (int u = 0; u < kQuadsPerThread; ++u) {
+      float4 v = st[tid + u * kThreads];
+      if (edge) {
+        const int64_t j = (cq + tid + u * kThreads) * 4 - r.head;
+        if (!(j >= 0 && j < r.L)) v.x = qnan;
+        if (!(j + 1 >= 0 && j + 1 < r.L)) v.y = qnan;
+        if (!(j + 2 >= 0 && j + 2 < r.L)) v.z = qnan;
+        if (!(j + 3 >= 0 && j + 3 < r.L)) v.w = qnan;
       }
-      if (has) {
-        const int e = __ffs(mm) - 1;
-        mm &= mm - 1u;
-        const uint32_t pos = wcnt + __popc(b & lt);
-        rkey[pos] = key_of(pick16(x, e));
-        rj[pos] = index16(jb0, e);
+      pass[u] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) >= tf;  // fmaxf ignores a NaN operand
+      B[u] = __ballot_sync(0xFFFFFFFFu, pass[u]);
+    }
+    const uint32_t P1 = __popc(B[0]), P2 = P1 + __popc(B[1]), P3 = P2 + __popc(B[2]);
+    const uint32_t T = P3 + __popc(B[3]);
+    if (T != 0u && !full) {
+      if (pass[0]) ql[__popc(B[0] & lt)] = (uint32_t)tid;
+      if (pass[1]) ql[P1 + __popc(B[1] & lt)] = (uint32_t)tid + kThreads;
+      if (pass[2]) ql[P2 + __popc(B[2] & lt)] = (uint32_t)tid + 2 * kThreads;
+      if (pass[3]) ql[P3 + __popc(B[3] & lt)] = (uint32_t)tid + 3 * kThreads;
+      __syncwarp();
+      for (uint32_t base = 0; base < T && !full; base += 32) {
+        const uint32_t i = base + lane;
+        uint32_t m4 = 0u, qi = 0u;
+        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < T) {
+          qi = ql[i];
+          q4 = st[qi];
+          const int64_t j = (cq + qi) * 4 - r.head;
+          m4 = (q4.x >= tf ? 1u : 0u) | (q4.y >= tf ? 2u : 0u) | (q4.z >= tf ? 4u : 0u) | (q4.w >= tf ? 8u : 0u);
+          if (edge) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (!(j + e >= 0 && j + e < r.L)) m4 &= ~(1u << e);
+          }
+        }
+        const int32_t jq = (int32_t)((cq + qi) * 4 - r.head);  // used only for in-window elements
+        while (true) {
+          const bool has = m4 != 0u;
+          const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
+          if (b == 0u) break;
+          const uint32_t nb = __popc(b);
+          if (wcnt + nb > (uint32_t)kRegion) {
+            full = true;
+            if (lane == 0) S.overflow = 1u;
+            break;
+          }
+          if (has) {
+            const int e = __ffs(m4) - 1;
+            m4 &= m4 - 1u;
+            const float val = (e & 2) ? ((e & 1) ? q4.w : q4.z) : ((e & 1) ? q4.y : q4.x);
+            const uint32_t key = key_of(val);
+            const uint32_t pos = wcnt + __popc(b & lt);
+            rkey[pos] = key;
+            rj[pos] = jq + e;
+            kmin = min(kmin, key);
+            kmax = max(kmax, key);
+          }
+          wcnt += nb;
+        }
       }
-      wcnt += nb;
+    }
+    // every read of the stage is done: give it back
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+    ++g;
+    if (++s == (uint32_t)kStages) {
+      s = 0u;
+      ph ^= 1u;
     }
   }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
   if (lane == 0) {
     S.rbase[w] = (uint32_t)(w * kRegion);
     S.rcnt[w] = wcnt;
+    S.wmin[w] = kmin;
+    S.wmax[w] = kmax;
   }
 }
 
@@ -706,14 +772,16 @@ __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const 
   const uint32_t rank = (uint32_t)min(want, (int64_t)kSamples);
   const Rule sel = select_buffer(S, kSamples, rank, 0u, nullptr, nullptr, par);
   cbar();
+  for (uint32_t b = threadIdx.x; b < (uint32_t)kBins2; b += kThreads) S.hist2[b] = 0u;
   if (threadIdx.x == 0) S.rule = rule_prefix(sel.mk, sel.tk);
   cbar();
 }
 
 // Writes the buffer entries that pass `sel` (exactly k of them) in ascending
 // window index, through the page transform, to out_row[0, k).
+// `clean`: the bitmap (hist1) is already all zero for the first segment.
 __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row,
-                                              const Rule sel, Par& par) {
+                                              const Rule sel, Par& par, bool clean) {
   const int t = threadIdx.x, lane = t & 31;
   const uint32_t rbase = S.rbase[t >> 5], rcnt = S.rcnt[t >> 5];
   uint32_t* bm = S.hist1;
@@ -724,32 +792,50 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
     const int32_t seg_lo = (int32_t)seg;
     const int32_t span = (int32_t)min((int64_t)kSegBits, (int64_t)r.L - seg);
     const int32_t nw = (span + 31) >> 5;
-    cbar();  // previous users of the bitmap are done
-    for (int i = 4 * t; i < nw; i += 4 * kThreads) *reinterpret_cast<uint4*>(bm + i) = make_uint4(0u, 0u, 0u, 0u);
-    cbar();
+    if (seg > 0 || !clean) {
+      cbar();  // previous users of the bitmap are done
+      for (int i = 4 * t; i < nw; i += 4 * kThreads) *reinterpret_cast<uint4*>(bm + i) = make_uint4(0u, 0u, 0u, 0u);
+      cbar();
+    }
     for (uint32_t i = lane; i < rcnt; i += 32) {
       const int32_t j = S.bj[rbase + i];
       if (j >= seg_lo && j - seg_lo < span && rule_pass(sel, S.bkey[rbase + i], j))
         atomicOr(&bm[(j - seg_lo) >> 5], 1u << ((j - seg_lo) & 31));
     }
     cbar();
-    // each thread scans a run of wpt consecutive words; an odd run length
-    // keeps the threads of a warp on different banks
-    const int32_t wpt = ((nw + kThreads - 1) / kThreads) | 1;
-    const int32_t w0 = min(t * wpt, nw), w1 = min(w0 + wpt, nw);
+    // warp w owns a run of whole 32-word rounds of the bitmap; in each round
+    // lane l takes word round * 32 + l, so the ranks come from warp scans
+    const int warp = t >> 5;
+    const int32_t wpw = ((nw + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+    const int32_t a0 = min(warp * wpw, nw), a1 = min(a0 + wpw, nw);
     uint32_t cnt = 0;
-    for (int32_t i = w0; i < w1; ++i) cnt += __popc(bm[i]);
-    uint32_t total;
-    uint32_t pos = out_base + cta_excl_scan(cnt, par.scratch(S), total);
-    for (int32_t i = w0; i < w1; ++i) {
-      for (uint32_t b = bm[i]; b; b &= b - 1u) {
+    for (int32_t i = a0 + lane; i < a1; i += 32) cnt += __popc(bm[i]);
+    const uint32_t wsum = __reduce_add_sync(0xFFFFFFFFu, cnt);
+    if (lane == 0) S.wtot[warp] = wsum;
+    cbar();
+    uint32_t pos0 = out_base, total = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+      const uint32_t v = S.wtot[i];
+      pos0 += i < warp ? v : 0u;
+      total += v;
+    }
+    for (int32_t i0 = a0; i0 < a1; i0 += 32) {
+      const int32_t i = i0 + lane;
+      const uint32_t word = i < a1 ? bm[i] : 0u;
+      const uint32_t c = __popc(word);
+      const uint32_t incl = warp_incl_scan(c);
+      uint32_t pos = pos0 + incl - c;
+      for (uint32_t b = word; b; b &= b - 1u) {
         if (pos < k)
           stage[pos] = seg_lo + i * 32 + (__ffs(b) - 1);
         else
           atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
         ++pos;
       }
+      pos0 += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
+    cbar();  // S.wtot is read again in the next segment
     out_base += total;
   }
   cbar();
@@ -813,6 +899,10 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
 
   Par par;
   uint32_t g = 0;  // chunks taken from the ring
+  // Between rows hist1 (histogram / bitmap) and hist2 (histogram / staging
+  // row) are cleared while the next row streams; they start clean.
+  for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
+  for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
 
   for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
     const Row r = load_row(p, (int32_t)row);
@@ -821,18 +911,12 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       continue;
     }
     const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
-    // ---- row set-up: empty buffer and histogram, threshold from the hint
-    {
-      uint4* h4 = reinterpret_cast<uint4*>(S.hist1);
-      for (int b = tid; b < kBins1 / 4; b += kThreads) h4[b] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    bool fast = S.hint_valid != 0u;  // read by every thread before thread 0 rewrites it below
-    cbar();
+    // ---- row set-up: threshold from the hint (written at the previous row's end)
+    bool fast = S.hint_valid != 0u;
     if (tid == 0) {
       S.count = 0u;
       S.overflow = 0u;
       S.rule = fast ? S.hint : rule_all();
-      S.hint_valid = 0u;
       // the CTA's next row that needs a selection, for the hint
       int32_t nl = 0;
       for (int64_t rr = row + gridDim.x; rr < p.num_rows; rr += gridDim.x) {
@@ -846,7 +930,10 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       // rank of about 1.25 k in a row of the next row's length
       S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
     }
-    cbar();
+    cbar();  // also: every thread is done with the previous row's hist1 / hist2
+    for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
+    for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
+    if (!fast && r.L < kSampleMinLen) cbar();  // exact mode counts into hist1 at once
     if (!fast && r.L >= kSampleMinLen) {
       // no hint: estimate a threshold from a sample of the row itself
       sample_threshold(S, p, r, nq, par);
@@ -863,7 +950,10 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     uint32_t n = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) n += S.rcnt[i];
-    if (n < k || S.overflow) {
+    const bool redo = n < k || S.overflow;
+    // a fast row that stands: hist1 / hist2 untouched since the set-up, key ranges known
+    const bool ready = fast && !redo;
+    if (redo) {
       // the hint was off: stream the row again, from global memory, exactly
       for (int b = tid; b < kBins1; b += kThreads) S.hist1[b] = 0u;
       cbar();
@@ -883,7 +973,8 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     Rule hint;
     uint32_t hint_ok = 0u;
     const uint32_t hr = S.hint_rank;
-    const Rule sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par);
+    const Rule sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par, ready);
+    if (tid == 0) S.hint_valid = 0u;
     if (tid == 0 && hr != 0u) {
       if (hint_ok) {
         S.hint = hint;
@@ -895,7 +986,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
         S.hint_valid = 1u;
       }
     }
-    emit_selected(S, p, r, row, sel, par);
+    emit_selected(S, p, r, row, sel, par, ready);
   }
 
   // (the producer warp joins this last block-wide vote)
