@@ -273,9 +273,11 @@ def run_e2e(a, w, device) -> dict:
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
 
 
-def cpu_baseline(w, target_s: float = 12.0, max_rows: int = 4096) -> dict:
+def cpu_baseline(w, target_s: float = 12.0) -> dict:
     """The CPU oracle, as it stands, on a bounded sample of the workload's rows
-    (windows copied to the host first, outside the timing), all host cores."""
+    (windows copied to the host first, outside the timing), all host cores.
+    A small probe sizes the sample to about `target_s` seconds of oracle work,
+    or the whole workload when that takes less."""
     from oracle import default_threads, topk_packed_reference
     from sparse_attention_top_packed_b300.workloads import gather_windows, sample_rows
 
@@ -292,10 +294,10 @@ def cpu_baseline(w, target_s: float = 12.0, max_rows: int = 4096) -> dict:
                               w.pt_stride, w.page_size, w.k, nthreads=cores)
         return time.perf_counter() - t0, int(rows.numel())
 
-    n = max(cores, 8)
-    dt, n = run_rows(n)
-    if dt < target_s / 4 and n < w.num_rows:
-        n2 = int(min(w.num_rows, max_rows, n * max(1.0, target_s / max(dt, 1e-3))))
+    dt, n = run_rows(min(w.num_rows, max(2 * cores, 16)))
+    if n < w.num_rows:
+        want = int(n * target_s / max(dt, 1e-4))
+        n2 = min(w.num_rows, max(n, want))
         if n2 > n:
             dt, n = run_rows(n2)
     return {"value": n / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
