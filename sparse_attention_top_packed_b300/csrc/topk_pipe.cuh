@@ -1,4 +1,4 @@
-// Pipelined single-pass kernel of the packed top-k + page transform (sm_103a).
+// Warp-block kernel of the packed top-k + page transform (sm_103a).
 //
 // Operation (page "[sglang] [AMD ROCm] GLM-5.x Prefill 성능을 66% 끌어올린 Top-K 커널
 // 최적화 분석", sglang PR #37889, Intro and sections 1-2): row i's window is
@@ -6,55 +6,47 @@
 // the k largest are kept (a tie goes to the lower j), listed in ascending j and
 // mapped through the row's page-table row; -1 pads windows shorter than k.
 //
-// Design (one CTA per row at a time, two CTAs per SM, rows strided over the
-// persistent grid):
+// Design (one CTA of 8 warps per row at a time, two CTAs per SM, rows strided
+// over the persistent grid):
 //
-//  * Load.  The CTA's windows, row after row, stream through a ring of
-//    kStages shared-memory stages filled by 1-D TMA bulk copies (16 KB each,
-//    L2 evict-first: every byte is read once).  A window is copied from its
-//    start rounded down to 16 bytes; lanes before the start and past the end
-//    are masked in registers (section 2 of the page, without writing the
-//    buffer).  Each stage has a "full" barrier (the copy landed) and an
-//    "empty" barrier (all 8 consumer warps took the chunk into registers).
-//    A ninth warp only produces: it refills each stage as soon as it is
-//    empty, running ahead across rows, so the next row's first chunks are in
-//    flight while a row is finished.  The consumer warps synchronise among
-//    themselves with named barrier 1, never with the producer.
+//  * Load.  A row's window, from its start rounded down to 16 bytes, is cut
+//    into 2 KB chunks; warp w owns the w-th eighth of them, a contiguous block.
+//    Each warp streams its blocks, row after row, through its own ring of
+//    kWStages shared-memory stages filled by 1-D TMA bulk copies (L2
+//    evict-first: every byte is read once).  Lane 0 refills a stage as soon as
+//    the warp has taken it, so each warp keeps its next chunks -- also those of
+//    its block of the next row -- in flight while a row is finished.  Lanes
+//    before the window start and past its end are masked in registers
+//    (section 2 of the page, without writing the buffer).
 //
-//  * Admission.  Each thread takes 16 floats of a chunk and keeps those at or
-//    above the admission threshold, a lower bound on the row's k-th largest
-//    key: one float compare per element.  Kept elements (order-preserving
-//    key, window index) go to a candidate buffer of kCap entries.
+//  * Admission.  Every row streams with a fixed threshold, a guess at a lower
+//    bound of its k-th largest key: from the CTA's previous row (the key that
+//    about 1.25 k of its candidates reach, scaled to the new length), or from
+//    a strided sample of the row itself.  Each lane takes 4 consecutive quads
+//    of a chunk and compares each quad's maximum with the threshold; the warp
+//    lists its passing quads (about 1 in 7) in window order, each lane takes
+//    one listed quad and appends its passing elements (order-preserving key,
+//    window index) to the warp's region of the candidate buffer at positions
+//    from a warp scan.  A region therefore holds its candidates in ascending
+//    window index, and the regions follow each other in warp order.  Each
+//    candidate is also counted in a fine histogram: 2047 equal key bins above
+//    the threshold, sized so that the k-th largest key lands in about bin 384.
 //
-//  * Threshold.  When the CTA's previous row gives a hint -- the key prefix
-//    that about 1.25 k of its candidates reach, scaled to the new row's
-//    length -- the row streams with that fixed threshold and no block-wide
-//    synchronisation ("fast" mode): each warp appends to its own region of
-//    the buffer at positions from warp ballots, with no shared atomics.  If
-//    that admits fewer than k elements or overflows a region, the row is
-//    streamed again from global memory in "exact" mode.  Without a hint
-//    (first row of a CTA, a much shorter row) the row streams in exact mode
-//    from the ring: one shared buffer, a 4096-bin histogram of the key's top
-//    12 bits kept as elements arrive, and a threshold that starts at -inf and,
-//    whenever a chunk would overflow the buffer, rises to the histogram bin of
-//    the k-th largest buffered key, or to the exact k-th largest (key, index)
-//    pair.  Any threshold at or below the k-th largest key of the elements
-//    seen so far is safe, so no selected element is ever dropped.
+//  * Selection.  The bin of the k-th largest key comes from the fine
+//    histogram; the few candidates in that bin are ranked by (key, ~j) in one
+//    warp, which gives the exact k-th largest pair -- a tie goes to the lower
+//    j.  When the histogram cannot settle it (the rank lies above its range, or
+//    its bin is crowded), a radix select over the buffer does.
 //
-//  * Selection.  A radix select on the buffer orders candidates by the
-//    64-bit pair (key, ~j): larger key first, then lower j.  The candidates'
-//    keys share a prefix (the bits where the smallest and largest agree); the
-//    digits, 11 bits each, start right below it, so the first level already
-//    spreads the candidates over up to 2048 bins.  Levels go on into ~j only
-//    for equal keys.  Pairs are unique, so the result is exactly k
-//    candidates, whatever the ties.
+//  * Emission.  Selected entries' output positions are prefix counts over the
+//    ordered regions: the page transform of section 1 is applied and the row is
+//    written in ascending order with warp ballots, no sorting.
 //
-//  * Emission.  The selected window indices are set in a bitmap of the window
-//    (reusing the histogram's shared memory, 131072 indices per segment); a
-//    block scan of the word popcounts puts the indices, in ascending j, into a
-//    staging row; then every thread maps k / 256 of them through the page
-//    transform of section 1 (independent loads) and the row leaves with
-//    coalesced stores.
+//  * Safety net.  If a threshold admitted fewer than k elements, or a region
+//    overflowed, the row is streamed again from global memory in exact mode: a
+//    threshold that starts at -inf and only ever rises to the k-th largest key
+//    of the elements seen so far (so no selected element is dropped), a shared
+//    buffer compacted when full, and a bitmap-ordered emission.
 #pragma once
 
 #include "topk_device.cuh"
@@ -62,27 +54,30 @@
 namespace topk {
 namespace pipe {
 
-constexpr int kThreads = 256;              // consumer threads (warps 0-7)
+constexpr int kThreads = 256;              // 8 warps
 constexpr int kWarps = kThreads / 32;
-constexpr int kBlock = kThreads + 32;      // + the producer warp
-constexpr int kChunkBytes = 16384;
-constexpr int kChunkQuads = kChunkBytes / 16;  // 1024
+constexpr int kBlock = kThreads;
+constexpr int kWChunkQuads = 128;          // 2 KB: 4 consecutive quads per lane
+constexpr int kWStages = 3;                // per-warp ring
+constexpr int kChunkQuads = 1024;          // exact mode reads global memory 16 KB at a time
 constexpr int kQuadsPerThread = kChunkQuads / kThreads;  // 4: quads tid + u * kThreads
 constexpr int kHalfElems = kChunkQuads * 2;    // exact mode admits a chunk in two halves of 2048
-constexpr int kStages = 3;
 constexpr int kKMax = 2048;
 constexpr int kCap = 4096;                 // candidate buffer entries
 constexpr int kRegion = kCap / kWarps;     // fast mode: one region of the buffer per warp
-constexpr int kBins1 = 4096;               // key bits [20, 32)
-constexpr int kBins2 = 2048;               // refinement levels (<= 11 bits)
+constexpr int kBins1 = 4096;               // exact mode: key bits [20, 32)
+constexpr int kBins2 = 2048;               // refinement levels (<= 11 bits) / fine histogram
+constexpr int kFineTop = kBins2 - 1;       // fine bins [0, kFineTop); keys above count apart
 constexpr int kSegBits = kBins1 * 32;      // bitmap indices per emission segment
 constexpr uint32_t kMaskBin = 0xFFF00000u;  // key bits of a level-1 bin
 constexpr uint32_t kMaskSub = 0xFFFFFC00u;  // key bits of a level-2 sub-bin
 
-static_assert(kQuadsPerThread == 4, "each thread takes four quads of a chunk");
+static_assert(kQuadsPerThread == 4, "exact mode: each thread takes four quads of a chunk");
 // After an exact compaction the buffer holds k entries; a half chunk must fit.
 static_assert(kCap - kKMax >= kHalfElems, "candidate buffer too small for k + half a chunk");
 static_assert(kBins2 >= kKMax, "the output staging row reuses the level-2 histogram");
+// a block of at most one chunk per warp always fits its region
+static_assert(kWChunkQuads * 4 <= kRegion, "a whole chunk must fit a warp's region");
 
 // Admission / selection rule on the pair (key, nj = ~j): an element passes
 // iff (key & mk, nj & mj) >= (tk, tj) lexicographically.  tf is a float with
@@ -120,37 +115,33 @@ struct PickOut {
 };
 
 struct Shared {
-  float4 ring[kStages][kChunkQuads];
+  float4 wring[kWarps][kWStages][kWChunkQuads];  // per-warp TMA rings
   uint32_t bkey[kCap];
   int32_t bj[kCap];
-  uint32_t hist1[kBins1];  // also the emission bitmap
-  uint32_t hist2[kBins2];  // also the output staging row
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint32_t hist1[kBins1];  // exact mode: histogram; then the emission bitmap
+  uint32_t hist2[kBins2];  // fine histogram / refinement levels / staging row
+  uint64_t wfull[kWarps][kWStages];
+  uint32_t qlist[kWarps][4 * 32];  // a warp's quads that may hold candidates
   uint32_t scratch[2][kWarps];
   PickOut pick[2];
   uint32_t wtot[kWarps];
-  uint32_t rbase[kWarps], rcnt[kWarps];  // the buffer, as one region per warp (see set_regions_*)
-  uint32_t qlist[kWarps][4 * 32];        // fast mode: a warp's quads that may hold candidates
-  uint32_t wmin[kWarps], wmax[kWarps];
-  uint32_t count;
-  uint32_t overflow;  // fast mode: a reservation did not fit
+  uint32_t rbase[kWarps], rcnt[kWarps];  // the buffer, as one region per warp
+  uint32_t wmin[kWarps], wmax[kWarps], wtop[kWarps];
+  uint32_t res_key[32];
+  int32_t res_j[32];
+  uint32_t res_n;
+  uint32_t pad0_;
+  uint64_t sel_T;     // the k-th largest pair, when resolved in the fine bin
+  uint32_t count;     // exact mode: entries in the shared buffer
+  uint32_t overflow;  // fast mode: a region overflowed
   Rule rule;          // admission rule of the current row
   Rule hint;          // admission rule proposed for the next row
   uint32_t hint_valid;
   uint32_t hint_rank;  // rank the next row's hint should reach in this row (0: none)
   int32_t next_len;    // window length of the CTA's next row that needs a selection
-  uint32_t pad_;
-};
-
-// Thread 0's cursor over the CTA's chunk sequence: the windows of rows
-// blockIdx.x, blockIdx.x + gridDim.x, ... (rows with seq_len <= k have none),
-// each cut into kChunkBytes pieces.
-struct Cursor {
-  const char* src;
-  int64_t left;
-  int64_t row;
-  uint32_t issued;
+  uint32_t fh_tk;      // fine histogram of this row: bins of 2^fh_sh keys from fh_tk
+  uint32_t fh_sh;
+  uint32_t hint_sh;    // fine shift proposed for the next row
 };
 
 struct Par {
@@ -191,34 +182,6 @@ __device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* scratch,
   const uint32_t wexcl = __shfl_sync(0xFFFFFFFFu, wincl - wt, warp);
   total = __shfl_sync(0xFFFFFFFFu, wincl, kWarps - 1);
   return wexcl + incl - v;
-}
-
-// The producer lane: issues chunk number cur.issued of the sequence into its stage,
-// after the stage's previous chunk was taken by every consumer warp.  Returns false
-// past the last chunk.
-__device__ __forceinline__ bool issue_next(Shared& S, Cursor& cur, const Params& p, uint64_t policy,
-                                           bool& timed_out) {
-  while (cur.left == 0) {
-    if (cur.row >= p.num_rows) return false;
-    cur.row += gridDim.x;
-    if (cur.row >= p.num_rows) return false;
-    const Row r = load_row(p, (int32_t)cur.row);
-    if (r.L <= p.k) continue;
-    cur.src = reinterpret_cast<const char*>(r.base4);
-    cur.left = (((int64_t)r.L + r.head + 3) >> 2) * 16;
-  }
-  const uint32_t c = cur.issued, s = c % kStages;
-  if (c >= (uint32_t)kStages) {
-    const uint32_t prev = c - kStages;
-    if (!timed_out && !mbar_wait_bounded(&S.empty[s], (prev / kStages) & 1u)) timed_out = true;
-  }
-  const uint32_t nb = (uint32_t)min((int64_t)kChunkBytes, cur.left);
-  mbar_arrive_expect_tx(&S.full[s], nb);
-  bulk_copy_g2s(&S.ring[s][0], cur.src, nb, &S.full[s], policy);
-  cur.src += nb;
-  cur.left -= nb;
-  ++cur.issued;
-  return true;
 }
 
 // Block-wide bucket pick over NB bins (bins below `lo` count as empty): the
@@ -446,51 +409,14 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   cbar();
 }
 
-// Takes this thread's 16 floats of the row's chunk (quads cq + tid + u * kThreads,
-// u < 4; x[4u + v] is element v of quad u): from ring chunk g, or straight
-// from global memory.  A ring stage must then be given back with
-// release_chunk once the values have been used.
-template <bool kRing>
-__device__ __forceinline__ void take_chunk(Shared& S, const Row& r, int64_t nq, int64_t cq, uint32_t g,
-                                           bool& timed_out, float x[16]) {
-  float4 v[kQuadsPerThread];
-  if constexpr (kRing) {
-    const uint32_t s = g % kStages;
-    if (!timed_out && !mbar_wait_bounded(&S.full[s], (g / kStages) & 1u)) timed_out = true;
-#pragma unroll
-    for (int u = 0; u < kQuadsPerThread; ++u) v[u] = S.ring[s][threadIdx.x + u * kThreads];
-  } else {
-#pragma unroll
-    for (int u = 0; u < kQuadsPerThread; ++u) {
-      const int64_t q = cq + threadIdx.x + u * kThreads;
-      v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < kQuadsPerThread; ++u) {
-    x[4 * u] = v[u].x;
-    x[4 * u + 1] = v[u].y;
-    x[4 * u + 2] = v[u].z;
-    x[4 * u + 3] = v[u].w;
-  }
-}
-
-// Exact mode's view of a chunk: the thread's quads 2h and 2h + 1 (8 floats)
-// of half h, read from the ring stage of chunk g (already waited for) or from
-// global memory.
-template <bool kRing>
-__device__ __forceinline__ void take_half(const Shared& S, const Row& r, int64_t nq, int64_t cq, uint32_t g,
-                                          int h, float x[8]) {
+// Exact mode's view of a chunk of kChunkQuads quads: the thread's quads 2h and
+// 2h + 1 (8 floats) of half h, read from global memory.
+__device__ __forceinline__ void take_half(const Row& r, int64_t nq, int64_t cq, int h, float x[8]) {
   float4 v[2];
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
-    const int qi = threadIdx.x + (2 * h + u) * kThreads;
-    if constexpr (kRing) {
-      v[u] = S.ring[g % kStages][qi];
-    } else {
-      const int64_t q = cq + qi;
-      v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    const int64_t q = cq + threadIdx.x + (2 * h + u) * kThreads;
+    v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   x[0] = v[0].x; x[1] = v[0].y; x[2] = v[0].z; x[3] = v[0].w;
   x[4] = v[1].x; x[5] = v[1].y; x[6] = v[1].z; x[7] = v[1].w;
@@ -505,32 +431,11 @@ __device__ __forceinline__ float pick8(const float x[8], int e) {
   return (e & 4) ? hi : lo;
 }
 
-__device__ __forceinline__ float pick16(const float x[16], int e) {
-  const float lo = pick8(x, e & 7), hi = pick8(x + 8, e & 7);
-  return (e & 8) ? hi : lo;
-}
-
 // Window index of element e of 8 consecutive x whose first element has index
 // jb0: elements 0-3 are one quad (index jb0 + e), elements 4-7 the quad
-// kThreads further on (index jb0 + 4 * kThreads + e - 4).  index16 extends
-// this to the thread's four quads.
+// kThreads further on (index jb0 + 4 * kThreads + e - 4).
 __device__ __forceinline__ int32_t index8(int64_t jb0, int e) {
   return (int32_t)(jb0 + (e & 3) + ((e & 4) ? 4 * kThreads : 0));
-}
-
-__device__ __forceinline__ int32_t index16(int64_t jb0, int e) {
-  return (int32_t)(jb0 + (e & 3) + (int64_t)(e >> 2) * 4 * kThreads);
-}
-
-// Gives ring stage g % kStages back to the producer.  The stage's next
-// content is written by a TMA copy (the async proxy) while these reads were
-// plain shared-memory loads (the generic proxy): each thread orders its reads
-// before that write with a proxy fence, after the loaded values have been
-// used, and the warp then arrives on the stage's "empty" barrier.
-__device__ __forceinline__ void release_chunk(Shared& S, uint32_t g) {
-  fence_proxy_async_smem();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&S.empty[g % kStages]);
 }
 
 // Bit e set when element e of 8 consecutive x (laid out as index8) passes
@@ -571,136 +476,22 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
   }
 }
 
-// Fast mode: the row's window through the ring with the fixed rule S.rule
-// (a key prefix: x >= rule.tf decides) and no block-wide synchronisation.
-// Per chunk each thread compares the maximum of each of its 4 quads with the
-// threshold; the warp lists its passing quads (about 1 in 7) in qlist, and
-// then each lane takes one listed quad from the stage and appends its
-// passing elements to the warp's region of the buffer (kRegion entries) at
-// positions from the warp's ballots.  A region that would overflow sets
-// S.overflow (the row is then done again in exact mode).
-__device__ __forceinline__ void stream_row_fast(Shared& S, const Row& r, int64_t nq, uint32_t& g,
-                                                bool& timed_out) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
-  const float tf = S.rule.tf;
-  const uint32_t lt = lanemask_lt();
-  uint32_t* rkey = S.bkey + w * kRegion;
-  int32_t* rj = S.bj + w * kRegion;
-  uint32_t* ql = S.qlist[w];
-  const float qnan = __uint_as_float(0x7FC00000u);  // fails every comparison
-  uint32_t wcnt = 0, kmin = 0xFFFFFFFFu, kmax = 0u;
-  bool full = false;
-  uint32_t s = g % kStages, ph = (g / kStages) & 1u;
-  for (int64_t c = 0; c < nch; ++c) {
-    const int64_t cq = c * kChunkQuads;
-    if (!mbar_try_wait(&S.full[s], ph) && !timed_out && !mbar_wait_bounded(&S.full[s], ph)) timed_out = true;
-    const float4* st = S.ring[s];
-    const bool edge = c == 0 || c == nch - 1;
-    uint32_t B[kQuadsPerThread];
-    bool pass[kQuadsPerThread];
-#pragma unroll
-    for (int u = 0; u < kQuadsPerThread; ++u) {
-      float4 v = st[tid + u * kThreads];
-      if (edge) {
-        const int64_t j = (cq + tid + u * kThreads) * 4 - r.head;
-        if (!(j >= 0 && j < r.L)) v.x = qnan;
-        if (!(j + 1 >= 0 && j + 1 < r.L)) v.y = qnan;
-        if (!(j + 2 >= 0 && j + 2 < r.L)) v.z = qnan;
-        if (!(j + 3 >= 0 && j + 3 < r.L)) v.w = qnan;
-      }
-      pass[u] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) >= tf;  // fmaxf ignores a NaN operand
-      B[u] = __ballot_sync(0xFFFFFFFFu, pass[u]);
-    }
-    const uint32_t P1 = __popc(B[0]), P2 = P1 + __popc(B[1]), P3 = P2 + __popc(B[2]);
-    const uint32_t T = P3 + __popc(B[3]);
-    if (T != 0u && !full) {
-      if (pass[0]) ql[__popc(B[0] & lt)] = (uint32_t)tid;
-      if (pass[1]) ql[P1 + __popc(B[1] & lt)] = (uint32_t)tid + kThreads;
-      if (pass[2]) ql[P2 + __popc(B[2] & lt)] = (uint32_t)tid + 2 * kThreads;
-      if (pass[3]) ql[P3 + __popc(B[3] & lt)] = (uint32_t)tid + 3 * kThreads;
-      __syncwarp();
-      for (uint32_t base = 0; base < T && !full; base += 32) {
-        const uint32_t i = base + lane;
-        uint32_t m4 = 0u, qi = 0u;
-        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < T) {
-          qi = ql[i];
-          q4 = st[qi];
-          const int64_t j = (cq + qi) * 4 - r.head;
-          m4 = (q4.x >= tf ? 1u : 0u) | (q4.y >= tf ? 2u : 0u) | (q4.z >= tf ? 4u : 0u) | (q4.w >= tf ? 8u : 0u);
-          if (edge) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (!(j + e >= 0 && j + e < r.L)) m4 &= ~(1u << e);
-          }
-        }
-        const int32_t jq = (int32_t)((cq + qi) * 4 - r.head);  // used only for in-window elements
-        while (true) {
-          const bool has = m4 != 0u;
-          const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
-          if (b == 0u) break;
-          const uint32_t nb = __popc(b);
-          if (wcnt + nb > (uint32_t)kRegion) {
-            full = true;
-            if (lane == 0) S.overflow = 1u;
-            break;
-          }
-          if (has) {
-            const int e = __ffs(m4) - 1;
-            m4 &= m4 - 1u;
-            const float val = (e & 2) ? ((e & 1) ? q4.w : q4.z) : ((e & 1) ? q4.y : q4.x);
-            const uint32_t key = key_of(val);
-            const uint32_t pos = wcnt + __popc(b & lt);
-            rkey[pos] = key;
-            rj[pos] = jq + e;
-            kmin = min(kmin, key);
-            kmax = max(kmax, key);
-          }
-          wcnt += nb;
-        }
-      }
-    }
-    // every read of the stage is done: give it back
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
-    ++g;
-    if (++s == (uint32_t)kStages) {
-      s = 0u;
-      ph ^= 1u;
-    }
-  }
-  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-  if (lane == 0) {
-    S.rbase[w] = (uint32_t)(w * kRegion);
-    S.rcnt[w] = wcnt;
-    S.wmin[w] = kmin;
-    S.wmax[w] = kmax;
-  }
-}
-
-// Exact mode: the row's window (from the ring, or from global memory) with a
-// rising threshold; the buffer is compacted whenever a half chunk would
-// overflow it.  One block-wide vote per half chunk.
-template <bool kRing>
-__device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, const Row& r, int64_t nq,
-                                                 uint32_t& g, bool& timed_out, Par& par) {
+// Exact mode: the row's window, straight from global memory, with a rising
+// threshold starting at -inf; the buffer (one shared region, kCap entries) is
+// compacted whenever a half chunk would overflow it.  One block-wide vote per
+// half chunk.  For rows whose fast pass failed (rare).
+__device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const Row& r, int64_t nq, Par& par) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t k = (uint32_t)p.k;
   const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
   Rule rule = S.rule;
   for (int64_t c = 0; c < nch; ++c) {
     const int64_t cq = c * kChunkQuads;
-    if constexpr (kRing) {
-      if (!timed_out && !mbar_wait_bounded(&S.full[g % kStages], (g / kStages) & 1u)) timed_out = true;
-    }
     const bool edge = c == 0 || c == nch - 1;
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       float xh[8];
-      take_half<kRing>(S, r, nq, cq, g, h, xh);
+      take_half(r, nq, cq, h, xh);
       const int64_t jb0 = (cq + tid) * 4 - r.head + (int64_t)h * 8 * kThreads;
       uint32_t m = admit_mask(rule, xh, jb0, edge, r.L);
       uint32_t pos;
@@ -731,54 +522,12 @@ __device__ __forceinline__ void stream_row_exact(Shared& S, const Params& p, con
       }
       append(S, xh, m, pos, jb0);
     }
-    if constexpr (kRing) {
-      release_chunk(S, g);
-      ++g;
-    }
   }
 }
 
-// A row without a hint takes its threshold from kSamples of its own elements:
-// kSamples / 4 quads spread evenly over the window, read from global memory
-// (the same bytes stream through the ring right after).  The threshold is the
-// key prefix of the sample's rank-R element, R = 1.4 k * kSamples / L, so
-// that about 1.4 k of the row's elements reach it.  It is only a guess: if it
-// admits fewer than k elements or overflows the buffer, the row is done
-// again in exact mode.  Windows of at least kSampleMinLen elements only (the
-// sampled quads are then distinct).
-constexpr int kSamples = 4096;
-constexpr int kSampleMinLen = 16384;
-static_assert(kSamples <= kCap, "the sample is ranked in the candidate buffer");
-
-__device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const Row& r, int64_t nq, Par& par) {
-  constexpr int kSampleQuads = kSamples / 4;
-#pragma unroll
-  for (int u = 0; u < kSampleQuads / kThreads; ++u) {
-    const int s = threadIdx.x + u * kThreads;
-    const int64_t q = ((2 * (int64_t)s + 1) * nq) / (2 * kSampleQuads);
-    const float4 v = __ldg(r.base4 + q);
-    const float f[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int64_t j = q * 4 - r.head + e;
-      const bool in = j >= 0 && j < r.L;
-      S.bkey[4 * s + e] = in ? key_of(f[e]) : 0u;  // below every real key
-      S.bj[4 * s + e] = in ? (int32_t)j : 0;
-    }
-  }
-  set_regions_contiguous(S, kSamples);
-  cbar();
-  const int64_t want = (7 * (int64_t)p.k * kSamples) / (5 * (int64_t)r.L) + 1;
-  const uint32_t rank = (uint32_t)min(want, (int64_t)kSamples);
-  const Rule sel = select_buffer(S, kSamples, rank, 0u, nullptr, nullptr, par);
-  cbar();
-  for (uint32_t b = threadIdx.x; b < (uint32_t)kBins2; b += kThreads) S.hist2[b] = 0u;
-  if (threadIdx.x == 0) S.rule = rule_prefix(sel.mk, sel.tk);
-  cbar();
-}
-
-// Writes the buffer entries that pass `sel` (exactly k of them) in ascending
-// window index, through the page transform, to out_row[0, k).
+// Exact-mode rows (buffer in no particular order): writes the entries that
+// pass `sel` (exactly k of them) in ascending window index, through the page
+// transform, to out_row[0, k), ordering them with a bitmap of the window.
 // `clean`: the bitmap (hist1) is already all zero for the first segment.
 __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row,
                                               const Rule sel, Par& par, bool clean) {
@@ -856,53 +605,348 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
       if (i < p.k) o[i] = pg[u] * (1 << p.page_bits) + (j[u] & ((1 << p.page_bits) - 1));
     }
   }
+  cbar();  // every thread is done with the staging row (hist2)
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp rings.
+// ---------------------------------------------------------------------------
+
+// Warp w's block of a row's aligned quads [0, nq): chunks [c0, c1) of
+// kWChunkQuads quads, contiguous, in warp order, sizes differing by at most 1.
+__device__ __forceinline__ void warp_block(int64_t nq, int w, int64_t& q0, int64_t& q1) {
+  const int64_t nch = (nq + kWChunkQuads - 1) / kWChunkQuads;
+  const int64_t c0 = nch * w / kWarps, c1 = nch * (w + 1) / kWarps;
+  q0 = min(c0 * kWChunkQuads, nq);
+  q1 = min(c1 * kWChunkQuads, nq);
+}
+
+// Lane 0's cursor over its warp's chunk sequence: the warp's block of each of
+// the CTA's rows (blockIdx.x, blockIdx.x + gridDim.x, ... with seq_len > k).
+struct WCursor {
+  const float4* src;
+  int64_t left;  // quads of the current block not yet issued
+  int64_t row;
+  uint32_t issued;
+};
+
+// Lane 0: issues the warp's next chunk into stage issued % kWStages (whose
+// previous chunk the warp has taken and fenced).  False past the last row.
+__device__ __forceinline__ bool warp_issue(Shared& S, WCursor& cur, const Params& p, int w, uint64_t policy) {
+  while (cur.left == 0) {
+    if (cur.row >= p.num_rows) return false;
+    cur.row += gridDim.x;
+    if (cur.row >= p.num_rows) return false;
+    const Row r = load_row(p, (int32_t)cur.row);
+    if (r.L <= p.k) continue;
+    int64_t q0, q1;
+    warp_block(((int64_t)r.L + r.head + 3) >> 2, w, q0, q1);
+    cur.src = r.base4 + q0;
+    cur.left = q1 - q0;
+  }
+  const uint32_t s = cur.issued % kWStages;
+  const uint32_t nquads = (uint32_t)min((int64_t)kWChunkQuads, cur.left);
+  mbar_arrive_expect_tx(&S.wfull[w][s], nquads * 16u);
+  bulk_copy_g2s(&S.wring[w][s][0], cur.src, nquads * 16u, &S.wfull[w][s], policy);
+  cur.src += nquads;
+  cur.left -= nquads;
+  ++cur.issued;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Fast pass: the warp's block of the row through its ring, fixed threshold.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const Row& r, int64_t nq, uint32_t& g,
+                                              WCursor& cur, uint64_t policy, bool& timed_out) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t q0, q1;
+  warp_block(nq, w, q0, q1);
+  const float tf = S.rule.tf;
+  const uint32_t tk = S.fh_tk, sh = S.fh_sh;
+  const uint32_t lt = lanemask_lt();
+  const int rot = (lane >> 1) & 3;  // rotated quad order keeps a warp's loads on distinct banks
+  uint32_t* rkey = S.bkey + w * kRegion;
+  int32_t* rj = S.bj + w * kRegion;
+  uint32_t* ql = S.qlist[w];
+  const float qnan = __uint_as_float(0x7FC00000u);  // fails every comparison
+  uint32_t wcnt = 0, top = 0u;
+  bool full = false;
+  for (int64_t cq = q0; cq < q1; cq += kWChunkQuads, ++g) {
+    const uint32_t s = g % kWStages;
+    if (!mbar_try_wait(&S.wfull[w][s], (g / kWStages) & 1u) && !timed_out &&
+        !mbar_wait_bounded(&S.wfull[w][s], (g / kWStages) & 1u))
+      timed_out = true;
+    const float4* st = S.wring[w][s];
+    const bool edge = cq == 0 || cq + kWChunkQuads >= nq;  // the row's first or last chunk
+    uint32_t pm = 0u;  // bit pq: quad 4 * lane + pq may hold a candidate
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int pq = (u + rot) & 3;
+      float4 v = st[4 * lane + pq];
+      if (edge) {
+        const int64_t j = (cq + 4 * lane + pq) * 4 - r.head;
+        if (!(j >= 0 && j < r.L)) v.x = qnan;
+        if (!(j + 1 >= 0 && j + 1 < r.L)) v.y = qnan;
+        if (!(j + 2 >= 0 && j + 2 < r.L)) v.z = qnan;
+        if (!(j + 3 >= 0 && j + 3 < r.L)) v.w = qnan;
+      }
+      pm |= (fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) >= tf ? 1u : 0u) << pq;  // fmaxf ignores a NaN
+    }
+    const uint32_t np = __popc(pm);
+    const uint32_t incl = warp_incl_scan(np);
+    const uint32_t T = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (T != 0u && !full) {
+      uint32_t at = incl - np;
+      for (uint32_t b = pm; b; b &= b - 1u) ql[at++] = 4u * lane + (__ffs(b) - 1);  // window order
+      __syncwarp();
+      for (uint32_t base = 0; base < T; base += 32) {
+        const uint32_t i = base + lane;
+        uint32_t m4 = 0u, q = 0u;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < T) {
+          q = ql[i];
+          v = st[q];
+          m4 = (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
+          if (edge) {
+            const int64_t j = (cq + q) * 4 - r.head;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (!(j + e >= 0 && j + e < r.L)) m4 &= ~(1u << e);
+          }
+        }
+        const uint32_t c4 = __popc(m4);
+        const uint32_t inc4 = warp_incl_scan(c4);
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, inc4, 31);
+        if (wcnt + tot > (uint32_t)kRegion) {
+          full = true;
+          if (lane == 0) S.overflow = 1u;
+          break;
+        }
+        uint32_t pos = wcnt + inc4 - c4;
+        const int32_t jq = (int32_t)((cq + q) * 4 - r.head);  // used for in-window elements only
+        for (uint32_t mm = m4; mm; mm &= mm - 1u) {
+          const int e = __ffs(mm) - 1;
+          const float x = (e & 2) ? ((e & 1) ? v.w : v.z) : ((e & 1) ? v.y : v.x);
+          const uint32_t key = key_of(x);
+          rkey[pos] = key;
+          rj[pos] = jq + e;
+          ++pos;
+          const uint32_t fb = (key - tk) >> sh;
+          if (fb < (uint32_t)kFineTop)
+            atomicAdd(&S.hist2[fb], 1u);
+          else
+            ++top;
+        }
+        wcnt += tot;
+      }
+    }
+    // the warp is done with the stage: order its reads before the next copy, refill
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) warp_issue(S, cur, p, w, policy);
+  }
+  top = __reduce_add_sync(0xFFFFFFFFu, top);
+  if (lane == 0) {
+    S.rbase[w] = (uint32_t)(w * kRegion);
+    S.rcnt[w] = wcnt;
+    S.wtop[w] = top;
+  }
+}
+
+// Fine shift for a row whose threshold key sits about `d` keys below its k-th
+// largest: bins of 2^shift keys put the k-th largest near bin 384.
+__device__ __forceinline__ uint32_t fine_shift(uint32_t d) {
+  const uint32_t x = max(d / 384u, 1u);
+  return (uint32_t)(31 - __clz(x));
+}
+
+// Fast rows: the k-th largest pair from the fine histogram.  Returns false
+// (uniformly) when it cannot be settled there -- rank above the histogram's
+// range, or more than 32 candidates in its bin -- and the generic selection
+// must run.  Also proposes the next row's hint (rank hr) and fine shift.
+__device__ __noinline__ bool resolve_fine(Shared& S, uint32_t n, uint32_t k, uint32_t hr, Rule& sel, Rule& hint,
+                                          uint32_t& hint_ok, uint32_t& hint_sh, Par& par) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t top = 0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) top += S.wtop[i];
+  if (top >= k) return false;
+  const uint32_t tk = S.fh_tk, sh = S.fh_sh;
+  const uint32_t r = k - top;
+  const uint32_t r2 = (hr > top && hr <= n) ? hr - top : 0u;
+  const PickOut pk = pick_bins<kBins2>(S.hist2, 0u, r, r2, S, par);
+  const uint32_t rem = r - pk.above;
+  const uint32_t lo_key = tk + (pk.bin << sh);
+  hint_ok = 0u;
+  hint_sh = sh;
+  if (hr != 0u && hr <= top) {
+    hint = rule_prefix(0xFFFFFFFFu, tk + ((uint32_t)kFineTop << sh));
+    hint_ok = 1u;
+  } else if (r2 != 0u && pk.has2) {
+    const uint32_t hk = tk + (pk.bin2 << sh);
+    hint = rule_prefix(0xFFFFFFFFu, hk);
+    hint_ok = 1u;
+    // ranks k and hr a few bins apart: size the next row's bins from their
+    // distance; in the same bin the bins were too wide: halve them
+    hint_sh = lo_key > hk ? fine_shift(lo_key - hk) : (sh > 0u ? sh - 1u : 0u);
+  }
+  if (pk.count == rem) {
+    sel = rule_prefix(0xFFFFFFFFu, lo_key);  // all of the bin and everything above
+    return true;
+  }
+  if (pk.count > 32u) return false;
+  // gather the bin's candidates and rank them by pair in one warp
+  const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
+  for (uint32_t i = lane; i < cnt; i += 32) {
+    const uint32_t key = S.bkey[base + i];
+    if (((key - tk) >> sh) == pk.bin) {
+      const uint32_t at = atomicAdd(&S.res_n, 1u);
+      if (at < 32u) {
+        S.res_key[at] = key;
+        S.res_j[at] = S.bj[base + i];
+      }
+    }
+  }
+  cbar();
+  if (w == 0) {
+    const uint32_t m = S.res_n;  // == pk.count
+    const uint64_t mine = lane < (int)m ? pair_of(S.res_key[lane], S.res_j[lane]) : 0ull;
+    uint32_t above = 0;
+    for (uint32_t o = 0; o < m; ++o) {
+      const uint64_t other = pair_of(S.res_key[o], S.res_j[o]);
+      above += other > mine ? 1u : 0u;
+    }
+    if (lane < (int)m && above == rem - 1u) S.sel_T = mine;
+  }
+  cbar();
+  sel = rule_of_pair_prefix(~0ull, S.sel_T);
+  return true;
+}
+
+// Fast rows: every warp's region is in ascending window index and the regions
+// follow each other in warp order, so the selected entries' output positions
+// are prefix counts -- one pass to count, one to write, no sorting.
+__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, const Row& r, int64_t row,
+                                             const Rule sel) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
+  const uint32_t lt = lanemask_lt(), k = (uint32_t)p.k;
+  uint32_t c = 0;
+  for (uint32_t i = lane; i < cnt; i += 32) c += rule_pass(sel, S.bkey[base + i], S.bj[base + i]) ? 1u : 0u;
+  c = __reduce_add_sync(0xFFFFFFFFu, c);
+  if (lane == 0) S.wtot[w] = c;
+  cbar();
+  uint32_t pos = 0;
+  for (int i = 0; i < w; ++i) pos += S.wtot[i];
+  int32_t* o = p.out + row * p.k;
+  // batches of kB groups of 32 entries: all page-table loads of a batch are
+  // in flight together (they come from L2: shared memory leaves little L1)
+  constexpr int kB = 8;
+  const int32_t pmask = (1 << p.page_bits) - 1;
+  for (uint32_t g0 = 0; g0 < cnt; g0 += 32 * kB) {
+    int32_t j[kB], pg[kB];
+    uint32_t q[kB];
+    bool take[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const uint32_t i = g0 + u * 32 + lane;
+      j[u] = 0;
+      take[u] = false;
+      if (i < cnt) {
+        j[u] = S.bj[base + i];
+        take[u] = rule_pass(sel, S.bkey[base + i], j[u]);
+      }
+      const uint32_t b = __ballot_sync(0xFFFFFFFFu, take[u]);
+      q[u] = pos + __popc(b & lt);
+      pos += __popc(b);
+    }
+#pragma unroll
+    for (int u = 0; u < kB; ++u) pg[u] = take[u] ? __ldg(r.page_row + (j[u] >> p.page_bits)) : 0;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      if (take[u]) {
+        if (q[u] < k)
+          o[q[u]] = pg[u] * (1 << p.page_bits) + (j[u] & pmask);
+        else
+          atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
+      }
+    }
+  }
+}
+
+// A row without a hint takes its threshold from kSamples of its own elements:
+// kSamples / 4 quads spread evenly over the window, read from global memory
+// (the same bytes stream through the rings right after).  The threshold is
+// the key prefix of the sample's rank-R element, R = 1.4 k * kSamples / L, so
+// that about 1.4 k of the row's elements reach it; the sample's rank-k element
+// sizes the fine histogram.  It is only a guess: if it admits fewer than k
+// elements or overflows a region, the row is done again in exact mode.
+constexpr int kSamples = 4096;
+static_assert(kSamples <= kCap, "the sample is ranked in the candidate buffer");
+
+__device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const Row& r, int64_t nq, Par& par) {
+  constexpr int kSampleQuads = kSamples / 4;
+#pragma unroll
+  for (int u = 0; u < kSampleQuads / kThreads; ++u) {
+    const int s = threadIdx.x + u * kThreads;
+    const int64_t q = ((2 * (int64_t)s + 1) * nq) / (2 * kSampleQuads);
+    const float4 v = __ldg(r.base4 + q);
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t j = q * 4 - r.head + e;
+      const bool in = j >= 0 && j < r.L;
+      S.bkey[4 * s + e] = in ? key_of(f[e]) : 0u;  // below every real key
+      S.bj[4 * s + e] = in ? (int32_t)j : 0;
+    }
+  }
+  set_regions_contiguous(S, kSamples);
+  cbar();
+  const int64_t want = (7 * (int64_t)p.k * kSamples) / (5 * (int64_t)r.L) + 1;
+  const uint32_t rank = (uint32_t)min(want, (int64_t)kSamples);
+  const uint32_t rank_k = (uint32_t)min((int64_t)p.k * kSamples / r.L + 1, (int64_t)rank);
+  const Rule sel = select_buffer(S, kSamples, rank, 0u, nullptr, nullptr, par);
+  cbar();
+  const Rule tau = select_buffer(S, kSamples, rank_k, 0u, nullptr, nullptr, par);  // sizes the bins
+  cbar();
+  for (uint32_t b = threadIdx.x; b < (uint32_t)kBins2; b += kThreads) S.hist2[b] = 0u;
+  if (threadIdx.x == 0) {
+    S.rule = rule_prefix(sel.mk, sel.tk);
+    S.fh_tk = S.rule.tk;
+    S.fh_sh = fine_shift(tau.tk > S.rule.tk ? tau.tk - S.rule.tk : 0u);
+  }
+  cbar();
 }
 
 __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Shared& S = *reinterpret_cast<Shared*>(smem_raw);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t k = (uint32_t)p.k;
   const uint64_t policy = l2_evict_first_policy();
   bool timed_out = false;
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kWarps);
-    }
+  if (lane == 0) {
+    for (int s = 0; s < kWStages; ++s) mbar_init(&S.wfull[w][s], 1);
     fence_barrier_init();
+  }
+  for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
+  if (tid == 0) {
     S.hint_valid = 0u;
+    S.hint_sh = 0u;
   }
   __syncthreads();
-
-  if (tid >= kThreads) {
-    // ---- producer warp: one lane streams every chunk of the CTA's rows
-    Cursor cur;
-    cur.src = nullptr;
-    cur.left = 0;
-    cur.row = (int64_t)blockIdx.x - gridDim.x;
-    cur.issued = 0;
-    if (tid == kThreads) {
-      while (issue_next(S, cur, p, policy, timed_out)) {
-      }
-    }
-    // Every issued chunk is taken by the consumers before they finish, so no
-    // copy is in flight at exit -- unless a wait gave up; then wait (bounded)
-    // for the last chunks issued.
-    if (__syncthreads_or(timed_out ? 1 : 0) && tid == kThreads) {
-      atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
-      const uint32_t first = cur.issued > (uint32_t)kStages ? cur.issued - kStages : 0u;
-      for (uint32_t c = first; c < cur.issued; ++c) mbar_wait_bounded(&S.full[c % kStages], (c / kStages) & 1u);
-    }
-    return;
-  }
+  // each warp starts its ring
+  WCursor cur;
+  cur.src = nullptr;
+  cur.left = 0;
+  cur.row = (int64_t)blockIdx.x - gridDim.x;
+  cur.issued = 0;
+  if (lane == 0)
+    for (int s = 0; s < kWStages; ++s) warp_issue(S, cur, p, w, policy);
 
   Par par;
-  uint32_t g = 0;  // chunks taken from the ring
-  // Between rows hist1 (histogram / bitmap) and hist2 (histogram / staging
-  // row) are cleared while the next row streams; they start clean.
-  for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
-  for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
+  uint32_t g = 0;  // chunks this warp took from its ring
 
   for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
     const Row r = load_row(p, (int32_t)row);
@@ -911,12 +955,21 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       continue;
     }
     const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
-    // ---- row set-up: threshold from the hint (written at the previous row's end)
-    bool fast = S.hint_valid != 0u;
+    // ---- row set-up: the threshold (hint, whole row, or sample)
+    const bool small = (nq + kWChunkQuads - 1) / kWChunkQuads <= kWarps;  // each warp one chunk at most
+    const bool hinted = !small && S.hint_valid != 0u;
     if (tid == 0) {
-      S.count = 0u;
       S.overflow = 0u;
-      S.rule = fast ? S.hint : rule_all();
+      S.res_n = 0u;
+      if (small) {
+        S.rule = rule_all();  // every element fits its warp's region
+        S.fh_tk = 0u;
+        S.fh_sh = 21u;
+      } else if (hinted) {
+        S.rule = S.hint;
+        S.fh_tk = S.hint.tk;
+        S.fh_sh = S.hint_sh;
+      }
       // the CTA's next row that needs a selection, for the hint
       int32_t nl = 0;
       for (int64_t rr = row + gridDim.x; rr < p.num_rows; rr += gridDim.x) {
@@ -930,67 +983,74 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       // rank of about 1.25 k in a row of the next row's length
       S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
     }
-    cbar();  // also: every thread is done with the previous row's hist1 / hist2
-    for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
     for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
-    if (!fast && r.L < kSampleMinLen) cbar();  // exact mode counts into hist1 at once
-    if (!fast && r.L >= kSampleMinLen) {
-      // no hint: estimate a threshold from a sample of the row itself
-      sample_threshold(S, p, r, nq, par);
-      fast = true;
-    }
-    if (fast) {
-      stream_row_fast(S, r, nq, g, timed_out);
-    } else {
-      stream_row_exact<true>(S, p, r, nq, g, timed_out, par);
-      cbar();
-      set_regions_contiguous(S, S.count);
-    }
+    cbar();  // also: every thread is done with the previous row's shared state
+    if (!small && !hinted) sample_threshold(S, p, r, nq, par);
+    stream_row_wb(S, p, r, nq, g, cur, policy, timed_out);
     cbar();
     uint32_t n = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) n += S.rcnt[i];
-    const bool redo = n < k || S.overflow;
-    // a fast row that stands: hist1 / hist2 untouched since the set-up, key ranges known
-    const bool ready = fast && !redo;
-    if (redo) {
-      // the hint was off: stream the row again, from global memory, exactly
-      for (int b = tid; b < kBins1; b += kThreads) S.hist1[b] = 0u;
+    const bool redo = n < k || S.overflow != 0u;
+    const uint32_t hr = S.hint_rank;
+    Rule sel, hint;
+    uint32_t hint_ok = 0u, hint_sh = S.fh_sh;
+    if (!redo) {
+      if (!resolve_fine(S, n, k, hr, sel, hint, hint_ok, hint_sh, par)) {
+        sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par, false);
+        hint_sh = (hint_ok && sel.tk > hint.tk) ? fine_shift(sel.tk - hint.tk) : S.fh_sh;
+      }
+    } else {
+      // the threshold was off: stream the row again, from global memory, exactly
+      for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
       cbar();
       if (tid == 0) {
         S.count = 0u;
-        S.overflow = 0u;
         S.rule = rule_all();
       }
       cbar();
-      stream_row_exact<false>(S, p, r, nq, g, timed_out, par);
+      stream_row_exact(S, p, r, nq, par);
       cbar();
       n = S.count;
       set_regions_contiguous(S, n);
       cbar();
+      sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par, false);
+      hint_sh = (hint_ok && sel.tk > hint.tk) ? fine_shift(sel.tk - hint.tk) : S.fh_sh;
     }
-    // ---- selection, next row's hint, emission
-    Rule hint;
-    uint32_t hint_ok = 0u;
-    const uint32_t hr = S.hint_rank;
-    const Rule sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par, ready);
-    if (tid == 0) S.hint_valid = 0u;
-    if (tid == 0 && hr != 0u) {
-      if (hint_ok) {
-        S.hint = hint;
-        S.hint_valid = 1u;
-      } else if ((uint64_t)n * (uint64_t)S.next_len * 5u >= (uint64_t)6u * k * (uint64_t)r.L) {
-        // too few candidates for the rank, but the admitted ones scale to
-        // at least 1.2 k in the next row: keep this row's threshold
-        S.hint = rule_prefix(S.rule.mk, S.rule.tk);
-        S.hint_valid = 1u;
+    if (tid == 0) {
+      S.hint_valid = 0u;
+      if (hr != 0u) {
+        if (hint_ok) {
+          S.hint = hint;
+          S.hint_sh = hint_sh;
+          S.hint_valid = 1u;
+        } else if (!redo && (uint64_t)n * (uint64_t)S.next_len * 5u >= (uint64_t)6u * k * (uint64_t)r.L) {
+          // too few candidates for the rank, but the admitted ones scale to
+          // at least 1.2 k in the next row: keep this row's threshold
+          S.hint = rule_prefix(S.rule.mk, S.rule.tk);
+          S.hint_sh = S.fh_sh;
+          S.hint_valid = 1u;
+        }
       }
     }
-    emit_selected(S, p, r, row, sel, par, ready);
+    if (!redo) {
+      emit_ordered(S, p, r, row, sel);
+    } else {
+      emit_selected(S, p, r, row, sel, par, false);
+      // hist1 is the bitmap now: clear it for the next exact row
+      for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 
-  // (the producer warp joins this last block-wide vote)
-  if (__syncthreads_or(timed_out ? 1 : 0) && tid == 0) atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
+  // Every issued chunk was taken by its warp, so no copy is in flight -- unless
+  // a wait gave up; then each warp waits (bounded) for its outstanding copies.
+  if (__syncthreads_or(timed_out ? 1 : 0)) {
+    if (lane == 0) {
+      if (tid == 0) atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
+      for (uint32_t c = g; c < cur.issued; ++c) mbar_wait_bounded(&S.wfull[w][c % kWStages], (c / kWStages) & 1u);
+    }
+    __syncthreads();
+  }
 }
 
 }  // namespace pipe

@@ -167,7 +167,7 @@ def test_zero_rows_launches_nothing(cuda_device):
 def test_plan_reports_the_launch(cuda_device):
     plan = binding.topk_packed_plan(140000, 2048, 4096)
     assert plan["path"] == binding.PATHS["pipe"]
-    assert plan["threads_per_cta"] == 288, "8 consumer warps + 1 producer warp"
+    assert plan["threads_per_cta"] == 256, "8 warps, each streaming its own block"
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert plan["grid_ctas"] == 2 * sms, "two pipelined CTAs per SM"
     assert binding.topk_packed_plan(140000, 2048, 7)["grid_ctas"] == 7
