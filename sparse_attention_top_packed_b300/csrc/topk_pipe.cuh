@@ -22,13 +22,13 @@
 //  * Admission.  Every row streams with a fixed threshold, a guess at a lower
 //    bound of its k-th largest key: from the CTA's previous row (the key that
 //    about 1.25 k of its candidates reach, scaled to the new length), or from
-//    a strided sample of the row itself.  Each lane takes 4 consecutive quads
-//    of a chunk and compares each quad's maximum with the threshold; the warp
-//    lists its passing quads (about 1 in 7) in window order, each lane takes
-//    one listed quad and appends its passing elements (order-preserving key,
-//    window index) to the warp's region of the candidate buffer at positions
-//    from a warp scan.  A region therefore holds its candidates in ascending
-//    window index, and the regions follow each other in warp order.  Each
+//    a strided sample of the row itself.  Each lane takes 16 consecutive floats
+//    of a chunk, compares them with the threshold, gives the stage back, and
+//    appends its passing elements (order-preserving key, window index) to the
+//    warp's region of the candidate buffer, at positions from an exclusive
+//    prefix of the lanes' counts (five ballots).  A region therefore holds its
+//    candidates in ascending window index, and the regions follow each other
+//    in warp order.  Each
 //    candidate is also counted in a fine histogram: 2047 equal key bins above
 //    the threshold, sized so that the k-th largest key lands in about bin 384.
 //
@@ -121,7 +121,6 @@ struct Shared {
   uint32_t hist1[kBins1];  // exact mode: histogram; then the emission bitmap
   uint32_t hist2[kBins2];  // fine histogram / refinement levels / staging row
   uint64_t wfull[kWarps][kWStages];
-  uint32_t qlist[kWarps][4 * 32];  // a warp's quads that may hold candidates
   uint32_t scratch[2][kWarps];
   PickOut pick[2];
   uint32_t wtot[kWarps];
@@ -657,6 +656,21 @@ __device__ __forceinline__ bool warp_issue(Shared& S, WCursor& cur, const Params
 // ---------------------------------------------------------------------------
 // Fast pass: the warp's block of the row through its ring, fixed threshold.
 // ---------------------------------------------------------------------------
+
+// Exclusive prefix over the warp's lanes of v (0 <= v < 32), from the
+// ballots of its five bits: independent votes, no shuffle chain.
+__device__ __forceinline__ uint32_t warp_excl_prefix5(uint32_t v, uint32_t lt, uint32_t& total) {
+  uint32_t pre = 0, tot = 0;
+#pragma unroll
+  for (int b = 0; b < 5; ++b) {
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, (v >> b) & 1u);
+    pre += (uint32_t)__popc(m & lt) << b;
+    tot += (uint32_t)__popc(m) << b;
+  }
+  total = tot;
+  return pre;
+}
+
 __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const Row& r, int64_t nq, uint32_t& g,
                                               WCursor& cur, uint64_t policy, bool& timed_out) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -665,10 +679,8 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
   const float tf = S.rule.tf;
   const uint32_t tk = S.fh_tk, sh = S.fh_sh;
   const uint32_t lt = lanemask_lt();
-  const int rot = (lane >> 1) & 3;  // rotated quad order keeps a warp's loads on distinct banks
   uint32_t* rkey = S.bkey + w * kRegion;
   int32_t* rj = S.bj + w * kRegion;
-  uint32_t* ql = S.qlist[w];
   const float qnan = __uint_as_float(0x7FC00000u);  // fails every comparison
   uint32_t wcnt = 0, top = 0u;
   bool full = false;
@@ -678,73 +690,51 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
         !mbar_wait_bounded(&S.wfull[w][s], (g / kWStages) & 1u))
       timed_out = true;
     const float4* st = S.wring[w][s];
-    const bool edge = cq == 0 || cq + kWChunkQuads >= nq;  // the row's first or last chunk
-    uint32_t pm = 0u;  // bit pq: quad 4 * lane + pq may hold a candidate
+    float x[16];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int pq = (u + rot) & 3;
-      float4 v = st[4 * lane + pq];
-      if (edge) {
-        const int64_t j = (cq + 4 * lane + pq) * 4 - r.head;
-        if (!(j >= 0 && j < r.L)) v.x = qnan;
-        if (!(j + 1 >= 0 && j + 1 < r.L)) v.y = qnan;
-        if (!(j + 2 >= 0 && j + 2 < r.L)) v.z = qnan;
-        if (!(j + 3 >= 0 && j + 3 < r.L)) v.w = qnan;
-      }
-      pm |= (fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) >= tf ? 1u : 0u) << pq;  // fmaxf ignores a NaN
+    for (int u = 0; u < 4; ++u) {  // lane's 4 consecutive quads, 16 consecutive elements
+      const float4 v = st[4 * lane + u];
+      x[4 * u] = v.x;
+      x[4 * u + 1] = v.y;
+      x[4 * u + 2] = v.z;
+      x[4 * u + 3] = v.w;
     }
-    const uint32_t np = __popc(pm);
-    const uint32_t incl = warp_incl_scan(np);
-    const uint32_t T = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    if (T != 0u && !full) {
-      uint32_t at = incl - np;
-      for (uint32_t b = pm; b; b &= b - 1u) ql[at++] = 4u * lane + (__ffs(b) - 1);  // window order
-      __syncwarp();
-      for (uint32_t base = 0; base < T; base += 32) {
-        const uint32_t i = base + lane;
-        uint32_t m4 = 0u, q = 0u;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < T) {
-          q = ql[i];
-          v = st[q];
-          m4 = (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
-          if (edge) {
-            const int64_t j = (cq + q) * 4 - r.head;
+    const int64_t jb = (cq + 4 * lane) * 4 - r.head;  // window index of x[0]
+    if (cq == 0 || cq + kWChunkQuads >= nq) {  // the row's first or last chunk
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (!(j + e >= 0 && j + e < r.L)) m4 &= ~(1u << e);
-          }
-        }
-        const uint32_t c4 = __popc(m4);
-        const uint32_t inc4 = warp_incl_scan(c4);
-        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, inc4, 31);
-        if (wcnt + tot > (uint32_t)kRegion) {
-          full = true;
-          if (lane == 0) S.overflow = 1u;
-          break;
-        }
-        uint32_t pos = wcnt + inc4 - c4;
-        const int32_t jq = (int32_t)((cq + q) * 4 - r.head);  // used for in-window elements only
-        for (uint32_t mm = m4; mm; mm &= mm - 1u) {
-          const int e = __ffs(mm) - 1;
-          const float x = (e & 2) ? ((e & 1) ? v.w : v.z) : ((e & 1) ? v.y : v.x);
-          const uint32_t key = key_of(x);
-          rkey[pos] = key;
-          rj[pos] = jq + e;
-          ++pos;
-          const uint32_t fb = (key - tk) >> sh;
-          if (fb < (uint32_t)kFineTop)
-            atomicAdd(&S.hist2[fb], 1u);
-          else
-            ++top;
-        }
-        wcnt += tot;
-      }
+      for (int e = 0; e < 16; ++e)
+        if (!(jb + e >= 0 && jb + e < r.L)) x[e] = qnan;
     }
-    // the warp is done with the stage: order its reads before the next copy, refill
+    uint32_t m = 0u;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) m |= (x[e] >= tf ? 1u : 0u) << e;
+    // the values are used: order the warp's reads before the next copy into the stage, refill it
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) warp_issue(S, cur, p, w, policy);
+    if (full) continue;
+    uint32_t tot;
+    uint32_t pos = wcnt + warp_excl_prefix5(__popc(m), lt, tot);
+    if (tot == 0u) continue;
+    if (wcnt + tot > (uint32_t)kRegion) {
+      full = true;
+      if (lane == 0) S.overflow = 1u;
+      continue;
+    }
+    for (uint32_t mm = m; mm; mm &= mm - 1u) {  // ascending e: window order within the lane
+      const int e = __ffs(mm) - 1;
+      const float xe = (e & 8) ? pick8(x + 8, e & 7) : pick8(x, e & 7);
+      const uint32_t key = key_of(xe);
+      rkey[pos] = key;
+      rj[pos] = (int32_t)(jb + e);
+      ++pos;
+      const uint32_t fb = (key - tk) >> sh;
+      if (fb < (uint32_t)kFineTop)
+        atomicAdd(&S.hist2[fb], 1u);
+      else
+        ++top;
+    }
+    wcnt += tot;
   }
   top = __reduce_add_sync(0xFFFFFFFFu, top);
   if (lane == 0) {
