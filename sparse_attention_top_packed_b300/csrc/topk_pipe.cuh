@@ -654,6 +654,60 @@ __device__ __forceinline__ bool warp_issue(Shared& S, WCursor& cur, const Params
 }
 
 // ---------------------------------------------------------------------------
+// Deferred page transform.  A fast row's emission writes the selected window
+// indices j in order; the page transform of section 1 (a load from the page
+// table, which comes from L2 -- shared memory leaves little L1) is then done in
+// place by each warp for its eighth of the row while the next row streams,
+// one position per lane per chunk, its loads issued one chunk ahead, so their
+// latency hides behind the stream.  What is left is finished before the next
+// fast row's emission and at the end of the kernel.
+// ---------------------------------------------------------------------------
+struct Deferred {
+  int32_t* o;               // output row being transformed (null: none)
+  const int32_t* page_row;
+  uint32_t next, end;       // this lane's next position to load, the warp's end
+  uint32_t ta, tb;          // positions in the pipeline
+  int32_t ja, jb, pgb;
+  bool va, vb;
+};
+
+// The indices of the row were written by every warp: a consumer barrier must
+// separate that emission from the first deferred_step / deferred_flush.
+__device__ __forceinline__ void deferred_start(Deferred& d, int32_t* o, const int32_t* page_row, uint32_t k) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  d.o = o;
+  d.page_row = page_row;
+  d.next = (uint32_t)((uint64_t)k * w / kWarps) + lane;
+  d.end = (uint32_t)((uint64_t)k * (w + 1) / kWarps);
+  d.va = d.vb = false;
+}
+
+// One step of the pipeline: store the oldest, load the page of the middle,
+// load the index of the newest.
+__device__ __forceinline__ void deferred_step(Deferred& d, int32_t page_bits) {
+  if (d.o == nullptr) return;
+  if (d.vb) d.o[d.tb] = d.pgb * (1 << page_bits) + (d.jb & ((1 << page_bits) - 1));
+  d.vb = d.va;
+  if (d.va) {
+    d.tb = d.ta;
+    d.jb = d.ja;
+    d.pgb = __ldg(d.page_row + (d.ja >> page_bits));
+  }
+  d.va = d.next < d.end;
+  if (d.va) {
+    d.ta = d.next;
+    d.ja = d.o[d.next];  // written by other warps of the block before a barrier
+    d.next += 32;
+  }
+}
+
+__device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
+  if (d.o == nullptr) return;
+  while (d.va || d.vb || d.next < d.end) deferred_step(d, page_bits);
+  d.o = nullptr;
+}
+
+// ---------------------------------------------------------------------------
 // Fast pass: the warp's block of the row through its ring, fixed threshold.
 // ---------------------------------------------------------------------------
 
@@ -672,7 +726,7 @@ __device__ __forceinline__ uint32_t warp_excl_prefix5(uint32_t v, uint32_t lt, u
 }
 
 __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const Row& r, int64_t nq, uint32_t& g,
-                                              WCursor& cur, uint64_t policy, bool& timed_out) {
+                                              WCursor& cur, uint64_t policy, bool& timed_out, Deferred& dfr) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int64_t q0, q1;
   warp_block(nq, w, q0, q1);
@@ -712,6 +766,7 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) warp_issue(S, cur, p, w, policy);
+    deferred_step(dfr, p.page_bits);
     if (full) continue;
     uint32_t tot;
     uint32_t pos = wcnt + warp_excl_prefix5(__popc(m), lt, tot);
@@ -816,9 +871,9 @@ __device__ __noinline__ bool resolve_fine(Shared& S, uint32_t n, uint32_t k, uin
 
 // Fast rows: every warp's region is in ascending window index and the regions
 // follow each other in warp order, so the selected entries' output positions
-// are prefix counts -- one pass to count, one to write, no sorting.
-__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, const Row& r, int64_t row,
-                                             const Rule sel) {
+// are prefix counts -- one pass to count, one to write, no sorting.  Writes
+// the window indices; the page transform follows (Deferred).
+__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t row, const Rule sel) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
   const uint32_t lt = lanemask_lt(), k = (uint32_t)p.k;
@@ -830,38 +885,23 @@ __device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, const R
   uint32_t pos = 0;
   for (int i = 0; i < w; ++i) pos += S.wtot[i];
   int32_t* o = p.out + row * p.k;
-  // batches of kB groups of 32 entries: all page-table loads of a batch are
-  // in flight together (they come from L2: shared memory leaves little L1)
-  constexpr int kB = 8;
-  const int32_t pmask = (1 << p.page_bits) - 1;
-  for (uint32_t g0 = 0; g0 < cnt; g0 += 32 * kB) {
-    int32_t j[kB], pg[kB];
-    uint32_t q[kB];
-    bool take[kB];
-#pragma unroll
-    for (int u = 0; u < kB; ++u) {
-      const uint32_t i = g0 + u * 32 + lane;
-      j[u] = 0;
-      take[u] = false;
-      if (i < cnt) {
-        j[u] = S.bj[base + i];
-        take[u] = rule_pass(sel, S.bkey[base + i], j[u]);
-      }
-      const uint32_t b = __ballot_sync(0xFFFFFFFFu, take[u]);
-      q[u] = pos + __popc(b & lt);
-      pos += __popc(b);
+  for (uint32_t i0 = 0; i0 < cnt; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    bool take = false;
+    int32_t j = 0;
+    if (i < cnt) {
+      j = S.bj[base + i];
+      take = rule_pass(sel, S.bkey[base + i], j);
     }
-#pragma unroll
-    for (int u = 0; u < kB; ++u) pg[u] = take[u] ? __ldg(r.page_row + (j[u] >> p.page_bits)) : 0;
-#pragma unroll
-    for (int u = 0; u < kB; ++u) {
-      if (take[u]) {
-        if (q[u] < k)
-          o[q[u]] = pg[u] * (1 << p.page_bits) + (j[u] & pmask);
-        else
-          atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
-      }
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, take);
+    if (take) {
+      const uint32_t q = pos + __popc(b & lt);
+      if (q < k)
+        o[q] = j;
+      else
+        atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
     }
+    pos += __popc(b);
   }
 }
 
@@ -937,6 +977,8 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
 
   Par par;
   uint32_t g = 0;  // chunks this warp took from its ring
+  Deferred dfr;
+  dfr.o = nullptr;
 
   for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
     const Row r = load_row(p, (int32_t)row);
@@ -960,23 +1002,29 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
         S.fh_tk = S.hint.tk;
         S.fh_sh = S.hint_sh;
       }
+    }
+    // the next row's length (for the hint) is read while the row streams
+    int32_t nl_first = 0;
+    if (tid == 0 && row + gridDim.x < p.num_rows) nl_first = __ldg(p.seq_lens + row + gridDim.x);
+    for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
+    cbar();  // also: every thread is done with the previous row's shared state
+    if (!small && !hinted) sample_threshold(S, p, r, nq, par);
+    stream_row_wb(S, p, r, nq, g, cur, policy, timed_out, dfr);
+    if (tid == 0) {
       // the CTA's next row that needs a selection, for the hint
-      int32_t nl = 0;
-      for (int64_t rr = row + gridDim.x; rr < p.num_rows; rr += gridDim.x) {
-        const int32_t l = __ldg(p.seq_lens + rr);
-        if (l > p.k) {
-          nl = l;
-          break;
+      int32_t nl = nl_first > p.k ? nl_first : 0;
+      if (nl == 0)
+        for (int64_t rr = row + 2 * (int64_t)gridDim.x; rr < p.num_rows; rr += gridDim.x) {
+          const int32_t l = __ldg(p.seq_lens + rr);
+          if (l > p.k) {
+            nl = l;
+            break;
+          }
         }
-      }
       S.next_len = nl;
       // rank of about 1.25 k in a row of the next row's length
       S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
     }
-    for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
-    cbar();  // also: every thread is done with the previous row's shared state
-    if (!small && !hinted) sample_threshold(S, p, r, nq, par);
-    stream_row_wb(S, p, r, nq, g, cur, policy, timed_out);
     cbar();
     uint32_t n = 0;
 #pragma unroll
@@ -1024,13 +1072,18 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       }
     }
     if (!redo) {
-      emit_ordered(S, p, r, row, sel);
+      deferred_flush(dfr, p.page_bits);  // the previous fast row's transform, if unfinished
+      emit_ordered(S, p, row, sel);
+      deferred_start(dfr, p.out + row * p.k, r.page_row, k);
     } else {
       emit_selected(S, p, r, row, sel, par, false);
       // hist1 is the bitmap now: clear it for the next exact row
       for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
+
+  cbar();  // the last fast row's indices, written by every warp, are visible to all
+  deferred_flush(dfr, p.page_bits);
 
   // Every issued chunk was taken by its warp, so no copy is in flight -- unless
   // a wait gave up; then each warp waits (bounded) for its outstanding copies.
