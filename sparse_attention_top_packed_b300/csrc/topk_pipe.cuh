@@ -57,27 +57,25 @@ namespace pipe {
 constexpr int kThreads = 256;              // 8 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kBlock = kThreads;
-constexpr int kWChunkQuads = 128;          // 2 KB: 4 consecutive quads per lane
-constexpr int kWStages = 3;                // per-warp ring
+constexpr int kWChunkQuads = 256;          // 4 KB: 8 consecutive quads (32 floats) per lane
+constexpr int kWStages = 2;                // per-warp ring
 constexpr int kChunkQuads = 1024;          // exact mode reads global memory 16 KB at a time
 constexpr int kQuadsPerThread = kChunkQuads / kThreads;  // 4: quads tid + u * kThreads
 constexpr int kHalfElems = kChunkQuads * 2;    // exact mode admits a chunk in two halves of 2048
 constexpr int kKMax = 2048;
 constexpr int kCap = 4096;                 // candidate buffer entries
 constexpr int kRegion = kCap / kWarps;     // fast mode: one region of the buffer per warp
-constexpr int kBins1 = 4096;               // exact mode: key bits [20, 32)
 constexpr int kBins2 = 2048;               // refinement levels (<= 11 bits) / fine histogram
 constexpr int kFineTop = kBins2 - 1;       // fine bins [0, kFineTop); keys above count apart
-constexpr int kSegBits = kBins1 * 32;      // bitmap indices per emission segment
-constexpr uint32_t kMaskBin = 0xFFF00000u;  // key bits of a level-1 bin
+constexpr int kSegBits = kBins2 * 32;      // bitmap indices per emission segment
+constexpr uint32_t kMaskBin = 0xFFE00000u;  // key bits of an exact-mode histogram bin (top 11)
 constexpr uint32_t kMaskSub = 0xFFFFFC00u;  // key bits of a level-2 sub-bin
 
 static_assert(kQuadsPerThread == 4, "exact mode: each thread takes four quads of a chunk");
 // After an exact compaction the buffer holds k entries; a half chunk must fit.
 static_assert(kCap - kKMax >= kHalfElems, "candidate buffer too small for k + half a chunk");
 static_assert(kBins2 >= kKMax, "the output staging row reuses the level-2 histogram");
-// a block of at most one chunk per warp always fits its region
-static_assert(kWChunkQuads * 4 <= kRegion, "a whole chunk must fit a warp's region");
+static_assert(kWChunkQuads == 8 * 32, "each lane takes 8 quads of a chunk");
 
 // Admission / selection rule on the pair (key, nj = ~j): an element passes
 // iff (key & mk, nj & mj) >= (tk, tj) lexicographically.  tf is a float with
@@ -98,7 +96,7 @@ __device__ __forceinline__ Rule rule_prefix(uint32_t mk, uint32_t tk) {
 
 __device__ __forceinline__ Rule rule_all() { return rule_prefix(0u, 0u); }
 
-__device__ __forceinline__ Rule rule_bin(uint32_t bin) { return rule_prefix(kMaskBin, bin << 20); }
+__device__ __forceinline__ Rule rule_bin(uint32_t bin) { return rule_prefix(kMaskBin, bin << 21); }
 
 __device__ __forceinline__ bool rule_pass(const Rule& a, uint32_t key, int32_t j) {
   const uint32_t kk = key & a.mk;
@@ -106,7 +104,7 @@ __device__ __forceinline__ bool rule_pass(const Rule& a, uint32_t key, int32_t j
 }
 
 // Lowest level-1 bin that can hold an admitted key under rule a.
-__device__ __forceinline__ uint32_t rule_low_bin(const Rule& a) { return (a.mk & kMaskBin) ? a.tk >> 20 : 0u; }
+__device__ __forceinline__ uint32_t rule_low_bin(const Rule& a) { return (a.mk & kMaskBin) ? a.tk >> 21 : 0u; }
 
 struct PickOut {
   uint32_t bin, above, count;  // first target: bin holding rank r, count above it, its count
@@ -118,8 +116,7 @@ struct Shared {
   float4 wring[kWarps][kWStages][kWChunkQuads];  // per-warp TMA rings
   uint32_t bkey[kCap];
   int32_t bj[kCap];
-  uint32_t hist1[kBins1];  // exact mode: histogram; then the emission bitmap
-  uint32_t hist2[kBins2];  // fine histogram / refinement levels / staging row
+  uint32_t hist2[kBins2];  // fine histogram / exact-mode histogram / refinement levels / bitmap
   uint64_t wfull[kWarps][kWStages];
   uint32_t scratch[2][kWarps];
   PickOut pick[2];
@@ -387,7 +384,7 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   const uint32_t lo = rule_low_bin(cur);
   if (attempt == 0 && !cur.exact) {
     cbar();
-    const PickOut p1 = pick_bins<kBins1>(S.hist1, lo, k, 0u, S, par);
+    const PickOut p1 = pick_bins<kBins2>(S.hist2, lo, k, 0u, S, par);
     if (p1.bin > lo || cur.mk == 0u) {
       const Rule a = rule_bin(p1.bin);
       filter_buffer(S, n, a, par);
@@ -400,11 +397,12 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   cbar();
   const Rule a = select_buffer(S, n, k, 0u, nullptr, nullptr, par);
   const uint32_t kept = filter_buffer(S, n, a, par);
-  // hist1 must count the buffer exactly again (the bin of the threshold lost entries)
-  for (int b = threadIdx.x; b < kBins1; b += kThreads) S.hist1[b] = 0u;
+  // hist2 must count the buffer exactly again (the selection used it, and the
+  // bin of the threshold lost entries)
+  for (int b = threadIdx.x; b < kBins2; b += kThreads) S.hist2[b] = 0u;
   if (threadIdx.x == 0) S.rule = a;
   cbar();
-  for (uint32_t i = threadIdx.x; i < kept; i += kThreads) atomicAdd(&S.hist1[S.bkey[i] >> 20], 1u);
+  for (uint32_t i = threadIdx.x; i < kept; i += kThreads) atomicAdd(&S.hist2[S.bkey[i] >> 21], 1u);
   cbar();
 }
 
@@ -463,7 +461,7 @@ __device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8
 }
 
 // Exact mode: appends the flagged elements (8 consecutive x) at pos, pos+1, ...
-// and counts them in hist1.
+// and counts them in the histogram of the key's top 11 bits (hist2).
 __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, uint32_t pos, int64_t jb0) {
   for (uint32_t mm = m; mm; mm &= mm - 1u) {
     const int e = __ffs(mm) - 1;
@@ -471,7 +469,7 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
     S.bkey[pos] = key;
     S.bj[pos] = index8(jb0, e);
     ++pos;
-    atomicAdd(&S.hist1[key >> 20], 1u);
+    atomicAdd(&S.hist2[key >> 21], 1u);
   }
 }
 
@@ -526,25 +524,23 @@ __device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const 
 
 // Exact-mode rows (buffer in no particular order): writes the entries that
 // pass `sel` (exactly k of them) in ascending window index, through the page
-// transform, to out_row[0, k), ordering them with a bitmap of the window.
-// `clean`: the bitmap (hist1) is already all zero for the first segment.
-__device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row,
-                                              const Rule sel, Par& par, bool clean) {
-  const int t = threadIdx.x, lane = t & 31;
-  const uint32_t rbase = S.rbase[t >> 5], rcnt = S.rcnt[t >> 5];
-  uint32_t* bm = S.hist1;
-  int32_t* stage = reinterpret_cast<int32_t*>(S.hist2);
+// transform, to out_row[0, k), ordering them with a bitmap of the window in
+// hist2 (kSegBits indices per segment).
+__device__ __noinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row, const Rule sel,
+                                           Par& par) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t rbase = S.rbase[warp], rcnt = S.rcnt[warp];
+  uint32_t* bm = S.hist2;
   const uint32_t k = (uint32_t)p.k;
+  int32_t* o = p.out + row * p.k;
   uint32_t out_base = 0;
   for (int64_t seg = 0; seg < r.L; seg += kSegBits) {
     const int32_t seg_lo = (int32_t)seg;
     const int32_t span = (int32_t)min((int64_t)kSegBits, (int64_t)r.L - seg);
     const int32_t nw = (span + 31) >> 5;
-    if (seg > 0 || !clean) {
-      cbar();  // previous users of the bitmap are done
-      for (int i = 4 * t; i < nw; i += 4 * kThreads) *reinterpret_cast<uint4*>(bm + i) = make_uint4(0u, 0u, 0u, 0u);
-      cbar();
-    }
+    cbar();  // previous users of the bitmap are done
+    for (int i = 4 * t; i < nw; i += 4 * kThreads) *reinterpret_cast<uint4*>(bm + i) = make_uint4(0u, 0u, 0u, 0u);
+    cbar();
     for (uint32_t i = lane; i < rcnt; i += 32) {
       const int32_t j = S.bj[rbase + i];
       if (j >= seg_lo && j - seg_lo < span && rule_pass(sel, S.bkey[rbase + i], j))
@@ -553,7 +549,6 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
     cbar();
     // warp w owns a run of whole 32-word rounds of the bitmap; in each round
     // lane l takes word round * 32 + l, so the ranks come from warp scans
-    const int warp = t >> 5;
     const int32_t wpw = ((nw + kWarps * 32 - 1) / (kWarps * 32)) * 32;
     const int32_t a0 = min(warp * wpw, nw), a1 = min(a0 + wpw, nw);
     uint32_t cnt = 0;
@@ -576,35 +571,16 @@ __device__ __forceinline__ void emit_selected(Shared& S, const Params& p, const 
       uint32_t pos = pos0 + incl - c;
       for (uint32_t b = word; b; b &= b - 1u) {
         if (pos < k)
-          stage[pos] = seg_lo + i * 32 + (__ffs(b) - 1);
+          o[pos] = page_slot(r.page_row, p.page_bits, seg_lo + i * 32 + (__ffs(b) - 1));
         else
           atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
         ++pos;
       }
       pos0 += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    cbar();  // S.wtot is read again in the next segment
     out_base += total;
   }
-  cbar();
-  int32_t* o = p.out + row * p.k;
-  constexpr int U = 4;
-  for (int i0 = t; i0 < p.k; i0 += kThreads * U) {
-    int32_t j[U], pg[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * kThreads;
-      j[u] = i < p.k ? stage[i] : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) pg[u] = i0 + u * kThreads < p.k ? __ldg(r.page_row + (j[u] >> p.page_bits)) : 0;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * kThreads;
-      if (i < p.k) o[i] = pg[u] * (1 << p.page_bits) + (j[u] & ((1 << p.page_bits) - 1));
-    }
-  }
-  cbar();  // every thread is done with the staging row (hist2)
+  cbar();  // every thread is done with the bitmap (hist2) and S.wtot
 }
 
 // ---------------------------------------------------------------------------
@@ -711,20 +687,6 @@ __device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
 // Fast pass: the warp's block of the row through its ring, fixed threshold.
 // ---------------------------------------------------------------------------
 
-// Exclusive prefix over the warp's lanes of v (0 <= v < 32), from the
-// ballots of its five bits: independent votes, no shuffle chain.
-__device__ __forceinline__ uint32_t warp_excl_prefix5(uint32_t v, uint32_t lt, uint32_t& total) {
-  uint32_t pre = 0, tot = 0;
-#pragma unroll
-  for (int b = 0; b < 5; ++b) {
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, (v >> b) & 1u);
-    pre += (uint32_t)__popc(m & lt) << b;
-    tot += (uint32_t)__popc(m) << b;
-  }
-  total = tot;
-  return pre;
-}
-
 __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const Row& r, int64_t nq, uint32_t& g,
                                               WCursor& cur, uint64_t policy, bool& timed_out, Deferred& dfr) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -732,64 +694,67 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
   warp_block(nq, w, q0, q1);
   const float tf = S.rule.tf;
   const uint32_t tk = S.fh_tk, sh = S.fh_sh;
-  const uint32_t lt = lanemask_lt();
+  const int rot = lane & 7;  // rotated quad order: the 8 lanes of a load phase hit 8 distinct bank groups
   uint32_t* rkey = S.bkey + w * kRegion;
   int32_t* rj = S.bj + w * kRegion;
-  const float qnan = __uint_as_float(0x7FC00000u);  // fails every comparison
   uint32_t wcnt = 0, top = 0u;
   bool full = false;
+  uint32_t s = g % kWStages, ph = (g / kWStages) & 1u;
   for (int64_t cq = q0; cq < q1; cq += kWChunkQuads, ++g) {
-    const uint32_t s = g % kWStages;
-    if (!mbar_try_wait(&S.wfull[w][s], (g / kWStages) & 1u) && !timed_out &&
-        !mbar_wait_bounded(&S.wfull[w][s], (g / kWStages) & 1u))
+    if (!mbar_try_wait(&S.wfull[w][s], ph) && !timed_out && !mbar_wait_bounded(&S.wfull[w][s], ph))
       timed_out = true;
     const float4* st = S.wring[w][s];
-    float x[16];
+    // the lane's 32 consecutive floats; bit 4u+c of mr is element 4*((u+rot)&7)+c
+    uint32_t mr = 0u;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {  // lane's 4 consecutive quads, 16 consecutive elements
-      const float4 v = st[4 * lane + u];
-      x[4 * u] = v.x;
-      x[4 * u + 1] = v.y;
-      x[4 * u + 2] = v.z;
-      x[4 * u + 3] = v.w;
+    for (int u = 0; u < 8; ++u) {
+      const float4 v = st[8 * lane + ((u + rot) & 7)];
+      const uint32_t q = (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
+      mr |= q << (4 * u);
     }
-    const int64_t jb = (cq + 4 * lane) * 4 - r.head;  // window index of x[0]
-    if (cq == 0 || cq + kWChunkQuads >= nq) {  // the row's first or last chunk
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        if (!(jb + e >= 0 && jb + e < r.L)) x[e] = qnan;
+    uint32_t m = __funnelshift_l(mr, mr, 4 * rot);  // bit e: element e of the lane's 32
+    const int64_t jb = (cq + 8 * lane) * 4 - r.head;  // window index of element 0
+    if (cq == 0 || cq + kWChunkQuads >= nq) {  // the row's first or last chunk: keep [0, L)
+      const int64_t lo = max(-jb, (int64_t)0), hi = min((int64_t)r.L - jb, (int64_t)32);
+      m = lo >= hi ? 0u : (((hi >= 32) ? 0xFFFFFFFFu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u));
+      m &= __funnelshift_l(mr, mr, 4 * rot);
     }
-    uint32_t m = 0u;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) m |= (x[e] >= tf ? 1u : 0u) << e;
-    // the values are used: order the warp's reads before the next copy into the stage, refill it
+    if (!full) {
+      const uint32_t n = __popc(m);
+      const uint32_t incl = warp_incl_scan(n);
+      const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      if (tot != 0u) {
+        if (wcnt + tot > (uint32_t)kRegion) {
+          full = true;
+          if (lane == 0) S.overflow = 1u;
+        } else {
+          uint32_t pos = wcnt + incl - n;
+          const float* sf = reinterpret_cast<const float*>(st) + 32 * lane;
+          for (uint32_t mm = m; mm; mm &= mm - 1u) {  // ascending e: window order within the lane
+            const int e = __ffs(mm) - 1;
+            const uint32_t key = key_of(sf[e]);
+            rkey[pos] = key;
+            rj[pos] = (int32_t)(jb + e);
+            ++pos;
+            const uint32_t fb = (key - tk) >> sh;
+            if (fb < (uint32_t)kFineTop)
+              atomicAdd(&S.hist2[fb], 1u);
+            else
+              ++top;
+          }
+          wcnt += tot;
+        }
+      }
+    }
+    // the warp is done with the stage: order its reads before the next copy, refill
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) warp_issue(S, cur, p, w, policy);
     deferred_step(dfr, p.page_bits);
-    if (full) continue;
-    uint32_t tot;
-    uint32_t pos = wcnt + warp_excl_prefix5(__popc(m), lt, tot);
-    if (tot == 0u) continue;
-    if (wcnt + tot > (uint32_t)kRegion) {
-      full = true;
-      if (lane == 0) S.overflow = 1u;
-      continue;
+    if (++s == (uint32_t)kWStages) {
+      s = 0u;
+      ph ^= 1u;
     }
-    for (uint32_t mm = m; mm; mm &= mm - 1u) {  // ascending e: window order within the lane
-      const int e = __ffs(mm) - 1;
-      const float xe = (e & 8) ? pick8(x + 8, e & 7) : pick8(x, e & 7);
-      const uint32_t key = key_of(xe);
-      rkey[pos] = key;
-      rj[pos] = (int32_t)(jb + e);
-      ++pos;
-      const uint32_t fb = (key - tk) >> sh;
-      if (fb < (uint32_t)kFineTop)
-        atomicAdd(&S.hist2[fb], 1u);
-      else
-        ++top;
-    }
-    wcnt += tot;
   }
   top = __reduce_add_sync(0xFFFFFFFFu, top);
   if (lane == 0) {
@@ -960,7 +925,6 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     for (int s = 0; s < kWStages; ++s) mbar_init(&S.wfull[w][s], 1);
     fence_barrier_init();
   }
-  for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) {
     S.hint_valid = 0u;
     S.hint_sh = 0u;
@@ -988,7 +952,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     }
     const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
     // ---- row set-up: the threshold (hint, whole row, or sample)
-    const bool small = (nq + kWChunkQuads - 1) / kWChunkQuads <= kWarps;  // each warp one chunk at most
+    const bool small = nq * 4 <= kRegion;  // the whole window fits one warp's region
     const bool hinted = !small && S.hint_valid != 0u;
     if (tid == 0) {
       S.overflow = 0u;
@@ -1040,8 +1004,8 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       }
     } else {
       // the threshold was off: stream the row again, from global memory, exactly
-      for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
       cbar();
+      for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
       if (tid == 0) {
         S.count = 0u;
         S.rule = rule_all();
@@ -1076,9 +1040,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
       emit_ordered(S, p, row, sel);
       deferred_start(dfr, p.out + row * p.k, r.page_row, k);
     } else {
-      emit_selected(S, p, r, row, sel, par, false);
-      // hist1 is the bitmap now: clear it for the next exact row
-      for (int b = tid; b < kBins1 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist1)[b] = make_uint4(0u, 0u, 0u, 0u);
+      emit_selected(S, p, r, row, sel, par);
     }
   }
 
