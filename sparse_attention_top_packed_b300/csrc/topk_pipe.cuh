@@ -123,11 +123,11 @@ struct Shared {
   uint32_t wtot[kWarps];
   uint32_t rbase[kWarps], rcnt[kWarps];  // the buffer, as one region per warp
   uint32_t wmin[kWarps], wmax[kWarps], wtop[kWarps];
-  uint32_t res_key[32];
+  uint32_t res_key[32];  // fast rows: the candidates of the fine bin holding rank k
   int32_t res_j[32];
+  uint32_t res_w[32];    // and the warp whose region holds each
   uint32_t res_n;
   uint32_t pad0_;
-  uint64_t sel_T;     // the k-th largest pair, when resolved in the fine bin
   uint32_t count;     // exact mode: entries in the shared buffer
   uint32_t overflow;  // fast mode: a region overflowed
   Rule rule;          // admission rule of the current row
@@ -774,7 +774,8 @@ __device__ __forceinline__ uint32_t fine_shift(uint32_t d) {
 // Fast rows: the k-th largest pair from the fine histogram.  Returns false
 // (uniformly) when it cannot be settled there -- rank above the histogram's
 // range, or more than 32 candidates in its bin -- and the generic selection
-// must run.  Also proposes the next row's hint (rank hr) and fine shift.
+// must run.  Also proposes the next row's hint (rank hr) and fine shift, and
+// leaves in S.wtot[w] how many of warp w's candidates are selected.
 __device__ __noinline__ bool resolve_fine(Shared& S, uint32_t n, uint32_t k, uint32_t hr, Rule& sel, Rule& hint,
                                           uint32_t& hint_ok, uint32_t& hint_sh, Par& par) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -801,52 +802,70 @@ __device__ __noinline__ bool resolve_fine(Shared& S, uint32_t n, uint32_t k, uin
     // distance; in the same bin the bins were too wide: halve them
     hint_sh = lo_key > hk ? fine_shift(lo_key - hk) : (sh > 0u ? sh - 1u : 0u);
   }
-  if (pk.count == rem) {
-    sel = rule_prefix(0xFFFFFFFFu, lo_key);  // all of the bin and everything above
-    return true;
-  }
-  if (pk.count > 32u) return false;
-  // gather the bin's candidates and rank them by pair in one warp
+  const bool split = pk.count != rem;  // only part of the bin is taken
+  if (split && pk.count > 32u) return false;
+  // one pass over the warp's region: candidates above the bin are selected;
+  // those in the bin are gathered when the bin is split
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
+  uint32_t c = 0;
   for (uint32_t i = lane; i < cnt; i += 32) {
     const uint32_t key = S.bkey[base + i];
-    if (((key - tk) >> sh) == pk.bin) {
-      const uint32_t at = atomicAdd(&S.res_n, 1u);
-      if (at < 32u) {
-        S.res_key[at] = key;
-        S.res_j[at] = S.bj[base + i];
+    const uint32_t fb = (key - tk) >> sh;
+    if (fb > pk.bin) {
+      ++c;
+    } else if (fb == pk.bin) {
+      if (!split) {
+        ++c;
+      } else {
+        const uint32_t at = atomicAdd(&S.res_n, 1u);
+        if (at < 32u) {
+          S.res_key[at] = key;
+          S.res_j[at] = S.bj[base + i];
+          S.res_w[at] = (uint32_t)w;
+        }
       }
     }
   }
-  cbar();
-  if (w == 0) {
-    const uint32_t m = S.res_n;  // == pk.count
-    const uint64_t mine = lane < (int)m ? pair_of(S.res_key[lane], S.res_j[lane]) : 0ull;
-    uint32_t above = 0;
-    for (uint32_t o = 0; o < m; ++o) {
-      const uint64_t other = pair_of(S.res_key[o], S.res_j[o]);
-      above += other > mine ? 1u : 0u;
-    }
-    if (lane < (int)m && above == rem - 1u) S.sel_T = mine;
+  c = __reduce_add_sync(0xFFFFFFFFu, c);
+  if (!split) {
+    if (lane == 0) S.wtot[w] = c;
+    cbar();
+    sel = rule_prefix(0xFFFFFFFFu, lo_key);  // all of the bin and everything above
+    return true;
   }
   cbar();
-  sel = rule_of_pair_prefix(~0ull, S.sel_T);
+  // the bin's m <= 32 candidates, ranked by pair: the rem-th largest is the threshold
+  const uint32_t m = S.res_n;  // == pk.count
+  const uint64_t mine = lane < (int)m ? pair_of(S.res_key[lane], S.res_j[lane]) : 0ull;
+  uint32_t above = 0;
+  for (uint32_t o = 0; o < m; ++o) above += pair_of(S.res_key[o], S.res_j[o]) > mine ? 1u : 0u;
+  const uint32_t tb = __ballot_sync(0xFFFFFFFFu, lane < (int)m && above == rem - 1u);
+  const uint64_t T = __shfl_sync(0xFFFFFFFFu, mine, __ffs(tb) - 1);
+  // plus this warp's gathered candidates at or above the threshold
+  c += __popc(__ballot_sync(0xFFFFFFFFu, lane < (int)m && S.res_w[lane] == (uint32_t)w && mine >= T));
+  if (lane == 0) S.wtot[w] = c;
+  cbar();
+  sel = rule_of_pair_prefix(~0ull, T);
   return true;
 }
 
 // Fast rows: every warp's region is in ascending window index and the regions
 // follow each other in warp order, so the selected entries' output positions
-// are prefix counts -- one pass to count, one to write, no sorting.  Writes
-// the window indices; the page transform follows (Deferred).
-__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t row, const Rule sel) {
+// are prefix counts.  `counted`: S.wtot already holds every warp's number of
+// selected entries (resolve_fine leaves it); otherwise they are counted here.
+// Writes the window indices; the page transform follows (Deferred).
+__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t row, const Rule sel,
+                                             bool counted) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
   const uint32_t lt = lanemask_lt(), k = (uint32_t)p.k;
-  uint32_t c = 0;
-  for (uint32_t i = lane; i < cnt; i += 32) c += rule_pass(sel, S.bkey[base + i], S.bj[base + i]) ? 1u : 0u;
-  c = __reduce_add_sync(0xFFFFFFFFu, c);
-  if (lane == 0) S.wtot[w] = c;
-  cbar();
+  if (!counted) {
+    uint32_t c = 0;
+    for (uint32_t i = lane; i < cnt; i += 32) c += rule_pass(sel, S.bkey[base + i], S.bj[base + i]) ? 1u : 0u;
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (lane == 0) S.wtot[w] = c;
+    cbar();
+  }
   uint32_t pos = 0;
   for (int i = 0; i < w; ++i) pos += S.wtot[i];
   int32_t* o = p.out + row * p.k;
@@ -997,8 +1016,10 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     const uint32_t hr = S.hint_rank;
     Rule sel, hint;
     uint32_t hint_ok = 0u, hint_sh = S.fh_sh;
+    bool counted = false;
     if (!redo) {
-      if (!resolve_fine(S, n, k, hr, sel, hint, hint_ok, hint_sh, par)) {
+      counted = resolve_fine(S, n, k, hr, sel, hint, hint_ok, hint_sh, par);
+      if (!counted) {
         sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par, false);
         hint_sh = (hint_ok && sel.tk > hint.tk) ? fine_shift(sel.tk - hint.tk) : S.fh_sh;
       }
@@ -1026,9 +1047,9 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
           S.hint = hint;
           S.hint_sh = hint_sh;
           S.hint_valid = 1u;
-        } else if (!redo && (uint64_t)n * (uint64_t)S.next_len * 5u >= (uint64_t)6u * k * (uint64_t)r.L) {
+        } else if (!redo && (uint64_t)n * (uint64_t)S.next_len * 20u >= (uint64_t)21u * k * (uint64_t)r.L) {
           // too few candidates for the rank, but the admitted ones scale to
-          // at least 1.2 k in the next row: keep this row's threshold
+          // at least 1.05 k in the next row: keep this row's threshold
           S.hint = rule_prefix(S.rule.mk, S.rule.tk);
           S.hint_sh = S.fh_sh;
           S.hint_valid = 1u;
@@ -1037,7 +1058,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     }
     if (!redo) {
       deferred_flush(dfr, p.page_bits);  // the previous fast row's transform, if unfinished
-      emit_ordered(S, p, row, sel);
+      emit_ordered(S, p, row, sel, counted);
       deferred_start(dfr, p.out + row * p.k, r.page_row, k);
     } else {
       emit_selected(S, p, r, row, sel, par);
