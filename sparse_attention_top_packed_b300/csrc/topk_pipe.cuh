@@ -119,6 +119,8 @@ struct Shared {
   uint32_t hist2[kBins2];  // fine histogram / exact-mode histogram / refinement levels / bitmap
   uint64_t wfull[kWarps][kWStages];
   uint32_t scratch[2][kWarps];
+  uint32_t fsuf[kThreads];  // fine pick: bins of lanes >= this one in its warp's range
+  uint32_t ftot[kWarps];    // fine pick: each warp's range of 256 bins
   PickOut pick[2];
   uint32_t wtot[kWarps];
   uint32_t rbase[kWarps], rcnt[kWarps];  // the buffer, as one region per warp
@@ -132,7 +134,8 @@ struct Shared {
   uint32_t overflow;  // fast mode: a region overflowed
   Rule rule;          // admission rule of the current row
   Rule hint;          // admission rule proposed for the next row
-  uint32_t hint_valid;
+  uint32_t hint_valid;  // thread 0's: the next row may stream with S.hint
+  uint32_t sample;      // this row takes its threshold from a sample (set with the row's rule)
   uint32_t hint_rank;  // rank the next row's hint should reach in this row (0: none)
   int32_t next_len;    // window length of the CTA's next row that needs a selection
   uint32_t fh_tk;      // fine histogram of this row: bins of 2^fh_sh keys from fh_tk
@@ -237,7 +240,8 @@ __device__ __forceinline__ PickOut pick_bins(const uint32_t* hist, uint32_t lo, 
 
 // Keeps the buffer entries i < n that pass `rule` (any order); returns the
 // new count, also stored in S.count.  Starts and ends with a barrier.
-__device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule rule, Par& par) {
+__device__ __noinline__ uint32_t filter_buffer(Shared& S, uint32_t n, const Rule rule) {
+  Par par;  // entered through a barrier: no thread still reads the scratch
   constexpr int E = kCap / kThreads;
   const int t = threadIdx.x;
   uint32_t key[E];
@@ -311,8 +315,14 @@ __device__ __forceinline__ Rule rule_of_pair_prefix(uint64_t M, uint64_t T) {
 //
 // `ready`: hist2 is all zero and S.wmin / S.wmax hold every region's key
 // range (the fast stream leaves both so); otherwise they are made here.
-__device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, uint32_t r2, Rule* hint,
-                                           uint32_t* hint_ok, Par& par, bool ready = false) {
+struct Selection {
+  Rule sel;   // selects the r largest pairs
+  Rule hint;  // key-prefix rule reaching rank r2 (valid when hint_ok)
+  uint32_t hint_ok;
+};
+
+__device__ __noinline__ Selection select_buffer(Shared& S, uint32_t n, uint32_t r, uint32_t r2, bool ready = false) {
+  Par par;  // every pick below follows a barrier
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
@@ -369,17 +379,18 @@ __device__ __noinline__ Rule select_buffer(Shared& S, uint32_t n, uint32_t r, ui
     pos = sh;
     if (pk.count == rem) break;
   }
-  if (hint_ok) {
-    *hint_ok = (r2 != 0u && r2 <= n) ? 1u : 0u;
-    *hint = rule_prefix((uint32_t)(HM >> 32), (uint32_t)(HT >> 32));  // the key part: never higher
-  }
-  return rule_of_pair_prefix(M, T);
+  Selection out;
+  out.sel = rule_of_pair_prefix(M, T);
+  out.hint_ok = (r2 != 0u && r2 <= n) ? 1u : 0u;
+  out.hint = rule_prefix((uint32_t)(HM >> 32), (uint32_t)(HT >> 32));  // the key part: never higher
+  return out;
 }
 
 // The buffer would overflow: raise the threshold.  attempt 0 moves it to the
 // level-1 bin of the k-th largest buffered key; attempt 1 (or when that does
 // not rise) to the exact k-th largest pair.  n > k entries are buffered.
-__device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int attempt, Par& par) {
+__device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int attempt) {
+  Par par;
   const Rule cur = S.rule;  // read before filter_buffer's first barrier; written after it
   const uint32_t lo = rule_low_bin(cur);
   if (attempt == 0 && !cur.exact) {
@@ -387,7 +398,7 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
     const PickOut p1 = pick_bins<kBins2>(S.hist2, lo, k, 0u, S, par);
     if (p1.bin > lo || cur.mk == 0u) {
       const Rule a = rule_bin(p1.bin);
-      filter_buffer(S, n, a, par);
+      filter_buffer(S, n, a);
       if (threadIdx.x == 0) S.rule = a;
       cbar();
       return;
@@ -395,8 +406,8 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   }
   set_regions_contiguous(S, n);
   cbar();
-  const Rule a = select_buffer(S, n, k, 0u, nullptr, nullptr, par);
-  const uint32_t kept = filter_buffer(S, n, a, par);
+  const Rule a = select_buffer(S, n, k, 0u).sel;
+  const uint32_t kept = filter_buffer(S, n, a);
   // hist2 must count the buffer exactly again (the selection used it, and the
   // bin of the threshold lost entries)
   for (int b = threadIdx.x; b < kBins2; b += kThreads) S.hist2[b] = 0u;
@@ -477,7 +488,7 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
 // threshold starting at -inf; the buffer (one shared region, kCap entries) is
 // compacted whenever a half chunk would overflow it.  One block-wide vote per
 // half chunk.  For rows whose fast pass failed (rare).
-__device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const Row& r, int64_t nq, Par& par) {
+__device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const Row r, int64_t nq) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t k = (uint32_t)p.k;
   const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
@@ -510,7 +521,7 @@ __device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const 
 #pragma unroll
         for (int i = 0; i < kWarps; ++i) added += S.wtot[i];
         const uint32_t held = S.count - added;
-        compact(S, held, k, attempt, par);
+        compact(S, held, k, attempt);
         rule = S.rule;
         for (uint32_t mm = m; mm; mm &= mm - 1u) {
           const int e = __ffs(mm) - 1;
@@ -526,8 +537,7 @@ __device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const 
 // pass `sel` (exactly k of them) in ascending window index, through the page
 // transform, to out_row[0, k), ordering them with a bitmap of the window in
 // hist2 (kSegBits indices per segment).
-__device__ __noinline__ void emit_selected(Shared& S, const Params& p, const Row& r, int64_t row, const Rule sel,
-                                           Par& par) {
+__device__ __noinline__ void emit_selected(Shared& S, const Params& p, const Row r, int64_t row, const Rule sel) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t rbase = S.rbase[warp], rcnt = S.rcnt[warp];
   uint32_t* bm = S.hist2;
@@ -587,42 +597,111 @@ __device__ __noinline__ void emit_selected(Shared& S, const Params& p, const Row
 // Per-warp rings.
 // ---------------------------------------------------------------------------
 
-// Warp w's block of a row's aligned quads [0, nq): chunks [c0, c1) of
-// kWChunkQuads quads, contiguous, in warp order, sizes differing by at most 1.
+// Warp w's block of a row's aligned quads [0, nq): quads [q0, q1), contiguous,
+// in warp order, cut at 128-byte units (8 quads) so that the blocks differ by
+// at most one unit.  Its chunks are kWChunkQuads quads from q0 on, the last one
+// partial.
 __device__ __forceinline__ void warp_block(int64_t nq, int w, int64_t& q0, int64_t& q1) {
-  const int64_t nch = (nq + kWChunkQuads - 1) / kWChunkQuads;
-  const int64_t c0 = nch * w / kWarps, c1 = nch * (w + 1) / kWarps;
-  q0 = min(c0 * kWChunkQuads, nq);
-  q1 = min(c1 * kWChunkQuads, nq);
+  const int64_t nu = (nq + 7) >> 3;
+  q0 = min(((nu * w) / kWarps) * 8, nq);
+  q1 = min(((nu * (w + 1)) / kWarps) * 8, nq);
 }
 
-// Lane 0's cursor over its warp's chunk sequence: the warp's block of each of
-// the CTA's rows (blockIdx.x, blockIdx.x + gridDim.x, ... with seq_len > k).
+// A row's descriptor as loaded; the Row is derived from it.
+struct RowRaw {
+  int32_t L, start, table_row;
+};
+
+__device__ __forceinline__ RowRaw load_row_raw(const Params& p, int64_t row) {
+  RowRaw x;
+  x.L = __ldg(p.seq_lens + row);
+  x.start = __ldg(p.row_starts + row);
+  x.table_row = p.row_to_batch ? __ldg(p.row_to_batch + row) : (int32_t)row;
+  return x;
+}
+
+__device__ __forceinline__ Row make_row(const Params& p, int64_t row, const RowRaw& x) {
+  Row r;
+  r.L = x.L > 0 ? x.L : 0;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + x.start);
+  r.head = (int32_t)((a & 15u) >> 2);
+  r.base4 = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
+  r.page_row = p.page_table + (int64_t)x.table_row * p.pt_stride;
+  return r;
+}
+
+// A warp's cursor over its chunk sequence: the warp's block of each of the
+// CTA's rows (blockIdx.x, blockIdx.x + gridDim.x, ... with seq_len > k).
+// Uniform across the warp.
 struct WCursor {
   const float4* src;
-  int64_t left;  // quads of the current block not yet issued
-  int64_t row;
+  int32_t left;  // quads of the current block not yet issued
+  int32_t row;   // row of the current block (num_rows: past the last)
   uint32_t issued;
 };
 
-// Lane 0: issues the warp's next chunk into stage issued % kWStages (whose
-// previous chunk the warp has taken and fenced).  False past the last row.
-__device__ __forceinline__ bool warp_issue(Shared& S, WCursor& cur, const Params& p, int w, uint64_t policy) {
-  while (cur.left == 0) {
-    if (cur.row >= p.num_rows) return false;
-    cur.row += gridDim.x;
-    if (cur.row >= p.num_rows) return false;
-    const Row r = load_row(p, (int32_t)cur.row);
-    if (r.L <= p.k) continue;
-    int64_t q0, q1;
-    warp_block(((int64_t)r.L + r.head + 3) >> 2, w, q0, q1);
-    cur.src = r.base4 + q0;
-    cur.left = q1 - q0;
+// Whole warp: moves the cursor to the block of its next row with seq_len > k
+// (rows that need no selection are skipped 32 at a time).  `ahead` is the
+// descriptor of row `ahead_row`, loaded ahead by the caller: used when it is
+// the row needed, which spares a wait for global memory.  False past the last.
+__device__ __forceinline__ bool cursor_next_row(WCursor& cur, const Params& p, int w, int64_t ahead_row,
+                                                const RowRaw& ahead) {
+  const int lane = threadIdx.x & 31;
+  int64_t row = (int64_t)cur.row + gridDim.x;
+  if (row >= p.num_rows) {
+    cur.row = p.num_rows;
+    return false;
   }
+  int32_t L, st;
+  if (row == ahead_row) {
+    L = ahead.L;
+    st = ahead.start;
+  } else {
+    L = __ldg(p.seq_lens + row);
+    st = __ldg(p.row_starts + row);
+  }
+  if (L <= p.k) {
+    const int64_t r_first = row + gridDim.x;
+    row = p.num_rows;
+    for (int64_t r0 = r_first; r0 < p.num_rows; r0 += 32 * (int64_t)gridDim.x) {
+      const int64_t rr = r0 + (int64_t)lane * gridDim.x;
+      const int32_t l = rr < p.num_rows ? __ldg(p.seq_lens + rr) : 0;
+      const uint32_t b = __ballot_sync(0xFFFFFFFFu, l > p.k);
+      if (b != 0u) {
+        const int src = __ffs(b) - 1;
+        row = r0 + (int64_t)src * gridDim.x;
+        L = __shfl_sync(0xFFFFFFFFu, l, src);
+        st = __ldg(p.row_starts + row);
+        break;
+      }
+    }
+    if (row >= p.num_rows) {
+      cur.row = p.num_rows;
+      return false;
+    }
+  }
+  cur.row = (int32_t)row;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + st);
+  const int32_t head = (int32_t)((a & 15u) >> 2);
+  int64_t q0, q1;
+  warp_block(((int64_t)L + head + 3) >> 2, w, q0, q1);
+  cur.src = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u) + q0;
+  cur.left = (int32_t)(q1 - q0);
+  return true;
+}
+
+// Whole warp: lane 0 issues the warp's next chunk into stage issued % kWStages
+// (whose previous chunk the warp has taken and fenced).  False past the last row.
+__device__ __forceinline__ bool warp_issue(Shared& S, WCursor& cur, const Params& p, int w, uint64_t policy,
+                                           int64_t ahead_row, const RowRaw& ahead) {
+  while (cur.left == 0)
+    if (!cursor_next_row(cur, p, w, ahead_row, ahead)) return false;
   const uint32_t s = cur.issued % kWStages;
-  const uint32_t nquads = (uint32_t)min((int64_t)kWChunkQuads, cur.left);
-  mbar_arrive_expect_tx(&S.wfull[w][s], nquads * 16u);
-  bulk_copy_g2s(&S.wring[w][s][0], cur.src, nquads * 16u, &S.wfull[w][s], policy);
+  const uint32_t nquads = (uint32_t)min(kWChunkQuads, cur.left);
+  if ((threadIdx.x & 31) == 0) {
+    mbar_arrive_expect_tx(&S.wfull[w][s], nquads * 16u);
+    bulk_copy_g2s(&S.wring[w][s][0], cur.src, nquads * 16u, &S.wfull[w][s], policy);
+  }
   cur.src += nquads;
   cur.left -= nquads;
   ++cur.issued;
@@ -641,10 +720,9 @@ __device__ __forceinline__ bool warp_issue(Shared& S, WCursor& cur, const Params
 struct Deferred {
   int32_t* o;               // output row being transformed (null: none)
   const int32_t* page_row;
-  uint32_t next, end;       // this lane's next position to load, the warp's end
-  uint32_t ta, tb;          // positions in the pipeline
+  uint32_t next;            // this lane's next position to load; next - 32 and
+  uint32_t first, end;      // next - 64 are in the pipeline if in [first, end)
   int32_t ja, jb, pgb;
-  bool va, vb;
 };
 
 // The indices of the row were written by every warp: a consumer barrier must
@@ -653,33 +731,28 @@ __device__ __forceinline__ void deferred_start(Deferred& d, int32_t* o, const in
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   d.o = o;
   d.page_row = page_row;
-  d.next = (uint32_t)((uint64_t)k * w / kWarps) + lane;
+  d.first = (uint32_t)((uint64_t)k * w / kWarps) + lane;
+  d.next = d.first;
   d.end = (uint32_t)((uint64_t)k * (w + 1) / kWarps);
-  d.va = d.vb = false;
 }
 
 // One step of the pipeline: store the oldest, load the page of the middle,
 // load the index of the newest.
 __device__ __forceinline__ void deferred_step(Deferred& d, int32_t page_bits) {
   if (d.o == nullptr) return;
-  if (d.vb) d.o[d.tb] = d.pgb * (1 << page_bits) + (d.jb & ((1 << page_bits) - 1));
-  d.vb = d.va;
-  if (d.va) {
-    d.tb = d.ta;
+  const uint32_t tb = d.next - 64u, ta = d.next - 32u;  // wrap around below 0: out of range
+  if (tb >= d.first && tb < d.end) __stcg(d.o + tb, d.pgb * (1 << page_bits) + (d.jb & ((1 << page_bits) - 1)));
+  if (ta >= d.first && ta < d.end) {
     d.jb = d.ja;
     d.pgb = __ldg(d.page_row + (d.ja >> page_bits));
   }
-  d.va = d.next < d.end;
-  if (d.va) {
-    d.ta = d.next;
-    d.ja = d.o[d.next];  // written by other warps of the block before a barrier
-    d.next += 32;
-  }
+  if (d.next < d.end) d.ja = __ldcg(d.o + d.next);  // written by other warps before a barrier (read from L2)
+  d.next += 32u;
 }
 
 __device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
   if (d.o == nullptr) return;
-  while (d.va || d.vb || d.next < d.end) deferred_step(d, page_bits);
+  while (d.next < d.end + 64u) deferred_step(d, page_bits);
   d.o = nullptr;
 }
 
@@ -688,7 +761,8 @@ __device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const Row& r, int64_t nq, uint32_t& g,
-                                              WCursor& cur, uint64_t policy, bool& timed_out, Deferred& dfr) {
+                                              WCursor& cur, uint64_t policy, bool& timed_out, Deferred& dfr,
+                                              int64_t ahead_row, const RowRaw& ahead) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int64_t q0, q1;
   warp_block(nq, w, q0, q1);
@@ -714,8 +788,11 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
     }
     uint32_t m = __funnelshift_l(mr, mr, 4 * rot);  // bit e: element e of the lane's 32
     const int64_t jb = (cq + 8 * lane) * 4 - r.head;  // window index of element 0
-    if (cq == 0 || cq + kWChunkQuads >= nq) {  // the row's first or last chunk: keep [0, L)
-      const int64_t lo = max(-jb, (int64_t)0), hi = min((int64_t)r.L - jb, (int64_t)32);
+    if (cq == 0 || cq + kWChunkQuads >= q1) {  // the row's first or the block's last chunk
+      // keep the window [0, L) and the block's quads [.., q1) (the rest of a
+      // partial chunk's stage is stale)
+      const int64_t lo = max(-jb, (int64_t)0);
+      const int64_t hi = min(min((int64_t)r.L - jb, (q1 - cq - 8 * lane) * 4), (int64_t)32);
       m = lo >= hi ? 0u : (((hi >= 32) ? 0xFFFFFFFFu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u));
       m &= __funnelshift_l(mr, mr, 4 * rot);
     }
@@ -749,7 +826,7 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
     // the warp is done with the stage: order its reads before the next copy, refill
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) warp_issue(S, cur, p, w, policy);
+    warp_issue(S, cur, p, w, policy, ahead_row, ahead);
     deferred_step(dfr, p.page_bits);
     if (++s == (uint32_t)kWStages) {
       s = 0u;
@@ -771,95 +848,249 @@ __device__ __forceinline__ uint32_t fine_shift(uint32_t d) {
   return (uint32_t)(31 - __clz(x));
 }
 
-// Fast rows: the k-th largest pair from the fine histogram.  Returns false
-// (uniformly) when it cannot be settled there -- rank above the histogram's
-// range, or more than 32 candidates in its bin -- and the generic selection
-// must run.  Also proposes the next row's hint (rank hr) and fine shift, and
-// leaves in S.wtot[w] how many of warp w's candidates are selected.
-__device__ __noinline__ bool resolve_fine(Shared& S, uint32_t n, uint32_t k, uint32_t hr, Rule& sel, Rule& hint,
-                                          uint32_t& hint_ok, uint32_t& hint_sh, Par& par) {
+// The fine histogram's bin of rank r (1 <= r <= its total), higher bins
+// first.  Thread t owns bins [8 t, 8 t + 8), warp x the range [256 x,
+// 256 x + 256); each warp has published, before a barrier, its range total
+// (ftot, passed in as `tot`) and per lane the count of its range's bins from
+// that lane's on (fsuf).  One warp, no barrier.
+struct FinePick {
+  uint32_t bin, above, count;  // the bin, the entries in higher bins, its own
+};
+
+// Every thread: publishes its warp's scan of `hist` (S.fsuf, S.ftot).  A
+// consumer barrier must follow before fine_find reads it.
+__device__ __forceinline__ void fine_publish(Shared& S, const uint32_t* hist) {
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 2 * threadIdx.x;
+  const uint4 a = h4[0], b = h4[1];
+  const uint32_t incl = warp_incl_suffix(a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w);
+  S.fsuf[threadIdx.x] = incl;
+  if ((threadIdx.x & 31) == 0) S.ftot[threadIdx.x >> 5] = incl;
+}
+
+__device__ __forceinline__ void fine_totals(const Shared& S, uint32_t (&tot)[kWarps]) {
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) tot[i] = S.ftot[i];
+}
+
+__device__ __forceinline__ FinePick fine_find(const Shared& S, const uint32_t* hist, const uint32_t (&tot)[kWarps],
+                                              uint32_t r) {
+  const int lane = threadIdx.x & 31;
+  uint32_t run = 0, x = 0, ax = 0;
+#pragma unroll
+  for (int i = kWarps - 1; i >= 0; --i) {
+    const uint32_t prev = run;
+    run += tot[i];
+    if (prev < r && run >= r) {
+      x = (uint32_t)i;
+      ax = prev;
+    }
+  }
+  const uint32_t t = x * 32u + (uint32_t)lane;
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 2 * t;
+  const uint4 a = h4[0], b = h4[1];
+  const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const uint32_t own = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+  const uint32_t hi = ax + S.fsuf[t] - own;  // entries in bins above this lane's
+  const uint32_t yb = __ballot_sync(0xFFFFFFFFu, hi < r && hi + own >= r);
+  const int y = yb ? __ffs(yb) - 1 : 0;
+  uint32_t bin = 0u, above = 0u, count = 0u;
+  uint32_t rr = hi;
+#pragma unroll
+  for (int i = 7; i >= 0; --i) {
+    const uint32_t prev = rr;
+    rr += h[i];
+    if (prev < r && rr >= r) {
+      bin = t * 8u + (uint32_t)i;
+      above = prev;
+      count = h[i];
+    }
+  }
+  FinePick out;
+  out.bin = __shfl_sync(0xFFFFFFFFu, bin, y);
+  out.above = __shfl_sync(0xFFFFFFFFu, above, y);
+  out.count = __shfl_sync(0xFFFFFFFFu, count, y);
+  return out;
+}
+
+// Thread 0: the admission rule of the CTA's next row (S.hint).  The row's
+// selection proposed `hint` (reaching rank hr, about 1.25 k scaled to the next
+// row's length) when hint_ok; otherwise a fast row whose admitted count scales
+// to at least 1.05 k of the next row keeps its own rule.  hr == 0: no next row.
+__device__ __forceinline__ void publish_hint(Shared& S, uint32_t hr, uint32_t hint_ok, const Rule& hint,
+                                             uint32_t hint_sh, bool fast, uint32_t n, uint32_t k, int32_t L) {
+  S.hint_valid = 0u;
+  if (hr == 0u) return;
+  if (hint_ok) {
+    S.hint = hint;
+    S.hint_sh = hint_sh;
+    S.hint_valid = 1u;
+  } else if (fast && (uint64_t)n * (uint64_t)S.next_len * 20u >= (uint64_t)21u * k * (uint64_t)L) {
+    S.hint = rule_prefix(S.rule.mk, S.rule.tk);
+    S.hint_sh = S.fh_sh;
+    S.hint_valid = 1u;
+  }
+}
+
+// Fast rows, entered through a barrier after the stream: the exact k-th
+// largest pair from the fine histogram, and the row's selected window indices
+// written to out[row] in ascending order.
+//
+// The bin holding rank k is picked (one barrier); each warp then compacts its
+// region in place to the candidates at or above that bin (window order kept),
+// counting those above it and gathering those in it; the bin's m <= 32
+// candidates are ranked by (key, ~j) in every warp, which settles the k-th
+// largest pair T; each warp's output position is the prefix of the warps'
+// selected counts, and its compacted candidates are written with ballots.
+//
+// Returns false (uniformly, before touching the buffer) when the histogram
+// cannot settle it: the rank lies above its range, or more than 32 candidates
+// share its bin.  Also proposes the next row's hint (rank hr) and fine shift.
+__device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int64_t row, int32_t L, uint32_t n,
+                                                 uint32_t k, uint32_t hr) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t top = 0;
 #pragma unroll
   for (int i = 0; i < kWarps; ++i) top += S.wtop[i];
   if (top >= k) return false;
   const uint32_t tk = S.fh_tk, sh = S.fh_sh;
-  const uint32_t r = k - top;
+  const uint32_t r = k - top;                                  // <= n - top, the histogram's total
   const uint32_t r2 = (hr > top && hr <= n) ? hr - top : 0u;
-  const PickOut pk = pick_bins<kBins2>(S.hist2, 0u, r, r2, S, par);
-  const uint32_t rem = r - pk.above;
+  fine_publish(S, S.hist2);
+  cbar();
+  uint32_t tot[kWarps];
+  fine_totals(S, tot);
+  const FinePick pk = fine_find(S, S.hist2, tot, r);
+  const FinePick p2 = fine_find(S, S.hist2, tot, r2 != 0u ? r2 : r);  // independent of the first
   const uint32_t lo_key = tk + (pk.bin << sh);
-  hint_ok = 0u;
-  hint_sh = sh;
+  Rule hint;
+  uint32_t hint_ok = 0u, hint_sh = sh;
   if (hr != 0u && hr <= top) {
     hint = rule_prefix(0xFFFFFFFFu, tk + ((uint32_t)kFineTop << sh));
     hint_ok = 1u;
-  } else if (r2 != 0u && pk.has2) {
-    const uint32_t hk = tk + (pk.bin2 << sh);
+  } else if (r2 != 0u) {
+    const uint32_t hk = tk + (p2.bin << sh);
     hint = rule_prefix(0xFFFFFFFFu, hk);
     hint_ok = 1u;
     // ranks k and hr a few bins apart: size the next row's bins from their
     // distance; in the same bin the bins were too wide: halve them
     hint_sh = lo_key > hk ? fine_shift(lo_key - hk) : (sh > 0u ? sh - 1u : 0u);
   }
-  const bool split = pk.count != rem;  // only part of the bin is taken
+  const uint32_t rem = r - pk.above;     // rank of the k-th largest inside its bin, 1 <= rem <= count
+  const bool split = pk.count != rem;    // only part of the bin is taken
   if (split && pk.count > 32u) return false;
-  // one pass over the warp's region: candidates above the bin are selected;
-  // those in the bin are gathered when the bin is split
-  const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
-  uint32_t c = 0;
-  for (uint32_t i = lane; i < cnt; i += 32) {
-    const uint32_t key = S.bkey[base + i];
-    const uint32_t fb = (key - tk) >> sh;
-    if (fb > pk.bin) {
-      ++c;
-    } else if (fb == pk.bin) {
-      if (!split) {
-        ++c;
-      } else {
-        const uint32_t at = atomicAdd(&S.res_n, 1u);
-        if (at < 32u) {
-          S.res_key[at] = key;
-          S.res_j[at] = S.bj[base + i];
-          S.res_w[at] = (uint32_t)w;
-        }
+
+  // compaction of the warp's region to the entries at or above the bin, in
+  // batches of 4 entries a lane: all read, then written
+  uint32_t* rkey = S.bkey + w * kRegion;
+  int32_t* rj = S.bj + w * kRegion;
+  const uint32_t cnt = S.rcnt[w], bin = pk.bin, lt = lanemask_lt();
+  uint32_t wc = 0, cin = 0;
+  for (uint32_t i0 = 0; i0 < cnt; i0 += 4 * 32) {
+    uint32_t key[4], bk[4];
+    int32_t jj[4];
+    uint32_t inb = 0u;  // bit u: entry u lies in the bin
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t i = min(i0 + 32u * u + (uint32_t)lane, (uint32_t)kRegion - 1u);
+      key[u] = rkey[i];
+      jj[u] = rj[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool valid = i0 + 32u * u + (uint32_t)lane < cnt;
+      const uint32_t fb = (key[u] - tk) >> sh;
+      bk[u] = __ballot_sync(0xFFFFFFFFu, valid && fb >= bin);
+      inb |= (valid && fb == bin) ? 1u << u : 0u;
+    }
+    __syncwarp();  // every lane has read its entries before any is overwritten
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if ((bk[u] >> lane) & 1u) {
+        const uint32_t q = wc + __popc(bk[u] & lt);
+        rkey[q] = key[u];
+        rj[q] = jj[u];
       }
+      wc += __popc(bk[u]);
+    }
+    // the bin's entries, when only part of it is taken: gathered for ranking
+    const uint32_t nin = split ? (uint32_t)__popc(inb) : 0u;
+    if (__any_sync(0xFFFFFFFFu, nin != 0u)) {
+      uint32_t at = nin ? atomicAdd(&S.res_n, nin) : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if ((inb >> u) & 1u) {
+          if (at < 32u) {  // fewer than count <= 32 are gathered
+            S.res_key[at] = key[u];
+            S.res_j[at] = jj[u];
+            S.res_w[at] = (uint32_t)w;
+          }
+          ++at;
+        }
+      cin += __reduce_add_sync(0xFFFFFFFFu, nin);
     }
   }
-  c = __reduce_add_sync(0xFFFFFFFFu, c);
-  if (!split) {
-    if (lane == 0) S.wtot[w] = c;
-    cbar();
-    sel = rule_prefix(0xFFFFFFFFu, lo_key);  // all of the bin and everything above
-    return true;
+  if (lane == 0) S.wtot[w] = wc - cin;  // selected for sure: above the bin, or all of an unsplit bin
+  if (threadIdx.x == 0) publish_hint(S, hr, hint_ok, hint, hint_sh, true, n, k, L);
+  cbar();
+
+  // the bin's candidates, ranked: the rem-th largest pair is the threshold T
+  uint64_t T = 0ull;
+  uint32_t pos = 0;
+  if (split) {
+    const uint32_t m = pk.count;  // == S.res_n
+    const uint64_t mine = lane < (int)m ? pair_of(S.res_key[lane], S.res_j[lane]) : 0ull;
+    const uint32_t mw = lane < (int)m ? S.res_w[lane] : (uint32_t)kWarps;
+    uint32_t above = 0;
+    for (uint32_t o = 0; o < m; ++o) above += __shfl_sync(0xFFFFFFFFu, mine, o) > mine ? 1u : 0u;
+    const uint32_t tb = __ballot_sync(0xFFFFFFFFu, lane < (int)m && above == rem - 1u);
+    T = __shfl_sync(0xFFFFFFFFu, mine, __ffs(tb) - 1);
+    pos = __popc(__ballot_sync(0xFFFFFFFFu, lane < (int)m && mine >= T && mw < (uint32_t)w));
   }
-  cbar();
-  // the bin's m <= 32 candidates, ranked by pair: the rem-th largest is the threshold
-  const uint32_t m = S.res_n;  // == pk.count
-  const uint64_t mine = lane < (int)m ? pair_of(S.res_key[lane], S.res_j[lane]) : 0ull;
-  uint32_t above = 0;
-  for (uint32_t o = 0; o < m; ++o) above += pair_of(S.res_key[o], S.res_j[o]) > mine ? 1u : 0u;
-  const uint32_t tb = __ballot_sync(0xFFFFFFFFu, lane < (int)m && above == rem - 1u);
-  const uint64_t T = __shfl_sync(0xFFFFFFFFu, mine, __ffs(tb) - 1);
-  // plus this warp's gathered candidates at or above the threshold
-  c += __popc(__ballot_sync(0xFFFFFFFFu, lane < (int)m && S.res_w[lane] == (uint32_t)w && mine >= T));
-  if (lane == 0) S.wtot[w] = c;
-  cbar();
-  sel = rule_of_pair_prefix(~0ull, T);
+#pragma unroll
+  for (int x = 0; x < kWarps; ++x) pos += x < w ? S.wtot[x] : 0u;
+
+  // the compacted entries that are selected, in window order: per batch the
+  // ballots first, then the stores
+  int32_t* o = p.out + row * p.k;
+  bool bad = false;
+  for (uint32_t i0 = 0; i0 < wc; i0 += 4 * 32) {
+    uint32_t key[4], bm[4];
+    int32_t jj[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t i = min(i0 + 32u * u + (uint32_t)lane, (uint32_t)kRegion - 1u);
+      key[u] = rkey[i];
+      jj[u] = rj[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t i = i0 + 32u * u + (uint32_t)lane;
+      const bool take = i < wc && (!split || ((key[u] - tk) >> sh) > bin || pair_of(key[u], jj[u]) >= T);
+      bm[u] = __ballot_sync(0xFFFFFFFFu, take);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t q = pos + __popc(bm[u] & lt);
+      if ((bm[u] >> lane) & 1u) {
+        if (q < k) __stcg(o + q, jj[u]);
+        bad |= q >= k;
+      }
+      pos += __popc(bm[u]);
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
   return true;
 }
 
-// Fast rows: every warp's region is in ascending window index and the regions
-// follow each other in warp order, so the selected entries' output positions
-// are prefix counts.  `counted`: S.wtot already holds every warp's number of
-// selected entries (resolve_fine leaves it); otherwise they are counted here.
-// Writes the window indices; the page transform follows (Deferred).
-__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t row, const Rule sel,
-                                             bool counted) {
+// Fast rows whose selection took the generic path: every warp's region is in
+// ascending window index and the regions follow each other in warp order, so
+// the selected entries' output positions are prefix counts.  Writes the
+// window indices; the page transform follows (Deferred).
+__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t row, const Rule sel) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
   const uint32_t lt = lanemask_lt(), k = (uint32_t)p.k;
-  if (!counted) {
+  {
     uint32_t c = 0;
     for (uint32_t i = lane; i < cnt; i += 32) c += rule_pass(sel, S.bkey[base + i], S.bj[base + i]) ? 1u : 0u;
     c = __reduce_add_sync(0xFFFFFFFFu, c);
@@ -891,49 +1122,90 @@ __device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t
 
 // A row without a hint takes its threshold from kSamples of its own elements:
 // kSamples / 4 quads spread evenly over the window, read from global memory
-// (the same bytes stream through the rings right after).  The threshold is
-// the key prefix of the sample's rank-R element, R = 1.4 k * kSamples / L, so
-// that about 1.4 k of the row's elements reach it; the sample's rank-k element
-// sizes the fine histogram.  It is only a guess: if it admits fewer than k
-// elements or overflows a region, the row is done again in exact mode.
+// (the same bytes stream through the rings right after); lanes outside the
+// window count as the lowest key.  The threshold is the sample's rank-R key,
+// R = 1.4 k * kSamples / L, so that about 1.4 k of the row's elements reach
+// it; the rank-k key (k * kSamples / L) sizes the fine histogram.  Both come
+// from two radix digits of 11 bits (keys to 2^-13 relative precision), the
+// threshold rounded down to its digit.  It is only a guess: if it admits
+// fewer than k elements or overflows a region, the row is done again in
+// exact mode.  Entered through a barrier with hist2 zero; leaves it zero.
 constexpr int kSamples = 4096;
-static_assert(kSamples <= kCap, "the sample is ranked in the candidate buffer");
+static_assert(kSamples <= kCap, "the sample is kept in the candidate buffer");
+static_assert(2 * kBins2 <= kCap, "the second digit's histograms use the index buffer");
 
-__device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const Row& r, int64_t nq, Par& par) {
+__device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const Row r, int64_t nq) {
   constexpr int kSampleQuads = kSamples / 4;
+  constexpr int U = kSampleQuads / kThreads;
+  const int t = threadIdx.x;
+  uint32_t* h1a = reinterpret_cast<uint32_t*>(S.bj);  // second digit under the rank-R digit
+  uint32_t* h1b = h1a + kBins2;                        // ... and under the rank-k digit
+  float4 v[U];
 #pragma unroll
-  for (int u = 0; u < kSampleQuads / kThreads; ++u) {
-    const int s = threadIdx.x + u * kThreads;
+  for (int u = 0; u < U; ++u) {
+    const int64_t q = ((2 * (int64_t)(t + u * kThreads) + 1) * nq) / (2 * kSampleQuads);
+    v[u] = __ldg(r.base4 + q);
+  }
+  for (int b = t; b < 2 * kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(h1a)[b] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int s = t + u * kThreads;
     const int64_t q = ((2 * (int64_t)s + 1) * nq) / (2 * kSampleQuads);
-    const float4 v = __ldg(r.base4 + q);
-    const float f[4] = {v.x, v.y, v.z, v.w};
+    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int64_t j = q * 4 - r.head + e;
-      const bool in = j >= 0 && j < r.L;
-      S.bkey[4 * s + e] = in ? key_of(f[e]) : 0u;  // below every real key
-      S.bj[4 * s + e] = in ? (int32_t)j : 0;
+      const uint32_t key = (j >= 0 && j < r.L) ? key_of(f[e]) : 0u;
+      S.bkey[4 * s + e] = key;
+      atomicAdd(&S.hist2[key >> 21], 1u);
     }
   }
-  set_regions_contiguous(S, kSamples);
-  cbar();
   const int64_t want = (7 * (int64_t)p.k * kSamples) / (5 * (int64_t)r.L) + 1;
-  const uint32_t rank = (uint32_t)min(want, (int64_t)kSamples);
-  const uint32_t rank_k = (uint32_t)min((int64_t)p.k * kSamples / r.L + 1, (int64_t)rank);
-  const Rule sel = select_buffer(S, kSamples, rank, 0u, nullptr, nullptr, par);
+  const uint32_t R = (uint32_t)min(want, (int64_t)kSamples);
+  const uint32_t Rk = (uint32_t)min((int64_t)p.k * kSamples / r.L + 1, (int64_t)R);
   cbar();
-  const Rule tau = select_buffer(S, kSamples, rank_k, 0u, nullptr, nullptr, par);  // sizes the bins
+  fine_publish(S, S.hist2);
   cbar();
-  for (uint32_t b = threadIdx.x; b < (uint32_t)kBins2; b += kThreads) S.hist2[b] = 0u;
-  if (threadIdx.x == 0) {
-    S.rule = rule_prefix(sel.mk, sel.tk);
+  uint32_t tot[kWarps];
+  fine_totals(S, tot);
+  const FinePick a = fine_find(S, S.hist2, tot, R), b = fine_find(S, S.hist2, tot, Rk);
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t key = S.bkey[4 * (t + u * kThreads) + e];  // this thread's own entries
+      const uint32_t d = key >> 21;
+      if (d == a.bin)
+        atomicAdd(&h1a[(key >> 10) & (kBins2 - 1)], 1u);
+      else if (d == b.bin)
+        atomicAdd(&h1b[(key >> 10) & (kBins2 - 1)], 1u);
+    }
+  cbar();  // every warp is done with hist2 and the first scan
+  for (int i = t; i < kBins2 / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fine_publish(S, h1a);
+  cbar();
+  fine_totals(S, tot);
+  const uint32_t a1 = fine_find(S, h1a, tot, R - a.above).bin;
+  uint32_t b1;
+  if (b.bin == a.bin) {
+    b1 = fine_find(S, h1a, tot, Rk - b.above).bin;
+  } else {
+    cbar();
+    fine_publish(S, h1b);
+    cbar();
+    fine_totals(S, tot);
+    b1 = fine_find(S, h1b, tot, Rk - b.above).bin;
+  }
+  if (t == 0) {
+    const uint32_t thr = (a.bin << 21) | (a1 << 10), tau = (b.bin << 21) | (b1 << 10);
+    S.rule = rule_prefix(0xFFFFFC00u, thr);
     S.fh_tk = S.rule.tk;
-    S.fh_sh = fine_shift(tau.tk > S.rule.tk ? tau.tk - S.rule.tk : 0u);
+    S.fh_sh = fine_shift(tau > thr ? tau - thr : 0u);
   }
   cbar();
 }
 
-__global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
+__global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Shared& S = *reinterpret_cast<Shared*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -950,21 +1222,22 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
   }
   __syncthreads();
   // each warp starts its ring
+  RowRaw nx = load_row_raw(p, blockIdx.x);  // the grid never exceeds num_rows
   WCursor cur;
   cur.src = nullptr;
   cur.left = 0;
-  cur.row = (int64_t)blockIdx.x - gridDim.x;
+  cur.row = (int32_t)blockIdx.x - (int32_t)gridDim.x;
   cur.issued = 0;
-  if (lane == 0)
-    for (int s = 0; s < kWStages; ++s) warp_issue(S, cur, p, w, policy);
+  for (int s = 0; s < kWStages; ++s) warp_issue(S, cur, p, w, policy, blockIdx.x, nx);
 
-  Par par;
   uint32_t g = 0;  // chunks this warp took from its ring
   Deferred dfr;
   dfr.o = nullptr;
 
   for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
-    const Row r = load_row(p, (int32_t)row);
+    const Row r = make_row(p, row, nx);
+    const bool has_next = row + gridDim.x < p.num_rows;
+    if (has_next) nx = load_row_raw(p, row + gridDim.x);  // used by the next iteration
     if (r.L <= p.k) {
       emit_whole_window<kThreads>(p, (int32_t)row, r, 0u, 1u);
       continue;
@@ -972,8 +1245,12 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
     // ---- row set-up: the threshold (hint, whole row, or sample)
     const bool small = nq * 4 <= kRegion;  // the whole window fits one warp's region
-    const bool hinted = !small && S.hint_valid != 0u;
     if (tid == 0) {
+      // S.hint_valid is thread 0's own write (after the previous row's
+      // selection, with no barrier since): the decision is taken here and
+      // published through the barrier below
+      const bool hinted = !small && S.hint_valid != 0u;
+      S.sample = (!small && !hinted) ? 1u : 0u;
       S.overflow = 0u;
       S.res_n = 0u;
       if (small) {
@@ -986,16 +1263,14 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
         S.fh_sh = S.hint_sh;
       }
     }
-    // the next row's length (for the hint) is read while the row streams
-    int32_t nl_first = 0;
-    if (tid == 0 && row + gridDim.x < p.num_rows) nl_first = __ldg(p.seq_lens + row + gridDim.x);
     for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
     cbar();  // also: every thread is done with the previous row's shared state
-    if (!small && !hinted) sample_threshold(S, p, r, nq, par);
-    stream_row_wb(S, p, r, nq, g, cur, policy, timed_out, dfr);
+    if (S.sample != 0u) sample_threshold(S, p, r, nq);
+    stream_row_wb(S, p, r, nq, g, cur, policy, timed_out, dfr, row + gridDim.x, nx);
+    deferred_flush(dfr, p.page_bits);  // the previous fast row's transform, if unfinished
     if (tid == 0) {
       // the CTA's next row that needs a selection, for the hint
-      int32_t nl = nl_first > p.k ? nl_first : 0;
+      int32_t nl = has_next && nx.L > p.k ? nx.L : 0;
       if (nl == 0)
         for (int64_t rr = row + 2 * (int64_t)gridDim.x; rr < p.num_rows; rr += gridDim.x) {
           const int32_t l = __ldg(p.seq_lens + rr);
@@ -1016,11 +1291,14 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
     const uint32_t hr = S.hint_rank;
     Rule sel, hint;
     uint32_t hint_ok = 0u, hint_sh = S.fh_sh;
-    bool counted = false;
+    bool emitted = false;
     if (!redo) {
-      counted = resolve_fine(S, n, k, hr, sel, hint, hint_ok, hint_sh, par);
-      if (!counted) {
-        sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par, false);
+      emitted = select_emit_fine(S, p, row, r.L, n, k, hr);
+      if (!emitted) {
+        const Selection x = select_buffer(S, n, k, hr);
+        sel = x.sel;
+        hint = x.hint;
+        hint_ok = x.hint_ok;
         hint_sh = (hint_ok && sel.tk > hint.tk) ? fine_shift(sel.tk - hint.tk) : S.fh_sh;
       }
     } else {
@@ -1032,36 +1310,23 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(Params p) {
         S.rule = rule_all();
       }
       cbar();
-      stream_row_exact(S, p, r, nq, par);
+      stream_row_exact(S, p, r, nq);
       cbar();
       n = S.count;
       set_regions_contiguous(S, n);
       cbar();
-      sel = select_buffer(S, n, k, hr, &hint, &hint_ok, par, false);
+      const Selection x = select_buffer(S, n, k, hr);
+      sel = x.sel;
+      hint = x.hint;
+      hint_ok = x.hint_ok;
       hint_sh = (hint_ok && sel.tk > hint.tk) ? fine_shift(sel.tk - hint.tk) : S.fh_sh;
     }
-    if (tid == 0) {
-      S.hint_valid = 0u;
-      if (hr != 0u) {
-        if (hint_ok) {
-          S.hint = hint;
-          S.hint_sh = hint_sh;
-          S.hint_valid = 1u;
-        } else if (!redo && (uint64_t)n * (uint64_t)S.next_len * 20u >= (uint64_t)21u * k * (uint64_t)r.L) {
-          // too few candidates for the rank, but the admitted ones scale to
-          // at least 1.05 k in the next row: keep this row's threshold
-          S.hint = rule_prefix(S.rule.mk, S.rule.tk);
-          S.hint_sh = S.fh_sh;
-          S.hint_valid = 1u;
-        }
-      }
-    }
+    if (tid == 0 && !emitted) publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
     if (!redo) {
-      deferred_flush(dfr, p.page_bits);  // the previous fast row's transform, if unfinished
-      emit_ordered(S, p, row, sel, counted);
+      if (!emitted) emit_ordered(S, p, row, sel);
       deferred_start(dfr, p.out + row * p.k, r.page_row, k);
     } else {
-      emit_selected(S, p, r, row, sel, par);
+      emit_selected(S, p, r, row, sel);
     }
   }
 
