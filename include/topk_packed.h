@@ -100,8 +100,9 @@ typedef enum {
   TOPK_PATH_AUTO = 0,      /* what topk_packed uses (currently TOPK_PATH_PIPE) */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
   TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
-  TOPK_PATH_PIPE = 3       /* persistent CTAs, two per SM: one TMA ring per CTA, candidate buffer
-                              with a threshold carried from row to row, bitmap-ordered emission */
+  TOPK_PATH_PIPE = 3       /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over
+                              contiguous blocks of the row, candidates kept in window order with a
+                              threshold carried from row to row, ordered emission by prefix counts */
 } topk_path_t;
 
 /* Launch choices; zero fields mean "choose automatically". */

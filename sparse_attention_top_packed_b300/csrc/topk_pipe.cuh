@@ -10,37 +10,40 @@
 // over the persistent grid):
 //
 //  * Load.  A row's window, from its start rounded down to 16 bytes, is cut
-//    into 2 KB chunks; warp w owns the w-th eighth of them, a contiguous block.
-//    Each warp streams its blocks, row after row, through its own ring of
-//    kWStages shared-memory stages filled by 1-D TMA bulk copies (L2
-//    evict-first: every byte is read once).  Lane 0 refills a stage as soon as
-//    the warp has taken it, so each warp keeps its next chunks -- also those of
-//    its block of the next row -- in flight while a row is finished.  Lanes
-//    before the window start and past its end are masked in registers
-//    (section 2 of the page, without writing the buffer).
+//    into 128-byte units; warp w owns the w-th eighth of them, a contiguous
+//    block, and streams it in 4 KB chunks (the last one partial) through its
+//    own ring of kWStages shared-memory stages filled by 1-D TMA bulk copies
+//    (L2 evict-first: every byte is read once).  Lane 0 refills a stage as
+//    soon as the warp has taken it, so each warp keeps its next chunks -- also
+//    those of its block of the next row -- in flight while a row is finished.
+//    Lanes before the window start, past its end and past the block's end are
+//    masked in registers (section 2 of the page, without writing the buffer).
 //
 //  * Admission.  Every row streams with a fixed threshold, a guess at a lower
 //    bound of its k-th largest key: from the CTA's previous row (the key that
 //    about 1.25 k of its candidates reach, scaled to the new length), or from
-//    a strided sample of the row itself.  Each lane takes 16 consecutive floats
-//    of a chunk, compares them with the threshold, gives the stage back, and
-//    appends its passing elements (order-preserving key, window index) to the
-//    warp's region of the candidate buffer, at positions from an exclusive
-//    prefix of the lanes' counts (five ballots).  A region therefore holds its
-//    candidates in ascending window index, and the regions follow each other
-//    in warp order.  Each
-//    candidate is also counted in a fine histogram: 2047 equal key bins above
-//    the threshold, sized so that the k-th largest key lands in about bin 384.
+//    a strided sample of the row itself.  Each lane compares 32 consecutive
+//    floats of a chunk with the threshold and appends the passing ones (order-
+//    preserving key, window index) to the warp's region of the candidate
+//    buffer, at positions from a prefix of the lanes' counts.  A region
+//    therefore holds its candidates in ascending window index, and the regions
+//    follow each other in warp order.  Each candidate is also counted in a
+//    fine histogram: 2047 equal key bins above the threshold, sized so that
+//    the k-th largest key lands in about bin 384.
 //
 //  * Selection.  The bin of the k-th largest key comes from the fine
-//    histogram; the few candidates in that bin are ranked by (key, ~j) in one
-//    warp, which gives the exact k-th largest pair -- a tie goes to the lower
-//    j.  When the histogram cannot settle it (the rank lies above its range, or
-//    its bin is crowded), a radix select over the buffer does.
+//    histogram (each warp scans its 256 bins and publishes the scan; after one
+//    barrier any warp finds a rank's bin alone).  Each warp compacts its region
+//    in place to the entries at or above that bin, and the bin's own entries
+//    (at most 32) are gathered and ranked by (key, ~j) in every warp, which
+//    gives the exact k-th largest pair -- a tie goes to the lower j.  When the
+//    histogram cannot settle it (the rank lies above its range, or its bin is
+//    crowded), a radix select over the buffer does.
 //
 //  * Emission.  Selected entries' output positions are prefix counts over the
-//    ordered regions: the page transform of section 1 is applied and the row is
-//    written in ascending order with warp ballots, no sorting.
+//    ordered regions: each warp writes its selected window indices in
+//    ascending order with ballots, no sorting.  The page transform of section
+//    1 is applied in place while the next row streams (Deferred).
 //
 //  * Safety net.  If a threshold admitted fewer than k elements, or a region
 //    overflowed, the row is streamed again from global memory in exact mode: a
