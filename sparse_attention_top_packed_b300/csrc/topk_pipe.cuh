@@ -132,6 +132,8 @@ struct Shared {
   int32_t res_j[32];
   uint32_t res_w[32];    // and the warp whose region holds each
   uint32_t res_n;
+  uint32_t wcin[kWarps];            // fast rows: entries of the k-th key's bin in each warp's region
+  uint32_t wkmin[kWarps], wkmax[kWarps];  // ... and their key range (crowded bins)
   uint32_t pad0_;
   uint32_t count;     // exact mode: entries in the shared buffer
   uint32_t overflow;  // fast mode: a region overflowed
@@ -980,14 +982,18 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
   }
   const uint32_t rem = r - pk.above;     // rank of the k-th largest inside its bin, 1 <= rem <= count
   const bool split = pk.count != rem;    // only part of the bin is taken
-  if (split && pk.count > 32u) return false;
+  // more than 32 entries in a split bin: too many to rank in a warp.  When
+  // they all share one key (ties, common with bf16 scores) the lowest window
+  // indices win, which prefix counts settle; otherwise the generic selection
+  // runs on the compacted buffer (it keeps every entry at or above the bin).
+  const bool crowded = split && pk.count > 32u;
 
   // compaction of the warp's region to the entries at or above the bin, in
   // batches of 4 entries a lane: all read, then written
   uint32_t* rkey = S.bkey + w * kRegion;
   int32_t* rj = S.bj + w * kRegion;
   const uint32_t cnt = S.rcnt[w], bin = pk.bin, lt = lanemask_lt();
-  uint32_t wc = 0, cin = 0;
+  uint32_t wc = 0, cin = 0, kmin = 0xFFFFFFFFu, kmax = 0u;
   for (uint32_t i0 = 0; i0 < cnt; i0 += 4 * 32) {
     uint32_t key[4], bk[4];
     int32_t jj[4];
@@ -1016,8 +1022,17 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
       wc += __popc(bk[u]);
     }
     // the bin's entries, when only part of it is taken: gathered for ranking
+    // (or, in a crowded bin, counted with their key range)
     const uint32_t nin = split ? (uint32_t)__popc(inb) : 0u;
-    if (__any_sync(0xFFFFFFFFu, nin != 0u)) {
+    if (crowded) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if ((inb >> u) & 1u) {
+          kmin = min(kmin, key[u]);
+          kmax = max(kmax, key[u]);
+        }
+      cin += __reduce_add_sync(0xFFFFFFFFu, nin);
+    } else if (__any_sync(0xFFFFFFFFu, nin != 0u)) {
       uint32_t at = nin ? atomicAdd(&S.res_n, nin) : 0u;
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -1032,14 +1047,48 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
       cin += __reduce_add_sync(0xFFFFFFFFu, nin);
     }
   }
-  if (lane == 0) S.wtot[w] = wc - cin;  // selected for sure: above the bin, or all of an unsplit bin
+  if (crowded) {
+    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  }
+  if (lane == 0) {
+    S.wtot[w] = wc - cin;  // selected for sure: above the bin, or all of an unsplit bin
+    S.rcnt[w] = wc;        // the region is now its compacted entries
+    S.wcin[w] = cin;
+    S.wkmin[w] = kmin;
+    S.wkmax[w] = kmax;
+  }
   if (threadIdx.x == 0) publish_hint(S, hr, hint_ok, hint, hint_sh, true, n, k, L);
   cbar();
+  // a crowded bin with several keys: the generic selection, on the compacted
+  // regions (uniform: every warp reads the same published ranges)
+  uint32_t quota = 0u;  // crowded single-key bin: this warp's entries of the bin that are taken
+  if (crowded) {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u, before = 0u;
+#pragma unroll
+    for (int x = 0; x < kWarps; ++x) {
+      lo = min(lo, S.wkmin[x]);
+      hi = max(hi, S.wkmax[x]);
+      before += x < w ? S.wcin[x] : 0u;
+    }
+    if (lo != hi) return false;
+    quota = rem > before ? min(rem - before, cin) : 0u;
+  }
 
   // the bin's candidates, ranked: the rem-th largest pair is the threshold T
   uint64_t T = 0ull;
   uint32_t pos = 0;
-  if (split) {
+  if (crowded) {
+    // warp x takes min(max(rem - (bin entries of warps < x), 0), its own)
+    uint32_t acc = 0u;
+#pragma unroll
+    for (int x = 0; x < kWarps; ++x) {
+      const uint32_t c = S.wcin[x];
+      const uint32_t q = rem > acc ? min(rem - acc, c) : 0u;
+      pos += x < w ? q : 0u;
+      acc += c;
+    }
+  } else if (split) {
     const uint32_t m = pk.count;  // == S.res_n
     const uint64_t mine = lane < (int)m ? pair_of(S.res_key[lane], S.res_j[lane]) : 0ull;
     const uint32_t mw = lane < (int)m ? S.res_w[lane] : (uint32_t)kWarps;
@@ -1056,6 +1105,7 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
   // ballots first, then the stores
   int32_t* o = p.out + row * p.k;
   bool bad = false;
+  uint32_t seen = 0u;  // crowded bin: its entries met so far in this warp's region
   for (uint32_t i0 = 0; i0 < wc; i0 += 4 * 32) {
     uint32_t key[4], bm[4];
     int32_t jj[4];
@@ -1068,7 +1118,16 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const uint32_t i = i0 + 32u * u + (uint32_t)lane;
-      const bool take = i < wc && (!split || ((key[u] - tk) >> sh) > bin || pair_of(key[u], jj[u]) >= T);
+      const bool above = ((key[u] - tk) >> sh) > bin;
+      bool take;
+      if (crowded) {
+        // the bin's entries in window order: the first `quota` are taken
+        const uint32_t bi = __ballot_sync(0xFFFFFFFFu, i < wc && !above);
+        take = i < wc && (above || seen + __popc(bi & lt) < quota);
+        seen += __popc(bi);
+      } else {
+        take = i < wc && (!split || above || pair_of(key[u], jj[u]) >= T);
+      }
       bm[u] = __ballot_sync(0xFFFFFFFFu, take);
     }
 #pragma unroll
@@ -1298,6 +1357,9 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     if (!redo) {
       emitted = select_emit_fine(S, p, row, r.L, n, k, hr);
       if (!emitted) {
+        n = 0u;  // the regions may have been compacted (every entry at or above the k-th key's bin kept)
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i) n += S.rcnt[i];
         const Selection x = select_buffer(S, n, k, hr);
         sel = x.sel;
         hint = x.hint;
