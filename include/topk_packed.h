@@ -23,7 +23,8 @@
  *     out[i * k + t] = page_row[j_t >> page_bits] * page_size + (j_t & (page_size - 1))
  *           for the t-th smallest j_t in S, and -1 for min(k, n) <= t < k,
  *     with page_row = page_table + b * pt_stride, b = row_to_batch ? row_to_batch[i] : i,
- *     page_bits = log2(page_size).
+ *     page_bits = log2(page_size).  Without a page table (page_table NULL) the
+ *     transform is the identity: out[i * k + t] = j_t, the raw window index.
  * The result is unique, so it is bit-exact whatever the algorithm.
  */
 #ifndef TOPK_PACKED_H_
@@ -66,9 +67,12 @@ typedef enum {
  *   seq_lens     int32[num_rows]: window length of each row (negative = 0).
  *   row_starts   int32[num_rows]: window column offset of each row.
  *   row_to_batch int32[num_rows] page-table row of each row, or NULL (identity).
- *   page_table   int32 page numbers; row b starts at page_table + b * pt_stride.
+ *   page_table   int32 page numbers; row b starts at page_table + b * pt_stride.  NULL:
+ *                no page transform, the output holds raw window indices.
  *   pt_stride    elements between page-table rows (>= 0; 0 lets every row share one).
- *   page_size    slots per page, a power of two (page_bits = log2(page_size)).
+ *                Not used (nor checked) when page_table is NULL.
+ *   page_size    slots per page, a power of two (page_bits = log2(page_size)).  Not
+ *                used (nor checked) when page_table is NULL.
  *   k            entries per output row, 1 <= k <= TOPK_K_MAX.
  *   out          int32[num_rows * k], row-major, written completely.
  *   num_rows     number of query rows (>= 0; 0 returns TOPK_OK and launches nothing).
@@ -81,10 +85,11 @@ typedef enum {
  *   no NaN inside a window.
  * Returns TOPK_OK once the work is queued.  The call never synchronizes and
  * never reads device arrays on the host.  Errors:
- *   TOPK_ERR_INVALID_ARG  num_rows < 0; k <= 0; page_size <= 0 or not a power of
- *                         two; row_stride < 0 or pt_stride < 0; a required pointer
- *                         NULL while num_rows > 0.
- *   TOPK_ERR_UNSUPPORTED  k > TOPK_K_MAX; scores not 4-byte aligned; page_size > 2^30.
+ *   TOPK_ERR_INVALID_ARG  num_rows < 0; k <= 0; row_stride < 0; with a page table,
+ *                         page_size <= 0 or not a power of two, or pt_stride < 0;
+ *                         scores, seq_lens, row_starts or out NULL while num_rows > 0.
+ *   TOPK_ERR_UNSUPPORTED  k > TOPK_K_MAX; scores not 4-byte aligned; with a page
+ *                         table, page_size > 2^30.
  *   TOPK_ERR_DEVICE       the current device is not sm_103a or cannot be queried.
  *   TOPK_ERR_LAUNCH       the kernel launch was rejected.
  * Thread safety: safe to call from several host threads; calls on different

@@ -66,24 +66,26 @@ def topk_packed_reference(scores, row_stride: int, seq_lens, row_starts, row_to_
 
     ``scores`` is a float32 array read at ``i*row_stride + row_starts[i] + j``;
     ``row_to_batch`` may be None (identity); ``page_table`` is read at
-    ``b*pt_stride + page``.  ``nthreads <= 0`` uses every online core.
+    ``b*pt_stride + page``, or is None for raw window indices (no page
+    transform).  ``nthreads <= 0`` uses every online core.
     """
     lib = _load()
     sc = np.ascontiguousarray(np.asarray(scores, dtype=np.float32)).reshape(-1)
     sl = _i32(seq_lens)
     rs = _i32(row_starts)
     rb = None if row_to_batch is None else _i32(row_to_batch)
-    pt = _i32(page_table).reshape(-1)
+    pt = None if page_table is None else _i32(page_table).reshape(-1)
     n = int(sl.shape[0]) if num_rows is None else int(num_rows)
     if sl.shape[0] < n or rs.shape[0] < n or (rb is not None and rb.shape[0] < n):
         raise ValueError("per-row arrays are shorter than num_rows")
     if k <= 0:
         raise ValueError("k must be positive")
     out = np.empty((n, k), dtype=np.int32)
-    if pt.size == 0:
+    if pt is not None and pt.size == 0:
         pt = np.zeros(1, dtype=np.int32)
     rc = lib.topk_oracle(sc.ctypes.data, int(row_stride), sl.ctypes.data, rs.ctypes.data,
-                         None if rb is None else rb.ctypes.data, pt.ctypes.data, int(pt_stride),
+                         None if rb is None else rb.ctypes.data, None if pt is None else pt.ctypes.data,
+                         int(pt_stride),
                          int(page_size), int(k), out.ctypes.data, n, int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (code {rc})")

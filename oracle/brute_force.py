@@ -55,8 +55,9 @@ def page_slot(page_row, page_size: int, j: int) -> int:
 
 
 def row_result(values, page_row, page_size: int, k: int) -> list[int]:
+    """page_row None: raw window indices (the identity transform)."""
     chosen = select_by_rank(values, k)
-    out = [page_slot(page_row, page_size, j) for j in chosen]
+    out = list(chosen) if page_row is None else [page_slot(page_row, page_size, j) for j in chosen]
     return out + [-1] * (k - len(out))
 
 
@@ -69,7 +70,10 @@ def packed_result(scores_flat, row_stride: int, seq_lens, row_starts, row_to_bat
         base = i * row_stride + int(row_starts[i])
         values = [float(scores_flat[base + j]) for j in range(n)]
         b = i if row_to_batch is None else int(row_to_batch[i])
-        pages_needed = (n + page_size - 1) // page_size
-        page_row = [int(page_table_flat[b * pt_stride + p]) for p in range(pages_needed)]
+        if page_table_flat is None:
+            page_row = None
+        else:
+            pages_needed = (n + page_size - 1) // page_size
+            page_row = [int(page_table_flat[b * pt_stride + p]) for p in range(pages_needed)]
         rows.append(row_result(values, page_row, page_size, k))
     return rows

@@ -22,7 +22,10 @@
  * library implements: the k largest window scores, a tie going to the lower
  * window index, emitted in ascending window index, each index j mapped to
  *   page_row[j >> page_bits] * page_size + (j & (page_size - 1)),
- * and -1 in every slot past min(k, seq_len).
+ * and -1 in every slot past min(k, seq_len).  Without a page table
+ * (page_table NULL) the transform degenerates to the identity: the output is
+ * the window index j itself (a reading of section 1's transform for callers
+ * that want raw indices; page_size and pt_stride are then unused).
  *
  * It is written as the plain definition, not as an algorithm:
  *   1. copy the window of row i: v_j = scores[i*row_stride + row_starts[i] + j],
@@ -50,7 +53,7 @@ typedef struct {
   const int32_t* seq_lens;
   const int32_t* row_starts;
   const int32_t* row_to_batch; /* may be NULL: identity */
-  const int32_t* page_table;
+  const int32_t* page_table; /* may be NULL: raw window indices */
   int64_t pt_stride;
   int32_t page_size;
   int32_t k;
@@ -94,13 +97,17 @@ static void oracle_row(const oracle_problem* p, int32_t i, scored_index* work, i
 
   /* Section 1: table row = row_to_batch[i], or i when the map is absent. */
   const int64_t table_row = p->row_to_batch ? (int64_t)p->row_to_batch[i] : (int64_t)i;
-  const int32_t* page_row = p->page_table + table_row * p->pt_stride;
-  const int32_t page_bits = log2_exact(p->page_size);
   int32_t* out_row = p->out + (int64_t)i * p->k;
-  for (int32_t t = 0; t < m; ++t) {
-    const int32_t j = chosen[t];
-    const int64_t slot = (int64_t)page_row[j >> page_bits] * p->page_size + (j & (p->page_size - 1));
-    out_row[t] = (int32_t)slot;
+  if (p->page_table == NULL) {
+    for (int32_t t = 0; t < m; ++t) out_row[t] = chosen[t];
+  } else {
+    const int32_t* page_row = p->page_table + table_row * p->pt_stride;
+    const int32_t page_bits = log2_exact(p->page_size);
+    for (int32_t t = 0; t < m; ++t) {
+      const int32_t j = chosen[t];
+      const int64_t slot = (int64_t)page_row[j >> page_bits] * p->page_size + (j & (p->page_size - 1));
+      out_row[t] = (int32_t)slot;
+    }
   }
   for (int32_t t = m; t < p->k; ++t) out_row[t] = -1;
 }
@@ -129,16 +136,17 @@ static void* oracle_worker(void* varg) {
 /*
  * Computes out[num_rows * k] for the problem above, rows split over
  * `nthreads` POSIX threads (<= 0: one per online core).  All pointers are
- * host memory.  Returns 0 on success, -1 on invalid arguments (k <= 0,
- * page_size not a positive power of two, negative sizes), -2 when memory
- * for the per-thread work arrays cannot be had.
+ * host memory; page_table may be NULL (raw window indices, page_size and
+ * pt_stride unused).  Returns 0 on success, -1 on invalid arguments (k <= 0,
+ * with a page table: page_size not a positive power of two; negative sizes),
+ * -2 when memory for the per-thread work arrays cannot be had.
  */
 int topk_oracle(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                 const int32_t* row_starts, const int32_t* row_to_batch, const int32_t* page_table,
                 int64_t pt_stride, int32_t page_size, int32_t k, int32_t* out, int32_t num_rows,
                 int32_t nthreads) {
-  if (k <= 0 || num_rows < 0 || row_stride < 0 || pt_stride < 0) return -1;
-  if (page_size <= 0 || (page_size & (page_size - 1)) != 0) return -1;
+  if (k <= 0 || num_rows < 0 || row_stride < 0) return -1;
+  if (page_table != NULL && (pt_stride < 0 || page_size <= 0 || (page_size & (page_size - 1)) != 0)) return -1;
   if (num_rows == 0) return 0;
 
   oracle_problem p = {scores, row_stride, seq_lens, row_starts, row_to_batch,

@@ -88,7 +88,7 @@ struct Row {
   int32_t L;                // window length, clamped at 0
   const float4* base4;      // 16-byte aligned, at or before the window start
   int32_t head;             // window index 0 is element `head` of base4[0]
-  const int32_t* page_row;  // page_table + table_row * pt_stride
+  const int32_t* page_row;  // page_table + table_row * pt_stride; null without a page table
 };
 
 __device__ __forceinline__ Row load_row(const Params& p, int32_t row) {
@@ -100,7 +100,7 @@ __device__ __forceinline__ Row load_row(const Params& p, int32_t row) {
   r.head = (int32_t)((a & 15u) >> 2);
   r.base4 = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
   const int64_t table_row = p.row_to_batch ? (int64_t)__ldg(p.row_to_batch + row) : (int64_t)row;
-  r.page_row = p.page_table + table_row * p.pt_stride;
+  r.page_row = p.page_table ? p.page_table + table_row * p.pt_stride : nullptr;
   return r;
 }
 
@@ -126,6 +126,7 @@ __device__ __forceinline__ Part part_of(const Row& r, uint32_t rank, uint32_t pa
 
 // Section 1's transform: page from the high bits of j, offset from the low bits.
 __device__ __forceinline__ int32_t page_slot(const int32_t* page_row, int32_t page_bits, int32_t j) {
+  if (page_row == nullptr) return j;  // no page table: the window index itself
   return __ldg(page_row + (j >> page_bits)) * (1 << page_bits) + (j & ((1 << page_bits) - 1));
 }
 

@@ -126,10 +126,13 @@ int log2_exact(int32_t v) {
   return b;
 }
 
+// `has_table`: a page table is given (without one, page_size and pt_stride
+// are not used and not checked).
 topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_size, int32_t k,
-                          int32_t num_rows, const topk_launch_config_t* cfg) {
-  if (num_rows < 0 || k <= 0 || row_stride < 0 || pt_stride < 0) return TOPK_ERR_INVALID_ARG;
-  if (page_size <= 0 || (page_size & (page_size - 1)) != 0) return TOPK_ERR_INVALID_ARG;
+                          int32_t num_rows, const topk_launch_config_t* cfg, bool has_table) {
+  if (num_rows < 0 || k <= 0 || row_stride < 0) return TOPK_ERR_INVALID_ARG;
+  if (has_table && (pt_stride < 0 || page_size <= 0 || (page_size & (page_size - 1)) != 0))
+    return TOPK_ERR_INVALID_ARG;
   if (cfg) {
     if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_PIPE) return TOPK_ERR_INVALID_ARG;
     const int c = cfg->cluster_size;
@@ -137,7 +140,7 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
     if (cfg->max_ctas < 0) return TOPK_ERR_INVALID_ARG;
   }
   if (k > TOPK_K_MAX) return TOPK_ERR_UNSUPPORTED;
-  if (page_size > (1 << 30)) return TOPK_ERR_UNSUPPORTED;
+  if (has_table && page_size > (1 << 30)) return TOPK_ERR_UNSUPPORTED;
   return TOPK_OK;
 }
 
@@ -208,10 +211,10 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
                              int32_t k, int32_t* out, int32_t num_rows,
                              const topk_launch_config_t* config, topk_stream_t stream) {
   g_last_cuda_error = 0;
-  topk_status_t st = check_sizes(row_stride, pt_stride, page_size, k, num_rows, config);
+  topk_status_t st = check_sizes(row_stride, pt_stride, page_size, k, num_rows, config, page_table != nullptr);
   if (st != TOPK_OK) return st;
   if (num_rows == 0) return TOPK_OK;
-  if (!scores || !seq_lens || !row_starts || !page_table || !out) return TOPK_ERR_INVALID_ARG;
+  if (!scores || !seq_lens || !row_starts || !out) return TOPK_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(scores) & 3u) != 0) return TOPK_ERR_UNSUPPORTED;
   const DeviceInfo* d = device_info(st);
   if (!d) return st;
@@ -223,8 +226,8 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   prm.row_starts = row_starts;
   prm.row_to_batch = row_to_batch;
   prm.page_table = page_table;
-  prm.pt_stride = pt_stride;
-  prm.page_bits = log2_exact(page_size);
+  prm.pt_stride = page_table ? pt_stride : 0;
+  prm.page_bits = page_table ? log2_exact(page_size) : 0;
   prm.k = k;
   prm.out = out;
   prm.num_rows = num_rows;
@@ -266,7 +269,7 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
                                const topk_launch_config_t* config, int32_t* path,
                                int32_t* cluster_size, int32_t* grid_ctas, int32_t* threads_per_cta) {
   g_last_cuda_error = 0;
-  topk_status_t st = check_sizes(row_stride, 0, 1, k, num_rows, config);
+  topk_status_t st = check_sizes(row_stride, 0, 1, k, num_rows, config, true);
   if (st != TOPK_OK) return st;
   const DeviceInfo* d = device_info(st);
   if (!d) return st;

@@ -631,7 +631,7 @@ __device__ __forceinline__ Row make_row(const Params& p, int64_t row, const RowR
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + x.start);
   r.head = (int32_t)((a & 15u) >> 2);
   r.base4 = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
-  r.page_row = p.page_table + (int64_t)x.table_row * p.pt_stride;
+  r.page_row = p.page_table ? p.page_table + (int64_t)x.table_row * p.pt_stride : nullptr;
   return r;
 }
 
@@ -1389,7 +1389,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     if (tid == 0 && !emitted) publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
     if (!redo) {
       if (!emitted) emit_ordered(S, p, row, sel);
-      deferred_start(dfr, p.out + row * p.k, r.page_row, k);
+      if (r.page_row != nullptr) deferred_start(dfr, p.out + row * p.k, r.page_row, k);  // else j is final
     } else {
       emit_selected(S, p, r, row, sel);
     }

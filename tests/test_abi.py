@@ -71,7 +71,6 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert _call(scores=None) == INVALID
     assert _call(seq=None) == INVALID
     assert _call(starts=None) == INVALID
-    assert _call(table=None) == INVALID
     assert _call(out=None) == INVALID
     assert _call(k=2049) == UNSUPPORTED
     assert _call(scores=0x1002) == UNSUPPORTED  # not 4-byte aligned
@@ -83,6 +82,20 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert _call(cfg=bad) == INVALID
     bad = binding.LaunchConfig(2, 0, -1)
     assert _call(cfg=bad) == INVALID
+
+
+def test_null_page_table_means_raw_indices_and_frees_page_arguments(lib):
+    """Without a page table the output is the window index itself, so
+    page_size and pt_stride are not checked.  Every call here stops at a
+    later check, before any device work (the pointers are not real)."""
+    INVALID, UNSUPPORTED, OK = 1, 2, 0
+    # a NULL table passes the pointer checks: the next check (alignment) answers
+    assert _call(table=None, scores=0x1002) == UNSUPPORTED
+    # page_size and pt_stride are ignored without a table, checked with one
+    assert _call(table=None, page_size=48, pt_stride=-5, k=2049) == UNSUPPORTED
+    assert _call(page_size=48, k=2049) == INVALID
+    assert _call(pt_stride=-5, k=2049) == INVALID
+    assert _call(table=None, num_rows=0, page_size=0) == OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -121,6 +121,38 @@ def test_unit_pages_identity_table_gives_raw_indices_and_matches_lexsort():
         assert got[i].tolist() == sorted(order[:k].tolist())
 
 
+def test_raw_indices_without_a_page_table_match_the_rank_definition():
+    """page_table None: the selected window indices themselves, ascending, then
+    -1; checked against the closed-form rank on tie-heavy tiny rows."""
+    rng = np.random.default_rng(21)
+    for trial in range(60):
+        kind = ["ties", "int", "normal", "bf16", "equal"][trial % 5]
+        max_len = int(rng.integers(1, 65))
+        k = int(rng.integers(1, max_len + 9))
+        p = random_problem(rng, rows=16, max_len=max_len, k=k, page_size=4, values=kind)
+        got = topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts, p.row_to_batch,
+                                    None, 0, 4, k)
+        for i in range(p.num_rows):
+            L = int(p.seq_lens[i])
+            base = i * p.row_stride + int(p.row_starts[i])
+            chosen = brute_force.select_by_rank_np(p.scores[base: base + L], k)
+            expect = [int(j) for j in chosen] + [-1] * (k - len(chosen))
+            assert got[i].tolist() == expect, (kind, trial, i)
+        assert got.tolist() == brute_force.packed_result(p.scores, p.row_stride, p.seq_lens, p.row_starts,
+                                                         p.row_to_batch, None, 0, 4, k)
+
+
+def test_raw_indices_equal_unit_pages_through_an_identity_table():
+    rng = np.random.default_rng(23)
+    p = random_problem(rng, rows=20, max_len=400, k=50, page_size=1, values="ties")
+    table = np.tile(np.arange(p.pt_stride, dtype=np.int32), p.num_rows)
+    via_table = topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts,
+                                      np.arange(p.num_rows), table, p.pt_stride, 1, 50)
+    raw = topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts, p.row_to_batch,
+                                None, 0, 1, 50)
+    assert np.array_equal(raw, via_table)
+
+
 def test_invariants_hold_on_larger_rows():
     rng = np.random.default_rng(11)
     for values in ["normal", "bf16", "int", "ties"]:
@@ -158,6 +190,9 @@ def test_oracle_rejects_bad_arguments():
         with pytest.raises(ValueError):
             topk_packed_reference(np.zeros(4, np.float32), 4, [4], [0], None, np.zeros(4),
                                   0, args["page_size"], args["k"])
+    # without a page table the page size is not used
+    out = topk_packed_reference(np.array([1, 3, 2, 0], np.float32), 4, [4], [0], None, None, -1, 3, 2)
+    assert out.tolist() == [[1, 2]]
 
 
 def test_oracle_thread_count_does_not_change_result():

@@ -276,6 +276,31 @@ def test_pipe_threshold_carried_between_rows(cuda_device, kind, ctas):
     assert bad.size == 0, f"rows {bad.tolist()} differ"
 
 
+RAW_CASES = [
+    # values, rows, max_len, k: several rows per CTA on one or two CTAs, windows
+    # shorter than k among them, so the row-to-row paths run without a table
+    ("normal", 12, 20000, 2048),
+    ("bf16", 16, 9000, 512),
+    ("ties", 10, 3000, 2048),
+]
+
+
+@pytest.mark.parametrize("case", RAW_CASES, ids=[f"{c[0]}-L{c[2]}-k{c[3]}" for c in RAW_CASES])
+@pytest.mark.parametrize("launch", PATHS + [dict(path="pipe", max_ctas=2)], ids=PATH_IDS + ["pipe2"])
+def test_raw_indices_without_page_table(cuda_device, case, launch):
+    values, rows, max_len, k = case
+    rng = np.random.default_rng(zlib.crc32(f"raw-{values}-{max_len}".encode()))
+    p = wl.random_problem(rng, rows=rows, max_len=max_len, k=k, page_size=64, values=values, slack=9)
+    w = host_problem_to_device(p, cuda_device)
+    out = torch.full((w.num_rows, k), -7, dtype=torch.int32, device=cuda_device)
+    binding.topk_packed_ex(w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch, None,
+                           0, 0, k, out, w.num_rows, **launch)
+    torch.cuda.synchronize()
+    want = topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts, p.row_to_batch,
+                                 None, 0, 1, k)
+    assert np.array_equal(out.cpu().numpy(), want)
+
+
 @pytest.mark.parametrize("launch", PATHS, ids=PATH_IDS)
 def test_kth_largest_is_negative_infinity(cuda_device, launch):
     rng = np.random.default_rng(11)
