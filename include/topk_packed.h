@@ -48,7 +48,8 @@ typedef struct CUstream_st* topk_stream_t;
 typedef enum {
   TOPK_OK = 0,
   TOPK_ERR_INVALID_ARG = 1, /* an argument breaks the contract below; nothing launched */
-  TOPK_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles; nothing launched */
+  TOPK_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles (or the chosen kernel
+                               cannot be resident on this device); nothing launched */
   TOPK_ERR_LAUNCH = 3,      /* the CUDA launch failed (the CUDA error is kept; see below) */
   TOPK_ERR_DEVICE = 4       /* no usable sm_103a device, or a CUDA query failed */
 } topk_status_t;
@@ -105,16 +106,19 @@ typedef enum {
   TOPK_PATH_AUTO = 0,      /* what topk_packed uses (currently TOPK_PATH_PIPE) */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
   TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
-  TOPK_PATH_PIPE = 3       /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over
+  TOPK_PATH_PIPE = 3,      /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over
                               contiguous blocks of the row, candidates kept in window order with a
                               threshold carried from row to row, ordered emission by prefix counts */
+  TOPK_PATH_SPLIT = 4      /* persistent CTAs, one per SM: 8 streaming warps (4-stage TMA rings)
+                              hand each row's candidates, in one of two buffer sets, to 8 finishing
+                              warps that select and emit it while the next row streams */
 } topk_path_t;
 
 /* Launch choices; zero fields mean "choose automatically". */
 typedef struct {
   int32_t path;         /* topk_path_t */
   int32_t cluster_size; /* STREAM: CTAs that share one row (1, 2, 4 or 8); 0 = auto */
-  int32_t max_ctas;     /* STREAM, PIPE, MULTIPASS: upper bound on the grid; 0 = auto */
+  int32_t max_ctas;     /* STREAM, PIPE, SPLIT, MULTIPASS: upper bound on the grid; 0 = auto */
 } topk_launch_config_t;
 
 /*

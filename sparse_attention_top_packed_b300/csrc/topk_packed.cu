@@ -7,6 +7,7 @@
 
 #include "topk_kernels.cuh"
 #include "topk_pipe.cuh"
+#include "topk_split.cuh"
 #include "topk_packed.h"
 
 namespace {
@@ -30,6 +31,7 @@ struct DeviceInfo {
   int stream_clusters[4] = {};    // max resident clusters for sizes 2, 4, 8 (index 1..3)
   int multipass_ctas_per_sm = 0;
   int pipe_ctas_per_sm = 0;
+  int split_ctas_per_sm = 0;
   cudaError_t error = cudaSuccess;
 };
 
@@ -80,13 +82,27 @@ void init_device(int dev) {
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.multipass_ctas_per_sm, topk::topk_multipass_kernel,
                                                       topk::kMultipassThreads, mp_smem);
-  const size_t pipe_smem = sizeof(topk::pipe::Shared);
+  const size_t pipe_smem = sizeof(topk::pipe::PipeSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(topk::pipe::topk_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)pipe_smem);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.pipe_ctas_per_sm, topk::pipe::topk_pipe_kernel,
                                                       topk::pipe::kBlock, pipe_smem);
+  if (e == cudaSuccess) {
+    // the split kernel is optional: if it cannot be made resident, its path
+    // reports TOPK_ERR_UNSUPPORTED and the others are unaffected
+    const size_t split_smem = sizeof(topk::split::SplitSmem);
+    cudaError_t es = cudaFuncSetAttribute(topk::split::topk_split_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)split_smem);
+    if (es == cudaSuccess)
+      es = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.split_ctas_per_sm, topk::split::topk_split_kernel,
+                                                         topk::split::kBlockThreads, split_smem);
+    if (es != cudaSuccess) {
+      d.split_ctas_per_sm = 0;
+      (void)cudaGetLastError();  // clear it: the other kernels stay usable
+    }
+  }
   if (e == cudaSuccess) e = prepare_stream<1>(d.stream_ctas_per_sm, d.sms);
   if (e == cudaSuccess) e = prepare_stream<2>(d.stream_clusters[1], d.sms);
   if (e == cudaSuccess) e = prepare_stream<4>(d.stream_clusters[2], d.sms);
@@ -134,7 +150,7 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
   if (has_table && (pt_stride < 0 || page_size <= 0 || (page_size & (page_size - 1)) != 0))
     return TOPK_ERR_INVALID_ARG;
   if (cfg) {
-    if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_PIPE) return TOPK_ERR_INVALID_ARG;
+    if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_SPLIT) return TOPK_ERR_INVALID_ARG;
     const int c = cfg->cluster_size;
     if (!(c == 0 || c == 1 || c == 2 || c == 4 || c == 8)) return TOPK_ERR_INVALID_ARG;
     if (cfg->max_ctas < 0) return TOPK_ERR_INVALID_ARG;
@@ -155,6 +171,12 @@ Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t num_rows,
   pl.cluster = 1;
   if (pl.path == TOPK_PATH_PIPE) {
     const int64_t cap = (int64_t)d.sms * d.pipe_ctas_per_sm;
+    pl.grid = num_rows < cap ? num_rows : cap;
+    if (cfg && cfg->max_ctas > 0 && pl.grid > cfg->max_ctas) pl.grid = cfg->max_ctas;
+    return pl;
+  }
+  if (pl.path == TOPK_PATH_SPLIT) {
+    const int64_t cap = (int64_t)d.sms * d.split_ctas_per_sm;
     pl.grid = num_rows < cap ? num_rows : cap;
     if (cfg && cfg->max_ctas > 0 && pl.grid > cfg->max_ctas) pl.grid = cfg->max_ctas;
     return pl;
@@ -233,10 +255,15 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   prm.num_rows = num_rows;
 
   const Plan pl = make_plan(*d, row_stride, num_rows, config);
+  if (pl.grid <= 0) return TOPK_ERR_UNSUPPORTED;  // the split kernel cannot be resident here
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl.path == TOPK_PATH_PIPE) {
-    topk::pipe::topk_pipe_kernel<<<(unsigned)pl.grid, topk::pipe::kBlock, sizeof(topk::pipe::Shared), s>>>(prm);
+    topk::pipe::topk_pipe_kernel<<<(unsigned)pl.grid, topk::pipe::kBlock, sizeof(topk::pipe::PipeSmem), s>>>(prm);
+    e = cudaGetLastError();
+  } else if (pl.path == TOPK_PATH_SPLIT) {
+    topk::split::topk_split_kernel<<<(unsigned)pl.grid, topk::split::kBlockThreads, sizeof(topk::split::SplitSmem),
+                                     s>>>(prm);
     e = cudaGetLastError();
   } else if (pl.path == TOPK_PATH_MULTIPASS) {
     topk::topk_multipass_kernel<<<(unsigned)pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), s>>>(prm);
@@ -274,11 +301,13 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
   const DeviceInfo* d = device_info(st);
   if (!d) return st;
   const Plan pl = make_plan(*d, row_stride, num_rows, config);
+  if (pl.grid <= 0 && num_rows > 0) return TOPK_ERR_UNSUPPORTED;
   if (path) *path = pl.path;
   if (cluster_size) *cluster_size = pl.cluster;
   if (grid_ctas) *grid_ctas = (int32_t)pl.grid;
   if (threads_per_cta)
     *threads_per_cta = pl.path == TOPK_PATH_PIPE        ? topk::pipe::kBlock
+                       : pl.path == TOPK_PATH_SPLIT     ? topk::split::kBlockThreads
                        : pl.path == TOPK_PATH_MULTIPASS ? topk::kMultipassThreads
                                                         : topk::kStreamThreads;
   return TOPK_OK;

@@ -115,12 +115,19 @@ struct PickOut {
   uint32_t total;
 };
 
-struct Shared {
-  float4 wring[kWarps][kWStages][kWChunkQuads];  // per-warp TMA rings
+// Per-warp TMA rings of NS stages (one mbarrier per stage).
+template <int NS>
+struct Ring {
+  float4 st[kWarps][NS][kWChunkQuads];
+  uint64_t full[kWarps][NS];
+};
+
+// Shared state of one row in flight: candidate buffer, histogram, rules and
+// the selection's scratch.
+struct alignas(16) Shared {
   uint32_t bkey[kCap];
   int32_t bj[kCap];
   uint32_t hist2[kBins2];  // fine histogram / exact-mode histogram / refinement levels / bitmap
-  uint64_t wfull[kWarps][kWStages];
   uint32_t scratch[2][kWarps];
   uint32_t fsuf[kThreads];  // fine pick: bins of lanes >= this one in its warp's range
   uint32_t ftot[kWarps];    // fine pick: each warp's range of 256 bins
@@ -695,17 +702,18 @@ __device__ __forceinline__ bool cursor_next_row(WCursor& cur, const Params& p, i
   return true;
 }
 
-// Whole warp: lane 0 issues the warp's next chunk into stage issued % kWStages
+// Whole warp: lane 0 issues the warp's next chunk into stage issued % NS
 // (whose previous chunk the warp has taken and fenced).  False past the last row.
-__device__ __forceinline__ bool warp_issue(Shared& S, WCursor& cur, const Params& p, int w, uint64_t policy,
+template <int NS>
+__device__ __forceinline__ bool warp_issue(Ring<NS>& R, WCursor& cur, const Params& p, int w, uint64_t policy,
                                            int64_t ahead_row, const RowRaw& ahead) {
   while (cur.left == 0)
     if (!cursor_next_row(cur, p, w, ahead_row, ahead)) return false;
-  const uint32_t s = cur.issued % kWStages;
+  const uint32_t s = cur.issued % NS;
   const uint32_t nquads = (uint32_t)min(kWChunkQuads, cur.left);
   if ((threadIdx.x & 31) == 0) {
-    mbar_arrive_expect_tx(&S.wfull[w][s], nquads * 16u);
-    bulk_copy_g2s(&S.wring[w][s][0], cur.src, nquads * 16u, &S.wfull[w][s], policy);
+    mbar_arrive_expect_tx(&R.full[w][s], nquads * 16u);
+    bulk_copy_g2s(&R.st[w][s][0], cur.src, nquads * 16u, &R.full[w][s], policy);
   }
   cur.src += nquads;
   cur.left -= nquads;
@@ -765,10 +773,13 @@ __device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
 // Fast pass: the warp's block of the row through its ring, fixed threshold.
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const Row& r, int64_t nq, uint32_t& g,
-                                              WCursor& cur, uint64_t policy, bool& timed_out, Deferred& dfr,
-                                              int64_t ahead_row, const RowRaw& ahead) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+// Warp w (of the kWarps streaming warps) takes its block of the row from its
+// ring (NS stages) into its region of S.
+template <int NS>
+__device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS>& R, int w, const Params& p, const Row& r, int64_t nq,
+                                              uint32_t& g, WCursor& cur, uint64_t policy, bool& timed_out,
+                                              Deferred& dfr, int64_t ahead_row, const RowRaw& ahead) {
+  const int lane = threadIdx.x & 31;
   int64_t q0, q1;
   warp_block(nq, w, q0, q1);
   const float tf = S.rule.tf;
@@ -778,11 +789,11 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
   int32_t* rj = S.bj + w * kRegion;
   uint32_t wcnt = 0, top = 0u;
   bool full = false;
-  uint32_t s = g % kWStages, ph = (g / kWStages) & 1u;
+  uint32_t s = g % NS, ph = (g / NS) & 1u;
   for (int64_t cq = q0; cq < q1; cq += kWChunkQuads, ++g) {
-    if (!mbar_try_wait(&S.wfull[w][s], ph) && !timed_out && !mbar_wait_bounded(&S.wfull[w][s], ph))
+    if (!mbar_try_wait(&R.full[w][s], ph) && !timed_out && !mbar_wait_bounded(&R.full[w][s], ph))
       timed_out = true;
-    const float4* st = S.wring[w][s];
+    const float4* st = R.st[w][s];
     // the lane's 32 consecutive floats; bit 4u+c of mr is element 4*((u+rot)&7)+c
     uint32_t mr = 0u;
 #pragma unroll
@@ -831,9 +842,9 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, const Params& p, const 
     // the warp is done with the stage: order its reads before the next copy, refill
     fence_proxy_async_smem();
     __syncwarp();
-    warp_issue(S, cur, p, w, policy, ahead_row, ahead);
+    warp_issue(R, cur, p, w, policy, ahead_row, ahead);
     deferred_step(dfr, p.page_bits);
-    if (++s == (uint32_t)kWStages) {
+    if (++s == (uint32_t)NS) {
       s = 0u;
       ph ^= 1u;
     }
@@ -950,8 +961,12 @@ __device__ __forceinline__ void publish_hint(Shared& S, uint32_t hr, uint32_t hi
 // Returns false (uniformly, before touching the buffer) when the histogram
 // cannot settle it: the rank lies above its range, or more than 32 candidates
 // share its bin.  Also proposes the next row's hint (rank hr) and fine shift.
-__device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int64_t row, int32_t L, uint32_t n,
-                                                 uint32_t k, uint32_t hr) {
+//
+// `o`: where the row's k window indices go -- its output row in global memory
+// (kToShared false: streaming stores) or a staging row in shared memory.
+template <bool kToShared = false>
+__device__ __forceinline__ bool select_emit_fine(Shared& S, int32_t* o, int32_t L, uint32_t n, uint32_t k,
+                                                 uint32_t hr) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t top = 0;
 #pragma unroll
@@ -1103,7 +1118,7 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
 
   // the compacted entries that are selected, in window order: per batch the
   // ballots first, then the stores
-  int32_t* o = p.out + row * p.k;
+  // o: the output row (or its staging copy)
   bool bad = false;
   uint32_t seen = 0u;  // crowded bin: its entries met so far in this warp's region
   for (uint32_t i0 = 0; i0 < wc; i0 += 4 * 32) {
@@ -1134,7 +1149,12 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
     for (int u = 0; u < 4; ++u) {
       const uint32_t q = pos + __popc(bm[u] & lt);
       if ((bm[u] >> lane) & 1u) {
-        if (q < k) __stcg(o + q, jj[u]);
+        if (q < k) {
+          if constexpr (kToShared)
+            o[q] = jj[u];
+          else
+            __stcg(o + q, jj[u]);
+        }
         bad |= q >= k;
       }
       pos += __popc(bm[u]);
@@ -1148,10 +1168,11 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Params& p, int
 // ascending window index and the regions follow each other in warp order, so
 // the selected entries' output positions are prefix counts.  Writes the
 // window indices; the page transform follows (Deferred).
-__device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t row, const Rule sel) {
+// `o`: the output row in global memory or a staging row in shared memory.
+__device__ __forceinline__ void emit_ordered(Shared& S, int32_t* o, uint32_t k, const Rule sel) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
-  const uint32_t lt = lanemask_lt(), k = (uint32_t)p.k;
+  const uint32_t lt = lanemask_lt();
   {
     uint32_t c = 0;
     for (uint32_t i = lane; i < cnt; i += 32) c += rule_pass(sel, S.bkey[base + i], S.bj[base + i]) ? 1u : 0u;
@@ -1161,7 +1182,6 @@ __device__ __forceinline__ void emit_ordered(Shared& S, const Params& p, int64_t
   }
   uint32_t pos = 0;
   for (int i = 0; i < w; ++i) pos += S.wtot[i];
-  int32_t* o = p.out + row * p.k;
   for (uint32_t i0 = 0; i0 < cnt; i0 += 32) {
     const uint32_t i = i0 + lane;
     bool take = false;
@@ -1267,15 +1287,23 @@ __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const 
   cbar();
 }
 
+// The pipe kernel's shared memory: its rings, then the row state.
+struct PipeSmem {
+  Ring<kWStages> ring;
+  Shared s;
+};
+
 __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  Shared& S = *reinterpret_cast<Shared*>(smem_raw);
+  PipeSmem& M = *reinterpret_cast<PipeSmem*>(smem_raw);
+  Shared& S = M.s;
+  Ring<kWStages>& R = M.ring;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t k = (uint32_t)p.k;
   const uint64_t policy = l2_evict_first_policy();
   bool timed_out = false;
   if (lane == 0) {
-    for (int s = 0; s < kWStages; ++s) mbar_init(&S.wfull[w][s], 1);
+    for (int s = 0; s < kWStages; ++s) mbar_init(&R.full[w][s], 1);
     fence_barrier_init();
   }
   if (tid == 0) {
@@ -1290,7 +1318,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
   cur.left = 0;
   cur.row = (int32_t)blockIdx.x - (int32_t)gridDim.x;
   cur.issued = 0;
-  for (int s = 0; s < kWStages; ++s) warp_issue(S, cur, p, w, policy, blockIdx.x, nx);
+  for (int s = 0; s < kWStages; ++s) warp_issue(R, cur, p, w, policy, blockIdx.x, nx);
 
   uint32_t g = 0;  // chunks this warp took from its ring
   Deferred dfr;
@@ -1328,7 +1356,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
     cbar();  // also: every thread is done with the previous row's shared state
     if (S.sample != 0u) sample_threshold(S, p, r, nq);
-    stream_row_wb(S, p, r, nq, g, cur, policy, timed_out, dfr, row + gridDim.x, nx);
+    stream_row_wb(S, R, w, p, r, nq, g, cur, policy, timed_out, dfr, row + gridDim.x, nx);
     deferred_flush(dfr, p.page_bits);  // the previous fast row's transform, if unfinished
     if (tid == 0) {
       // the CTA's next row that needs a selection, for the hint
@@ -1355,7 +1383,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     uint32_t hint_ok = 0u, hint_sh = S.fh_sh;
     bool emitted = false;
     if (!redo) {
-      emitted = select_emit_fine(S, p, row, r.L, n, k, hr);
+      emitted = select_emit_fine(S, p.out + row * p.k, r.L, n, k, hr);
       if (!emitted) {
         n = 0u;  // the regions may have been compacted (every entry at or above the k-th key's bin kept)
 #pragma unroll
@@ -1388,7 +1416,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     }
     if (tid == 0 && !emitted) publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
     if (!redo) {
-      if (!emitted) emit_ordered(S, p, row, sel);
+      if (!emitted) emit_ordered(S, p.out + row * p.k, k, sel);
       if (r.page_row != nullptr) deferred_start(dfr, p.out + row * p.k, r.page_row, k);  // else j is final
     } else {
       emit_selected(S, p, r, row, sel);
@@ -1403,7 +1431,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
   if (__syncthreads_or(timed_out ? 1 : 0)) {
     if (lane == 0) {
       if (tid == 0) atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
-      for (uint32_t c = g; c < cur.issued; ++c) mbar_wait_bounded(&S.wfull[w][c % kWStages], (c / kWStages) & 1u);
+      for (uint32_t c = g; c < cur.issued; ++c) mbar_wait_bounded(&R.full[w][c % kWStages], (c / kWStages) & 1u);
     }
     __syncthreads();
   }

@@ -17,10 +17,10 @@ from tests.gpu_helpers import check_invariants_all_rows, oracle_rows, sample_row
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [dict(path="pipe"), dict(path="multipass"), dict(path="stream", cluster_size=1),
+PATHS = [dict(path="pipe"), dict(path="split"), dict(path="multipass"), dict(path="stream", cluster_size=1),
          dict(path="stream", cluster_size=2), dict(path="stream", cluster_size=4),
          dict(path="stream", cluster_size=8)]
-PATH_IDS = ["pipe", "multipass", "stream1", "stream2", "stream4", "stream8"]
+PATH_IDS = ["pipe", "split", "multipass", "stream1", "stream2", "stream4", "stream8"]
 
 
 def run(w, **launch):
@@ -203,6 +203,7 @@ def test_prefill_full_size(cuda_device):
     # the cluster path gives the same bits
     out2 = run(w, path="stream", cluster_size=2)
     assert torch.equal(out, out2)
+    assert torch.equal(out, run(w, path="split"))
 
 
 def test_long_context_full_size(cuda_device):
@@ -213,6 +214,7 @@ def test_long_context_full_size(cuda_device):
     assert torch.equal(out, out_id), "row_to_batch=NULL with pt_stride 0 must match the zero map"
     out4 = run(w, path="stream", cluster_size=4)
     assert torch.equal(out, out4)
+    assert torch.equal(out, run(w, path="split"))
 
 
 def test_mixed_full_size(cuda_device):
@@ -221,6 +223,7 @@ def test_mixed_full_size(cuda_device):
     out = _full_size(w, sample=768)
     out2 = run(w, path="multipass")
     assert torch.equal(out, out2)
+    assert torch.equal(out, run(w, path="split"))
 
 
 # ---------------------------------------------------------------------------
@@ -266,12 +269,13 @@ def _sequence_problem(rng, kind, rows=12, L=20000, k=2048, page_size=64):
 
 @pytest.mark.parametrize("kind", ["falling", "rising", "ties", "neg_inf", "ramp", "lengths"])
 @pytest.mark.parametrize("ctas", [1, 2])
-def test_pipe_threshold_carried_between_rows(cuda_device, kind, ctas):
+@pytest.mark.parametrize("path", ["pipe", "split"])
+def test_pipe_threshold_carried_between_rows(cuda_device, kind, ctas, path):
     rng = np.random.default_rng(zlib.crc32(kind.encode()))
     p = _sequence_problem(rng, kind)
     w = host_problem_to_device(p, cuda_device)
     want = oracle_host(p)
-    got = run(w, path="pipe", max_ctas=ctas).cpu().numpy()
+    got = run(w, path=path, max_ctas=ctas).cpu().numpy()
     bad = np.nonzero((got != want).any(axis=1))[0]
     assert bad.size == 0, f"rows {bad.tolist()} differ"
 
@@ -310,11 +314,12 @@ def test_kth_largest_is_negative_infinity(cuda_device, launch):
 
 
 @pytest.mark.parametrize("name", ["long", "prefill"])
-def test_repeated_launches_are_identical(cuda_device, name):
+@pytest.mark.parametrize("path", ["auto", "split"])
+def test_repeated_launches_are_identical(cuda_device, name, path):
     """The ring's stages are refilled by TMA while other warps may still be
     finishing a row: any ordering mistake between the consumers' reads and the
     next copy shows up as launch-to-launch differences."""
     w = wl.named(name, device=cuda_device)
-    first = run(w)
+    first = run(w, path=path)
     for _ in range(3):
-        assert torch.equal(first, run(w)), "two launches on the same input disagree"
+        assert torch.equal(first, run(w, path=path)), "two launches on the same input disagree"
