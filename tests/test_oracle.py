@@ -7,8 +7,12 @@ The oracle (oracle/topk_oracle.c) is checked against things other than itself:
   * special cases that reduce to a library routine (k >= L: the identity
     selection; page_size 1 with an identity table: raw indices; numpy lexsort);
   * the invariants of oracle/invariants.py on larger rows;
+  * metamorphic relations that follow from the definition: exact power-of-two
+    scaling, values outside the windows, a permuted page table with the row
+    map following it, reversed windows;
   * planted mistakes: mutated copies of the oracle source must fail these pins.
 """
+import dataclasses
 import json
 import os
 
@@ -201,3 +205,79 @@ def test_oracle_thread_count_does_not_change_result():
     a = run_oracle(p, nthreads=1)
     b = run_oracle(p, nthreads=7)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# Metamorphic pins: transformations of the input whose effect on the result
+# follows from the definition alone.
+# ---------------------------------------------------------------------------
+def _windows_mask(p):
+    """True at every cell of `scores` that lies inside some row's window."""
+    inside = np.zeros(p.scores.shape[0], dtype=bool)
+    for i in range(p.num_rows):
+        L = max(int(p.seq_lens[i]), 0)
+        base = i * p.row_stride + int(p.row_starts[i])
+        inside[base: base + L] = True
+    return inside
+
+
+@pytest.mark.parametrize("values", ["normal", "ties", "bf16", "int"])
+def test_exact_power_of_two_scaling_keeps_the_result(values):
+    """Scaling every score by 2^e (exact in float32 for these magnitudes)
+    keeps every comparison, so the result is unchanged; -0.0 stays equal to
+    +0.0 and the infinities stay infinite."""
+    rng = np.random.default_rng(31)
+    p = random_problem(rng, rows=20, max_len=300, k=40, page_size=8, values=values)
+    base = run_oracle(p)
+    for e in (-3, 5):
+        q = dataclasses.replace(p, scores=(p.scores * np.float32(2.0 ** e)).astype(np.float32))
+        assert np.array_equal(run_oracle(q), base), e
+
+
+def test_values_outside_the_windows_do_not_matter():
+    rng = np.random.default_rng(33)
+    p = random_problem(rng, rows=24, max_len=500, k=64, page_size=16, values="ties")
+    base = run_oracle(p)
+    inside = _windows_mask(p)
+    for fill in (np.float32(np.inf), np.float32(-np.inf), np.float32(1e30)):
+        s = p.scores.copy()
+        s[~inside] = fill
+        assert np.array_equal(run_oracle(dataclasses.replace(p, scores=s)), base)
+    s = p.scores.copy()
+    s[~inside] = rng.standard_normal(int((~inside).sum())).astype(np.float32) * 100
+    assert np.array_equal(run_oracle(dataclasses.replace(p, scores=s)), base)
+
+
+def test_page_table_rows_follow_the_row_map():
+    """Permuting the page table's rows and the row map with it leaves every
+    output unchanged: a row reads its pages only through row_to_batch."""
+    rng = np.random.default_rng(35)
+    p = random_problem(rng, rows=30, max_len=400, k=50, page_size=16, values="normal", table_rows=6)
+    base = run_oracle(p)
+    n_table = p.page_table.size // p.pt_stride
+    perm = rng.permutation(n_table)
+    table = p.page_table.reshape(n_table, p.pt_stride)
+    moved = np.empty_like(table)
+    moved[perm] = table  # old row b now sits at perm[b]
+    rtb = perm[p.row_to_batch].astype(np.int32)
+    q = dataclasses.replace(p, page_table=moved.reshape(-1), row_to_batch=rtb)
+    assert np.array_equal(run_oracle(q), base)
+
+
+def test_reversed_windows_mirror_the_selection_up_to_ties():
+    """On tie-free rows, reversing each window maps index j to L-1-j, so the
+    selected set is mirrored (raw indices, no page table)."""
+    rng = np.random.default_rng(37)
+    p = random_problem(rng, rows=16, max_len=300, k=30, page_size=1, values="normal")
+    raw = topk_packed_reference(p.scores, p.row_stride, p.seq_lens, p.row_starts, None, None, 0, 1, 30)
+    s = p.scores.copy()
+    for i in range(p.num_rows):
+        L = max(int(p.seq_lens[i]), 0)
+        base = i * p.row_stride + int(p.row_starts[i])
+        s[base: base + L] = s[base: base + L][::-1]
+    rev = topk_packed_reference(s, p.row_stride, p.seq_lens, p.row_starts, None, None, 0, 1, 30)
+    for i in range(p.num_rows):
+        L = max(int(p.seq_lens[i]), 0)
+        m = min(L, 30)
+        want = sorted(L - 1 - int(j) for j in raw[i, :m])
+        assert rev[i, :m].tolist() == want and (rev[i, m:] == -1).all()
