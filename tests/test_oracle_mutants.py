@@ -37,6 +37,10 @@ MUTANTS = {
     "padding with zero": ("out_row[t] = -1;", "out_row[t] = 0;"),
     "one slot short": ("const int32_t m = n < p->k ? n : p->k;",
                        "const int32_t m = n < p->k ? n : p->k - 1;"),
+    "raw index off by one": ("for (int32_t t = 0; t < m; ++t) out_row[t] = chosen[t];",
+                             "for (int32_t t = 0; t < m; ++t) out_row[t] = chosen[t] + 1;"),
+    "raw rows left unpadded": ("if (p->page_table == NULL) {\n    for (int32_t t = 0; t < m; ++t) out_row[t] = chosen[t];\n  }",
+                               "if (p->page_table == NULL) {\n    for (int32_t t = 0; t < m; ++t) out_row[t] = chosen[t];\n    return;\n  }"),
 }
 
 
@@ -61,11 +65,11 @@ def _call(lib, scores, row_stride, seq_lens, row_starts, rtb, table, pt_stride, 
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     rs = np.ascontiguousarray(row_starts, dtype=np.int32)
     rb = None if rtb is None else np.ascontiguousarray(rtb, dtype=np.int32)
-    pt = np.ascontiguousarray(table, dtype=np.int32)
-    out = np.empty((sl.shape[0], k), dtype=np.int32)
+    pt = None if table is None else np.ascontiguousarray(table, dtype=np.int32)
+    out = np.full((sl.shape[0], k), 12345, dtype=np.int32)
     lib.topk_oracle(sc.ctypes.data, row_stride, sl.ctypes.data, rs.ctypes.data,
-                    None if rb is None else rb.ctypes.data, pt.ctypes.data, pt_stride,
-                    page_size, k, out.ctypes.data, sl.shape[0], 1)
+                    None if rb is None else rb.ctypes.data, None if pt is None else pt.ctypes.data,
+                    pt_stride, page_size, k, out.ctypes.data, sl.shape[0], 1)
     return out
 
 
@@ -88,6 +92,13 @@ def _passes_pins(lib) -> bool:
         want = brute_force.packed_result(p.scores, p.row_stride, p.seq_lens, p.row_starts,
                                          p.row_to_batch, p.page_table, p.pt_stride, p.page_size,
                                          p.k)
+        if got.tolist() != want:
+            return False
+        # and without a page table: raw window indices
+        got = _call(lib, p.scores, p.row_stride, p.seq_lens, p.row_starts, p.row_to_batch,
+                    None, 0, p.page_size, p.k)
+        want = brute_force.packed_result(p.scores, p.row_stride, p.seq_lens, p.row_starts,
+                                         p.row_to_batch, None, 0, p.page_size, p.k)
         if got.tolist() != want:
             return False
     return True
