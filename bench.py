@@ -350,7 +350,7 @@ def run_reference(a, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
-KERNEL_NAMES = {1: "topk_multipass_kernel", 2: "topk_stream_kernel", 3: "topk_pipe_kernel"}
+KERNEL_NAMES = {1: "topk_multipass_kernel", 2: "topk_stream_kernel", 3: "topk_pipe_kernel", 4: "topk_split_kernel"}
 METRIC = "packed top-k rows/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
 
 

@@ -103,7 +103,8 @@ TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, cons
 
 /* Kernel families behind topk_packed_ex. */
 typedef enum {
-  TOPK_PATH_AUTO = 0,      /* what topk_packed uses (currently TOPK_PATH_PIPE) */
+  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: TOPK_PATH_SPLIT for batches of at most one
+                              row per SM, else TOPK_PATH_PIPE */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
   TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
   TOPK_PATH_PIPE = 3,      /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over

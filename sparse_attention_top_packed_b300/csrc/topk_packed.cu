@@ -167,7 +167,11 @@ Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t num_rows,
   (void)row_stride;
   Plan pl;
   const int32_t want = cfg ? cfg->path : TOPK_PATH_AUTO;
-  pl.path = want == TOPK_PATH_AUTO ? TOPK_PATH_PIPE : want;
+  // a batch with no more rows than SMs (decode-like) gets one CTA per row
+  // from the split kernel, whose deeper rings stream a row faster; larger
+  // batches, two pipelined CTAs per SM
+  const bool few_rows = num_rows <= d.sms && d.split_ctas_per_sm > 0;
+  pl.path = want != TOPK_PATH_AUTO ? want : few_rows ? TOPK_PATH_SPLIT : TOPK_PATH_PIPE;
   pl.cluster = 1;
   if (pl.path == TOPK_PATH_PIPE) {
     const int64_t cap = (int64_t)d.sms * d.pipe_ctas_per_sm;

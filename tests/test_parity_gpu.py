@@ -170,7 +170,11 @@ def test_plan_reports_the_launch(cuda_device):
     assert plan["threads_per_cta"] == 256, "8 warps, each streaming its own block"
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert plan["grid_ctas"] == 2 * sms, "two pipelined CTAs per SM"
-    assert binding.topk_packed_plan(140000, 2048, 7)["grid_ctas"] == 7
+    small = binding.topk_packed_plan(140000, 2048, 7)
+    assert small["grid_ctas"] == 7 and small["path"] == binding.PATHS["split"], "decode-like batches"
+    assert small["threads_per_cta"] == 512
+    assert binding.topk_packed_plan(140000, 2048, sms)["path"] == binding.PATHS["split"]
+    assert binding.topk_packed_plan(140000, 2048, sms + 1)["path"] == binding.PATHS["pipe"]
     st = binding.topk_packed_plan(140000, 2048, 4096, path="stream")
     assert st["threads_per_cta"] == 1024
     assert st["grid_ctas"] % st["cluster_size"] == 0
