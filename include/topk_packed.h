@@ -48,13 +48,13 @@ typedef struct CUstream_st* topk_stream_t;
 typedef enum {
   TOPK_OK = 0,
   TOPK_ERR_INVALID_ARG = 1, /* an argument breaks the contract below; nothing launched */
-  TOPK_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles (or the chosen kernel
+  TOPK_ERR_UNSUPPORTED = 2, /* valid but outside what the library handles (or the chosen kernel
                                cannot be resident on this device); nothing launched */
   TOPK_ERR_LAUNCH = 3,      /* the CUDA launch failed (the CUDA error is kept; see below) */
   TOPK_ERR_DEVICE = 4       /* no usable sm_103a device, or a CUDA query failed */
 } topk_status_t;
 
-/* Largest k this build accepts. */
+/* Largest k the library accepts. */
 #define TOPK_K_MAX 2048
 
 /*

@@ -321,7 +321,7 @@ const char* topk_status_string(topk_status_t status) {
   switch (status) {
     case TOPK_OK: return "success";
     case TOPK_ERR_INVALID_ARG: return "invalid argument";
-    case TOPK_ERR_UNSUPPORTED: return "unsupported argument for this build";
+    case TOPK_ERR_UNSUPPORTED: return "unsupported argument for this library";
     case TOPK_ERR_LAUNCH: return "kernel launch failed";
     case TOPK_ERR_DEVICE: return "no usable sm_103a device";
   }
