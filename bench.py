@@ -157,9 +157,18 @@ def l2_flush_buffer(device):
     return torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
 
 
-def prepare_timing(w, steps: int, warmup: int, flush: bool, device):
-    """Arguments of the timed call, after `warmup` untimed calls, and the events."""
+def make_launch(path: str):
+    """The timed call: topk_packed (the automatic choice) or topk_packed_ex with
+    an explicit kernel family."""
     from sparse_attention_top_packed_b300 import binding
+
+    if path == "auto":
+        return lambda args, stream: binding.topk_packed(*args, stream=stream)
+    return lambda args, stream: binding.topk_packed_ex(*args, path=path, stream=stream)
+
+
+def prepare_timing(w, steps: int, warmup: int, flush: bool, device, launch):
+    """Arguments of the timed call, after `warmup` untimed calls, and the events."""
 
     out = torch.empty((w.num_rows, w.k), dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
@@ -169,7 +178,7 @@ def prepare_timing(w, steps: int, warmup: int, flush: bool, device):
     for _ in range(warmup):
         if flush:
             scratch.fill_(1.0)
-        binding.topk_packed(*args, stream=stream)
+        launch(args, stream)
     torch.cuda.synchronize(device)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -185,7 +194,8 @@ def run_ours(a, rank: int, world: int, device) -> dict:
     alg_bytes = w.algorithmic_bytes()
     big = w.window_bytes() > 4 * L2_BYTES
     flush = not big
-    args, stream, scratch, starts, ends = prepare_timing(w, a.steps, a.warmup, flush, device)
+    launch = make_launch(a.path)
+    args, stream, scratch, starts, ends = prepare_timing(w, a.steps, a.warmup, flush, device, launch)
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -203,7 +213,7 @@ def run_ours(a, rank: int, world: int, device) -> dict:
         if flush:
             scratch.fill_(1.0)
         starts[i].record(stream)
-        binding.topk_packed(*args, stream=stream)
+        launch(args, stream)
         ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(device)
@@ -377,6 +387,8 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="keep only the first N rows of the workload (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "pipe", "split", "stream", "multipass"],
+                    help="kernel family (auto: the choice topk_packed makes)")
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3
@@ -398,7 +410,7 @@ def main():
     w = r["workload"]
     if rank == 0:
         peaks = measured_peaks()
-        plan = binding.topk_packed_plan(w.row_stride, w.k, w.num_rows)
+        plan = binding.topk_packed_plan(w.row_stride, w.k, w.num_rows, path=a.path)
         achieved = r["alg_bytes"] / (r["kernel_ms"] / 1e3) / 1e9
         value = world * w.num_rows / (r["step_ms"] / 1e3)
         traffic = profiled_traffic(a.workload)

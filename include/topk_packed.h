@@ -103,23 +103,29 @@ TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, cons
 
 /* Kernel families behind topk_packed_ex. */
 typedef enum {
-  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: TOPK_PATH_SPLIT for batches of at most one
-                              row per SM, else TOPK_PATH_PIPE */
+  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: TOPK_PATH_SPLIT (TOPK_PATH_PIPE if the split
+                              kernel cannot be resident on the device) */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
   TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
   TOPK_PATH_PIPE = 3,      /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over
                               contiguous blocks of the row, candidates kept in window order with a
                               threshold carried from row to row, ordered emission by prefix counts */
-  TOPK_PATH_SPLIT = 4      /* persistent CTAs, one per SM: 8 streaming warps (4-stage TMA rings)
-                              hand each row's candidates, in one of two buffer sets, to 8 finishing
-                              warps that select and emit it while the next row streams */
+  TOPK_PATH_SPLIT = 4      /* persistent CTAs, one per SM, each on a contiguous range of rows
+                              balanced by cost: 8 streaming warps (8 KB TMA stages, 128 KB in flight
+                              per SM) hand each row's candidates, in one of two buffer sets, to 8
+                              finishing warps that select and emit it while the next row streams */
 } topk_path_t;
 
 /* Launch choices; zero fields mean "choose automatically". */
 typedef struct {
-  int32_t path;         /* topk_path_t */
-  int32_t cluster_size; /* STREAM: CTAs that share one row (1, 2, 4 or 8); 0 = auto */
-  int32_t max_ctas;     /* STREAM, PIPE, SPLIT, MULTIPASS: upper bound on the grid; 0 = auto */
+  int32_t path;            /* topk_path_t */
+  int32_t cluster_size;    /* STREAM: CTAs that share one row (1, 2, 4 or 8); 0 = auto */
+  int32_t max_ctas;        /* STREAM, PIPE, SPLIT, MULTIPASS: upper bound on the grid; 0 = auto */
+  uint32_t stream_wait_ns; /* PIPE, SPLIT: bound of each wait for a streamed chunk of the window, in
+                              ns; 0 = the default of about 2 s.  A wait that runs out sets bit 0 of
+                              the diagnostics word and leaves the affected rows unspecified; the
+                              kernel still waits, with the default bound, for every copy it issued
+                              before it exits.  Meant for testing that path. */
 } topk_launch_config_t;
 
 /*

@@ -35,6 +35,9 @@ constexpr int kShift3 = 0;
 constexpr uint32_t kFlagStreamWaitTimeout = 1u;
 constexpr uint32_t kFlagBadOutputPosition = 2u;
 
+// Default bound of a wait inside a kernel: ~2 s.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // The diagnostic word (the library is one translation unit).
 __device__ uint32_t g_device_flags;
 
@@ -50,7 +53,12 @@ struct Params {
   int32_t k;
   int32_t* out;
   int32_t num_rows;
+  uint32_t stream_wait_ns;  // bound of a wait for a streamed chunk (0: kWaitLimitNs)
 };
+
+__device__ __forceinline__ uint64_t stream_wait_limit(const Params& p) {
+  return p.stream_wait_ns ? (uint64_t)p.stream_wait_ns : kWaitLimitNs;
+}
 
 // ---------------------------------------------------------------------------
 // Keys.  key(x) orders like x for every non-NaN float; -0.0 is first turned
@@ -227,13 +235,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete, for at most ~2 s.
-// Returns false when it gave up (the caller records a diagnostic bit).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete, for at most
+// `limit_ns`.  Returns false when it gave up (the caller records a diagnostic
+// bit).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-    if (global_timer_ns() - t0 > 2000000000ull) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
     __nanosleep(64);
   }
   return true;

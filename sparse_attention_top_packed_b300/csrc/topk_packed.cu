@@ -167,11 +167,9 @@ Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t num_rows,
   (void)row_stride;
   Plan pl;
   const int32_t want = cfg ? cfg->path : TOPK_PATH_AUTO;
-  // a batch with no more rows than SMs (decode-like) gets one CTA per row
-  // from the split kernel, whose deeper rings stream a row faster; larger
-  // batches, two pipelined CTAs per SM
-  const bool few_rows = num_rows <= d.sms && d.split_ctas_per_sm > 0;
-  pl.path = want != TOPK_PATH_AUTO ? want : few_rows ? TOPK_PATH_SPLIT : TOPK_PATH_PIPE;
+  // the warp-specialised split kernel, whose stream never waits for the end
+  // of a row; the pipelined kernel when the split one cannot be resident
+  pl.path = want != TOPK_PATH_AUTO ? want : d.split_ctas_per_sm > 0 ? TOPK_PATH_SPLIT : TOPK_PATH_PIPE;
   pl.cluster = 1;
   if (pl.path == TOPK_PATH_PIPE) {
     const int64_t cap = (int64_t)d.sms * d.pipe_ctas_per_sm;
@@ -257,6 +255,7 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   prm.k = k;
   prm.out = out;
   prm.num_rows = num_rows;
+  prm.stream_wait_ns = config ? config->stream_wait_ns : 0u;
 
   const Plan pl = make_plan(*d, row_stride, num_rows, config);
   if (pl.grid <= 0) return TOPK_ERR_UNSUPPORTED;  // the split kernel cannot be resident here

@@ -53,6 +53,9 @@
 #pragma once
 
 #include "topk_device.cuh"
+#include "topk_sched.cuh"
+
+#include <type_traits>
 
 namespace topk {
 namespace pipe {
@@ -115,12 +118,16 @@ struct PickOut {
   uint32_t total;
 };
 
-// Per-warp TMA rings of NS stages (one mbarrier per stage).
-template <int NS>
+// Per-warp TMA rings of NS stages of CQ quads for NW warps (one mbarrier per stage).
+template <int NS, int NW = kWarps, int CQ = kWChunkQuads>
 struct Ring {
-  float4 st[kWarps][NS][kWChunkQuads];
-  uint64_t full[kWarps][NS];
+  static constexpr int kChunk = CQ;
+  float4 st[NW][NS][CQ];
+  uint64_t full[NW][NS];
 };
+
+// Most streaming warps a kernel has (each fills its own part of the buffer).
+constexpr int kMaxStreamWarps = 16;
 
 // Shared state of one row in flight: candidate buffer, histogram, rules and
 // the selection's scratch.
@@ -139,6 +146,7 @@ struct alignas(16) Shared {
   int32_t res_j[32];
   uint32_t res_w[32];    // and the warp whose region holds each
   uint32_t res_n;
+  uint32_t scnt[kMaxStreamWarps];  // with more streaming warps than regions: each one's entry count
   uint32_t wcin[kWarps];            // fast rows: entries of the k-th key's bin in each warp's region
   uint32_t wkmin[kWarps], wkmax[kWarps];  // ... and their key range (crowded bins)
   uint32_t pad0_;
@@ -613,10 +621,15 @@ __device__ __noinline__ void emit_selected(Shared& S, const Params& p, const Row
 // in warp order, cut at 128-byte units (8 quads) so that the blocks differ by
 // at most one unit.  Its chunks are kWChunkQuads quads from q0 on, the last one
 // partial.
-__device__ __forceinline__ void warp_block(int64_t nq, int w, int64_t& q0, int64_t& q1) {
+template <int NB>
+__device__ __forceinline__ void warp_block_of(int64_t nq, int w, int64_t& q0, int64_t& q1) {
   const int64_t nu = (nq + 7) >> 3;
-  q0 = min(((nu * w) / kWarps) * 8, nq);
-  q1 = min(((nu * (w + 1)) / kWarps) * 8, nq);
+  q0 = min(((nu * w) / NB) * 8, nq);
+  q1 = min(((nu * (w + 1)) / NB) * 8, nq);
+}
+
+__device__ __forceinline__ void warp_block(int64_t nq, int w, int64_t& q0, int64_t& q1) {
+  warp_block_of<kWarps>(nq, w, q0, q1);
 }
 
 // A row's descriptor as loaded; the Row is derived from it.
@@ -643,25 +656,26 @@ __device__ __forceinline__ Row make_row(const Params& p, int64_t row, const RowR
 }
 
 // A warp's cursor over its chunk sequence: the warp's block of each of the
-// CTA's rows (blockIdx.x, blockIdx.x + gridDim.x, ... with seq_len > k).
+// CTA's rows (its contiguous range [lo, hi), rows with seq_len > k).
 // Uniform across the warp.
 struct WCursor {
   const float4* src;
   int32_t left;  // quads of the current block not yet issued
-  int32_t row;   // row of the current block (num_rows: past the last)
+  int32_t row;   // row of the current block (hi: past the last)
   uint32_t issued;
+  int32_t lo, hi;        // the CTA's rows
+  const uint32_t* bits;  // which of them need a selection (sched::balanced_range)
 };
 
 // Whole warp: moves the cursor to the block of its next row with seq_len > k
-// (rows that need no selection are skipped 32 at a time).  `ahead` is the
-// descriptor of row `ahead_row`, loaded ahead by the caller: used when it is
-// the row needed, which spares a wait for global memory.  False past the last.
+// (found in the CTA's bitmask).  `ahead` is the descriptor of row `ahead_row`,
+// loaded ahead by the caller: used when it is the row needed, which spares a
+// wait for global memory.  False past the last.
 __device__ __forceinline__ bool cursor_next_row(WCursor& cur, const Params& p, int w, int64_t ahead_row,
                                                 const RowRaw& ahead) {
-  const int lane = threadIdx.x & 31;
-  int64_t row = (int64_t)cur.row + gridDim.x;
-  if (row >= p.num_rows) {
-    cur.row = p.num_rows;
+  const int64_t row = sched::next_selected_row(p, cur.bits, cur.lo, cur.hi, (int64_t)cur.row + 1);
+  if (row >= cur.hi) {
+    cur.row = cur.hi;
     return false;
   }
   int32_t L, st;
@@ -671,26 +685,6 @@ __device__ __forceinline__ bool cursor_next_row(WCursor& cur, const Params& p, i
   } else {
     L = __ldg(p.seq_lens + row);
     st = __ldg(p.row_starts + row);
-  }
-  if (L <= p.k) {
-    const int64_t r_first = row + gridDim.x;
-    row = p.num_rows;
-    for (int64_t r0 = r_first; r0 < p.num_rows; r0 += 32 * (int64_t)gridDim.x) {
-      const int64_t rr = r0 + (int64_t)lane * gridDim.x;
-      const int32_t l = rr < p.num_rows ? __ldg(p.seq_lens + rr) : 0;
-      const uint32_t b = __ballot_sync(0xFFFFFFFFu, l > p.k);
-      if (b != 0u) {
-        const int src = __ffs(b) - 1;
-        row = r0 + (int64_t)src * gridDim.x;
-        L = __shfl_sync(0xFFFFFFFFu, l, src);
-        st = __ldg(p.row_starts + row);
-        break;
-      }
-    }
-    if (row >= p.num_rows) {
-      cur.row = p.num_rows;
-      return false;
-    }
   }
   cur.row = (int32_t)row;
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + st);
@@ -773,67 +767,106 @@ __device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
 // Fast pass: the warp's block of the row through its ring, fixed threshold.
 // ---------------------------------------------------------------------------
 
-// Warp w (of the kWarps streaming warps) takes its block of the row from its
-// ring (NS stages) into its region of S.
-template <int NS>
-__device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS>& R, int w, const Params& p, const Row& r, int64_t nq,
-                                              uint32_t& g, WCursor& cur, uint64_t policy, bool& timed_out,
-                                              Deferred& dfr, int64_t ahead_row, const RowRaw& ahead) {
+// Warp w (of the NW streaming warps) takes its block of the row from its
+// ring (NS stages) into its region of S (kCap / NW entries).  With NW ==
+// kWarps the regions are the selection's; with more streaming warps their
+// counts go to S.scnt and the finishing side merges regions.
+//
+// The stream loop is kept short: each lane compares its 32 consecutive floats
+// with the threshold, the lanes' output positions come from one reduction and
+// six ballots (the bits of the lanes' counts), and an admitted element is
+// stored as its raw float bits with its window index.  Keys and the fine
+// histogram are made afterwards, once per admitted element
+// (keys_and_histogram).
+//
+// A chunk is taken only once its copy has landed.  If a wait gives up
+// (`limit_ns`), the warp records it in timed_out and leaves the row: the
+// chunk stays outstanding and its stage is not refilled, so no stage ever
+// holds two copies in flight; the kernel's exit waits for what is left.
+template <int NS, int NW, int CQ, class AfterChunk>
+__device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, int w, const Row& r, int64_t nq,
+                                              uint32_t& g, bool& timed_out, uint64_t limit_ns,
+                                              AfterChunk&& after_chunk) {
+  static_assert(NW == kWarps || NW <= kMaxStreamWarps, "streaming warps");
+  constexpr int QPL = CQ / 32;  // quads per lane: 8 (4 KB chunks) or 16 (8 KB chunks)
+  static_assert(QPL == 8 || QPL == 16, "chunk size");
+  using Mask = typename std::conditional<QPL == 8, uint32_t, uint64_t>::type;
+  constexpr int kBits = 4 * QPL;   // elements per lane per chunk
+  constexpr int kReg = kCap / NW;  // this warp's region
   const int lane = threadIdx.x & 31;
   int64_t q0, q1;
-  warp_block(nq, w, q0, q1);
+  warp_block_of<NW>(nq, w, q0, q1);
   const float tf = S.rule.tf;
-  const uint32_t tk = S.fh_tk, sh = S.fh_sh;
   const int rot = lane & 7;  // rotated quad order: the 8 lanes of a load phase hit 8 distinct bank groups
-  uint32_t* rkey = S.bkey + w * kRegion;
-  int32_t* rj = S.bj + w * kRegion;
-  uint32_t wcnt = 0, top = 0u;
+  const uint32_t lt = lanemask_lt();
+  uint32_t* rraw = S.bkey + w * kReg;  // raw float bits here; keys after keys_and_histogram
+  int32_t* rj = S.bj + w * kReg;
+  uint32_t wcnt = 0;
   bool full = false;
   uint32_t s = g % NS, ph = (g / NS) & 1u;
-  for (int64_t cq = q0; cq < q1; cq += kWChunkQuads, ++g) {
-    if (!mbar_try_wait(&R.full[w][s], ph) && !timed_out && !mbar_wait_bounded(&R.full[w][s], ph))
-      timed_out = true;
-    const float4* st = R.st[w][s];
-    // the lane's 32 consecutive floats; bit 4u+c of mr is element 4*((u+rot)&7)+c
-    uint32_t mr = 0u;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4 v = st[8 * lane + ((u + rot) & 7)];
-      const uint32_t q = (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
-      mr |= q << (4 * u);
+  for (int64_t cq = q0; cq < q1; cq += CQ, ++g) {
+    if (!mbar_try_wait(&R.full[w][s], ph)) {
+      if (timed_out || !mbar_wait_bounded(&R.full[w][s], ph, limit_ns)) {
+        timed_out = true;
+        break;
+      }
     }
-    uint32_t m = __funnelshift_l(mr, mr, 4 * rot);  // bit e: element e of the lane's 32
-    const int64_t jb = (cq + 8 * lane) * 4 - r.head;  // window index of element 0
-    if (cq == 0 || cq + kWChunkQuads >= q1) {  // the row's first or the block's last chunk
+    const float4* st = R.st[w][s];
+    // the lane's kBits consecutive floats; bit 4u+c of mr is element 4*((u+rot)%QPL)+c
+    Mask mr = 0u;
+#pragma unroll
+    for (int u = 0; u < QPL; ++u) {
+      const float4 v = st[QPL * lane + ((u + rot) & (QPL - 1))];
+      if (v.x >= tf) mr |= (Mask)1u << (4 * u);
+      if (v.y >= tf) mr |= (Mask)2u << (4 * u);
+      if (v.z >= tf) mr |= (Mask)4u << (4 * u);
+      if (v.w >= tf) mr |= (Mask)8u << (4 * u);
+    }
+    // bit e: element e of the lane's kBits (rotate left by 4 rot)
+    Mask m = rot == 0 ? mr : (Mask)((mr << (4 * rot)) | (mr >> (kBits - 4 * rot)));
+    // window index of the lane's element 0 (window indices fit in 32 bits;
+    // lanes before the window start get negative ones, masked below)
+    const int32_t jb = (int32_t)((cq + QPL * lane) * 4 - r.head);
+    if (cq == 0 || cq + CQ >= q1) {  // the row's first or the block's last chunk
       // keep the window [0, L) and the block's quads [.., q1) (the rest of a
       // partial chunk's stage is stale)
-      const int64_t lo = max(-jb, (int64_t)0);
-      const int64_t hi = min(min((int64_t)r.L - jb, (q1 - cq - 8 * lane) * 4), (int64_t)32);
-      m = lo >= hi ? 0u : (((hi >= 32) ? 0xFFFFFFFFu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u));
-      m &= __funnelshift_l(mr, mr, 4 * rot);
+      const int64_t lo = max(-(int64_t)jb, (int64_t)0);
+      const int64_t hi = min(min((int64_t)r.L - jb, (q1 - cq - QPL * lane) * 4), (int64_t)kBits);
+      const Mask below_hi = hi >= kBits ? ~(Mask)0 : (((Mask)1 << (hi > 0 ? hi : 0)) - 1u);
+      const Mask from_lo = lo >= kBits ? (Mask)0 : ~(((Mask)1 << lo) - 1u);
+      m &= lo >= hi ? (Mask)0 : (below_hi & from_lo);
     }
     if (!full) {
-      const uint32_t n = __popc(m);
-      const uint32_t incl = warp_incl_scan(n);
-      const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      const uint32_t n = (uint32_t)(QPL == 8 ? __popc((uint32_t)m) : __popcll((unsigned long long)m));
+      const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, n);
       if (tot != 0u) {
-        if (wcnt + tot > (uint32_t)kRegion) {
+        if (wcnt + tot > (uint32_t)kReg) {
           full = true;
           if (lane == 0) S.overflow = 1u;
         } else {
-          uint32_t pos = wcnt + incl - n;
-          const float* sf = reinterpret_cast<const float*>(st) + 32 * lane;
-          for (uint32_t mm = m; mm; mm &= mm - 1u) {  // ascending e: window order within the lane
-            const int e = __ffs(mm) - 1;
-            const uint32_t key = key_of(sf[e]);
-            rkey[pos] = key;
-            rj[pos] = (int32_t)(jb + e);
-            ++pos;
-            const uint32_t fb = (key - tk) >> sh;
-            if (fb < (uint32_t)kFineTop)
-              atomicAdd(&S.hist2[fb], 1u);
-            else
-              ++top;
+          // exclusive prefix of n over the lanes, from the bits of n
+          uint32_t pos = wcnt;
+#pragma unroll
+          for (int b = 0; b < (QPL == 8 ? 6 : 7); ++b)
+            pos += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (n >> b) & 1u) & lt) << b;
+          const uint32_t* sf = reinterpret_cast<const uint32_t*>(st) + kBits * lane;
+          // ascending e: window order within the lane; two at a time, so the
+          // two loads are in flight together
+          Mask mm = m;
+          while (mm) {
+            const int e0 = (int)(QPL == 8 ? __ffs((uint32_t)mm) : __ffsll((unsigned long long)mm)) - 1;
+            mm &= mm - 1u;
+            const int e1 = (int)(QPL == 8 ? __ffs((uint32_t)mm) : __ffsll((unsigned long long)mm)) - 1;
+            const uint32_t x0 = sf[e0];
+            const uint32_t x1 = e1 >= 0 ? sf[e1] : 0u;
+            rraw[pos] = x0;
+            rj[pos] = jb + e0;
+            if (e1 >= 0) {
+              rraw[pos + 1] = x1;
+              rj[pos + 1] = jb + e1;
+              mm &= mm - 1u;
+            }
+            pos += e1 >= 0 ? 2u : 1u;
           }
           wcnt += tot;
         }
@@ -842,19 +875,44 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS>& R, int w, con
     // the warp is done with the stage: order its reads before the next copy, refill
     fence_proxy_async_smem();
     __syncwarp();
-    warp_issue(R, cur, p, w, policy, ahead_row, ahead);
-    deferred_step(dfr, p.page_bits);
+    after_chunk();
     if (++s == (uint32_t)NS) {
       s = 0u;
       ph ^= 1u;
     }
   }
-  top = __reduce_add_sync(0xFFFFFFFFu, top);
   if (lane == 0) {
-    S.rbase[w] = (uint32_t)(w * kRegion);
-    S.rcnt[w] = wcnt;
-    S.wtop[w] = top;
+    if constexpr (NW == kWarps) {
+      S.rbase[w] = (uint32_t)(w * kRegion);
+      S.rcnt[w] = wcnt;
+    } else {
+      S.scnt[w] = wcnt;
+    }
   }
+}
+
+// Warp w, after the stream of a fast row (its region's count published):
+// turns the region's raw float bits into keys in place and counts them in the
+// fine histogram (hist2, zero beforehand; bins of 2^fh_sh keys from fh_tk),
+// keys above its range in S.wtop[w].  Touches only region w and hist2 (by
+// atomics); a consumer barrier must follow before the selection.
+__device__ __forceinline__ void keys_and_histogram(Shared& S) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  __syncwarp();  // the region's count was written by one lane of this warp
+  const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
+  const uint32_t tk = S.fh_tk, sh = S.fh_sh;
+  uint32_t top = 0;
+  for (uint32_t i = lane; i < cnt; i += 32) {
+    const uint32_t key = key_of(__uint_as_float(S.bkey[base + i]));
+    S.bkey[base + i] = key;
+    const uint32_t fb = (key - tk) >> sh;
+    if (fb < (uint32_t)kFineTop)
+      atomicAdd(&S.hist2[fb], 1u);
+    else
+      ++top;
+  }
+  top = __reduce_add_sync(0xFFFFFFFFu, top);
+  if (lane == 0) S.wtop[w] = top;
 }
 
 // Fine shift for a row whose threshold key sits about `d` keys below its k-th
@@ -1291,7 +1349,12 @@ __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const 
 struct PipeSmem {
   Ring<kWStages> ring;
   Shared s;
+  sched::RangeSmem range;
 };
+
+// Cost floor of a row in the balanced split (elements): the end of a row
+// stalls the CTA's stream for about as long as streaming this many elements.
+constexpr uint32_t kPipeCostFloor = 24576;
 
 __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -1311,23 +1374,29 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     S.hint_sh = 0u;
   }
   __syncthreads();
+  int64_t lo, hi;
+  sched::balanced_range<kThreads>(p, blockIdx.x, gridDim.x, kPipeCostFloor, M.range, lo, hi);
   // each warp starts its ring
-  RowRaw nx = load_row_raw(p, blockIdx.x);  // the grid never exceeds num_rows
+  RowRaw nx = {0, 0, 0};
+  if (lo < hi) nx = load_row_raw(p, lo);
   WCursor cur;
   cur.src = nullptr;
   cur.left = 0;
-  cur.row = (int32_t)blockIdx.x - (int32_t)gridDim.x;
+  cur.row = (int32_t)lo - 1;
   cur.issued = 0;
-  for (int s = 0; s < kWStages; ++s) warp_issue(R, cur, p, w, policy, blockIdx.x, nx);
+  cur.lo = (int32_t)lo;
+  cur.hi = (int32_t)hi;
+  cur.bits = M.range.bits;
+  for (int s = 0; s < kWStages; ++s) warp_issue(R, cur, p, w, policy, lo, nx);
 
   uint32_t g = 0;  // chunks this warp took from its ring
   Deferred dfr;
   dfr.o = nullptr;
 
-  for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
+  for (int64_t row = lo; row < hi; ++row) {
     const Row r = make_row(p, row, nx);
-    const bool has_next = row + gridDim.x < p.num_rows;
-    if (has_next) nx = load_row_raw(p, row + gridDim.x);  // used by the next iteration
+    const bool has_next = row + 1 < hi;
+    if (has_next) nx = load_row_raw(p, row + 1);  // used by the next iteration
     if (r.L <= p.k) {
       emit_whole_window<kThreads>(p, (int32_t)row, r, 0u, 1u);
       continue;
@@ -1356,22 +1425,24 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     for (int b = tid; b < kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
     cbar();  // also: every thread is done with the previous row's shared state
     if (S.sample != 0u) sample_threshold(S, p, r, nq);
-    stream_row_wb(S, R, w, p, r, nq, g, cur, policy, timed_out, dfr, row + gridDim.x, nx);
+    stream_row_wb(S, R, w, r, nq, g, timed_out, stream_wait_limit(p), [&] {
+      warp_issue(R, cur, p, w, policy, row + 1, nx);
+      deferred_step(dfr, p.page_bits);
+    });
     deferred_flush(dfr, p.page_bits);  // the previous fast row's transform, if unfinished
-    if (tid == 0) {
+    keys_and_histogram(S);  // this warp's region, written by this warp
+    if (w == 0) {
       // the CTA's next row that needs a selection, for the hint
       int32_t nl = has_next && nx.L > p.k ? nx.L : 0;
-      if (nl == 0)
-        for (int64_t rr = row + 2 * (int64_t)gridDim.x; rr < p.num_rows; rr += gridDim.x) {
-          const int32_t l = __ldg(p.seq_lens + rr);
-          if (l > p.k) {
-            nl = l;
-            break;
-          }
-        }
-      S.next_len = nl;
-      // rank of about 1.25 k in a row of the next row's length
-      S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
+      if (nl == 0) {
+        const int64_t rr = sched::next_selected_row(p, M.range.bits, lo, hi, row + 2);
+        if (rr < hi) nl = __ldg(p.seq_lens + rr);
+      }
+      if (lane == 0) {
+        S.next_len = nl;
+        // rank of about 1.25 k in a row of the next row's length
+        S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
+      }
     }
     cbar();
     uint32_t n = 0;

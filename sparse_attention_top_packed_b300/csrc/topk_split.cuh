@@ -9,41 +9,113 @@
 // groups of warps of one CTA per SM, so that the stream never waits for the
 // end of a row:
 //
-//  * Streaming warps (warps 8-15) only stream: each takes its block of a row
-//    through its own ring of 4 stages of 4 KB (128 KB in flight per SM) into
-//    one of two row states ("sets"), then hands the set over and goes on with
-//    the CTA's next row in the other set.
-//  * Finishing warps (warps 0-7) take a full set, select and emit its row --
+//  * Streaming warps (warps 8 on) only stream: each takes its block of a row
+//    through its own ring of 4 KB stages (128 KB in flight per SM) into its
+//    part of one of two row states ("sets"), then hands the set over and goes
+//    on with the next row in the other set.  Their loop only compares and
+//    appends raw candidates (topk_pipe.cuh, stream_row_wb).  Their rings run
+//    ahead on their own: each warp's cursor finds the next row in the CTA's
+//    bitmask and has its descriptor loaded a row ahead, so a row change costs
+//    no round trip.
+//  * Finishing warps (warps 0-7) take a full set, turn its candidates into
+//    keys and the fine histogram (joining the streaming warps' parts pairwise
+//    into the eight regions of the selection when there are sixteen of them),
+//    select and emit its row --
 //    the window indices staged in shared memory, then mapped through the page
-//    table with independent loads and written out -- and prepare the set for
-//    the row two streamed rows later: its admission rule comes from this row
-//    (the key that about 1.25 k candidates reach, scaled to the new length), or
-//    from a sample of that row taken right here, or the whole row when small.
-//    They also emit the rows whose window is not longer than k.
+//    table -- and prepare the set for the row two streamed rows later: its
+//    descriptor (read by the streaming warps), its admission rule (the key
+//    that about 1.25 k candidates of this row reach, scaled to the new length,
+//    or a sample of the new row, or the whole row when small), and a bulk copy
+//    of its page-table row into shared memory, so that the page transform
+//    reads no global memory.  Descriptors are loaded a row ahead.  While a set
+//    is still streaming they emit the rows whose window is not longer than k.
 //
-// Two mbarriers per set carry the hand-over (streamed / prepared).  Every wait
-// is bounded; one that gives up raises bit 0 of the diagnostics word.
+// Each CTA takes a contiguous range of rows balanced by cost (topk_sched.cuh).
+// With sixteen streaming warps the CTA is launched with 80 registers a thread;
+// the streaming warpgroups then give theirs down to 56 and the finishing ones
+// take 128 (setmaxnreg).
+// Three mbarriers per set carry the hand-overs (streamed / prepared / page row
+// staged).  Every wait is bounded; one that gives up raises bit 0 of the
+// diagnostics word.
 #pragma once
 
 #include "topk_pipe.cuh"
+#include "topk_sched.cuh"
 
 namespace topk {
 namespace split {
 
 using namespace topk::pipe;
 
-constexpr int kStages = 4;                   // the streaming warps' ring depth
-constexpr int kBlockThreads = 2 * kThreads;  // 8 finishing warps, then 8 streaming warps
+constexpr int kSW = 8;                       // streaming warps (8 or 16)
+constexpr int kSChunk = 512;                 // quads per stage: 8 KB, 64 floats a lane
+constexpr int kStages = 16 / kSW;            // their ring depth: 128 KB in flight
+constexpr int kBlockThreads = kThreads + kSW * 32;  // 8 finishing warps, then the streaming warps
+constexpr int kPart = kCap / kSW;            // buffer entries of one streaming warp
+// Register split (setmaxnreg, per warpgroup of 128 threads): launched with
+// kLaunchRegs each; the streaming warpgroups drop to kStreamRegs, the
+// finishing ones rise to kFinishRegs.  The sum must not exceed the launch's.
+constexpr int kLaunchRegs = 80;
+constexpr int kStreamRegs = 56;
+constexpr int kFinishRegs = 128;
+constexpr bool kRegSplit = kSW > kWarps;
+static_assert(!kRegSplit || kSW * 32 * kStreamRegs + kThreads * kFinishRegs <= kBlockThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+static_assert(!kRegSplit || kLaunchRegs * kBlockThreads <= 65536, "launch allocation exceeds the register file");
+static_assert(kSW == kWarps || 2 * kPart == kRegion, "two streaming parts make one selection region");
+constexpr int kPageStage = 1536;             // page-table entries a set can stage (6 KB)
+// Cost floor of a row in the balanced split (elements): the finishing warps
+// need about as long per row as the stream takes for this many elements.
+constexpr uint32_t kSplitCostFloor = 32768;
 
-struct SplitSmem {
-  pipe::Ring<kStages> ring;
-  pipe::Shared set[2];
-  uint64_t set_full[2];  // streaming -> finishing warps: the set holds its streamed row
-  uint64_t set_free[2];  // finishing -> streaming warps: the set is ready for its next row
+// The row a set is prepared for, as the streaming warps read it.
+struct SetRow {
+  int64_t row;  // >= the range's end: no more rows
+  int32_t L, start, trow, pad_;
 };
 
-// Barrier among the 8 streaming warps (the finishing warps use barrier 1).
-__device__ __forceinline__ void sbar() { asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory"); }
+// What a set's page stage holds.
+struct PageStage {
+  int32_t trow;    // table row staged (-1: none)
+  int32_t off;     // position of page_row[0] in the stage
+  int32_t count;   // entries staged from page_row[0] on
+  int32_t staged;  // the row the set is prepared for reads its pages from the stage
+};
+
+struct SplitSmem {
+  pipe::Ring<kStages, kSW, kSChunk> ring;
+  pipe::Shared set[2];
+  int32_t pages[2][kPageStage];
+  SetRow srow[2];
+  PageStage pstage[2];
+  uint64_t set_full[2];   // streaming -> finishing warps: the set holds its streamed row
+  uint64_t set_free[2];   // finishing -> streaming warps: the set is ready for its next row
+  uint64_t page_full[2];  // the set's page stage is written (one phase per prepared row)
+  sched::RangeSmem range;
+};
+
+// Barrier among the streaming warps (the finishing warps use barrier 1).
+__device__ __forceinline__ void sbar() { asm volatile("bar.sync 2, %0;" ::"n"(kSW * 32) : "memory"); }
+
+__device__ __forceinline__ bool sbar_or(bool v) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\t"
+               "setp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.or.pred q, 2, %2, p;\n\t"
+               "selp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(r) : "r"(v ? 1u : 0u), "n"(kSW * 32) : "memory");
+  return r != 0u;
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, bool& timed_out) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -52,27 +124,101 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, boo
   return !timed_out;
 }
 
-// All finishing threads (uniform): the CTA's first row at or after `from`,
-// stepping by the grid, whose window is longer than k; num_rows when none.
-__device__ __forceinline__ int64_t next_streamed(const Params& p, int64_t from) {
-  const int lane = threadIdx.x & 31;
-  for (int64_t r0 = from; r0 < p.num_rows; r0 += 32 * (int64_t)gridDim.x) {
-    const int64_t rr = r0 + (int64_t)lane * gridDim.x;
-    const int32_t l = rr < p.num_rows ? __ldg(p.seq_lens + rr) : 0;
-    const uint32_t b = __ballot_sync(0xFFFFFFFFu, l > p.k);
-    if (b != 0u) return r0 + (int64_t)(__ffs(b) - 1) * gridDim.x;
-  }
-  return p.num_rows;
+// 1-D bulk copy global -> shared with the default L2 policy (the page-table
+// rows are read by many rows).
+__device__ __forceinline__ void bulk_copy_g2s_keep(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Streaming warps' cursor over their chunk sequence: the warp's block of each
+// row of the CTA's range that needs a selection.  Uniform across the warp.
+// ---------------------------------------------------------------------------
+struct SCursor {
+  const float4* src;
+  int32_t left;       // quads of the current block not yet issued
+  uint32_t issued;    // chunks issued
+  int64_t nrow;       // the row whose block comes next (>= hi: none)
+  int32_t nL, nstart; // its descriptor, loaded ahead
+  int64_t lo, hi;
+  const uint32_t* bits;
+};
+
+__device__ __forceinline__ void scursor_init(SCursor& c, const Params& p, int64_t lo, int64_t hi,
+                                             const uint32_t* bits) {
+  c.src = nullptr;
+  c.left = 0;
+  c.issued = 0;
+  c.lo = lo;
+  c.hi = hi;
+  c.bits = bits;
+  c.nrow = sched::next_selected_row(p, bits, lo, hi, lo);
+  c.nL = 0;
+  c.nstart = 0;
+  if (c.nrow < hi) {
+    c.nL = __ldg(p.seq_lens + c.nrow);
+    c.nstart = __ldg(p.row_starts + c.nrow);
+  }
+}
+
+// Moves to the block of row c.nrow and loads the descriptor of the row after
+// it (used at the next move).  False past the last row.
+__device__ __forceinline__ bool scursor_advance(SCursor& c, const Params& p, int w) {
+  if (c.nrow >= c.hi) return false;
+  const int64_t row = c.nrow;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + c.nstart);
+  const int32_t head = (int32_t)((a & 15u) >> 2);
+  int64_t q0, q1;
+  warp_block_of<kSW>(((int64_t)c.nL + head + 3) >> 2, w, q0, q1);
+  c.src = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u) + q0;
+  c.left = (int32_t)(q1 - q0);
+  c.nrow = sched::next_selected_row(p, c.bits, c.lo, c.hi, row + 1);
+  if (c.nrow < c.hi) {
+    c.nL = __ldg(p.seq_lens + c.nrow);
+    c.nstart = __ldg(p.row_starts + c.nrow);
+  }
+  return true;
+}
+
+// Whole warp: lane 0 issues the warp's next chunk into stage issued % kStages
+// (whose previous chunk the warp has taken and fenced).  False past the last row.
+__device__ __forceinline__ bool scursor_issue(pipe::Ring<kStages, kSW, kSChunk>& R, SCursor& c, const Params& p, int w,
+                                              uint64_t policy) {
+  while (c.left == 0)
+    if (!scursor_advance(c, p, w)) return false;
+  const uint32_t s = c.issued % kStages;
+  const uint32_t nquads = (uint32_t)min(kSChunk, c.left);
+  if ((threadIdx.x & 31) == 0) {
+    mbar_arrive_expect_tx(&R.full[w][s], nquads * 16u);
+    bulk_copy_g2s(&R.st[w][s][0], c.src, nquads * 16u, &R.full[w][s], policy);
+  }
+  c.src += nquads;
+  c.left -= nquads;
+  ++c.issued;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Finishing warps.
+// ---------------------------------------------------------------------------
+
 // Finishing threads, entered after a finishing barrier that follows every use
-// of S by its previous row: S's admission rule for row R -- the hint S holds,
-// the whole row, or a sample of it -- with the histogram cleared.  Ends with a
-// finishing barrier.
-__device__ __forceinline__ void prepare_set(pipe::Shared& S, const Params& p, int64_t R) {
-  const Row r = load_row(p, (int32_t)R);
+// of set b by its previous row: prepares set b for row R (descriptor d), or
+// marks it as the end when R >= hi.  Thread 0 then arrives on set_free[b]
+// (done by the caller).  Ends with a finishing barrier.
+__device__ __forceinline__ void prepare_set(SplitSmem& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
+                                            int64_t hi) {
+  pipe::Shared& S = M.set[b];
+  if (R >= hi) {
+    if (threadIdx.x == 0) M.srow[b].row = hi;
+    pipe::cbar();
+    return;
+  }
+  const Row r = make_row(p, R, d);
   const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
-  const bool small = nq * 4 <= kRegion;  // every element fits its warp's region
+  const bool small = nq * 4 <= kPart;  // every element fits its streaming warp's part
   if (threadIdx.x == 0) {
     const bool hinted = !small && S.hint_valid != 0u;  // thread 0's own write
     S.sample = (!small && !hinted) ? 1u : 0u;
@@ -87,24 +233,100 @@ __device__ __forceinline__ void prepare_set(pipe::Shared& S, const Params& p, in
       S.fh_tk = S.hint.tk;
       S.fh_sh = S.hint_sh;
     }
+    SetRow sr;
+    sr.row = R;
+    sr.L = d.L;
+    sr.start = d.start;
+    sr.trow = d.table_row;
+    sr.pad_ = 0;
+    M.srow[b] = sr;
+    // the page-table row, into the set's page stage (from its 16-byte aligned
+    // start; it is reused when the previous row of this set had the same one)
+    PageStage& ps = M.pstage[b];
+    bool staged = false, copy = false;
+    uint32_t bytes = 0;
+    uintptr_t a = 0;
+    if (r.page_row != nullptr) {
+      const int64_t npages = ((int64_t)r.L + (1 << p.page_bits) - 1) >> p.page_bits;
+      a = reinterpret_cast<uintptr_t>(r.page_row);
+      const int32_t off = (int32_t)((a & 15u) >> 2);
+      const int64_t span = (((int64_t)off + npages) * 4 + 15) & ~(int64_t)15;
+      if (span <= (int64_t)kPageStage * 4) {
+        staged = true;
+        if (!(ps.trow == d.table_row && ps.off == off && (int64_t)ps.count >= npages)) {
+          copy = true;
+          bytes = (uint32_t)span;
+          ps.trow = d.table_row;
+          ps.off = off;
+          ps.count = (int32_t)(span / 4) - off;
+        }
+      }
+    }
+    ps.staged = staged ? 1 : 0;
+    if (copy) {
+      fence_proxy_async_smem();  // earlier reads of the stage come before the copy's writes
+      mbar_arrive_expect_tx(&M.page_full[b], bytes);
+      bulk_copy_g2s_keep(M.pages[b], reinterpret_cast<const void*>(a & ~(uintptr_t)15u), bytes, &M.page_full[b]);
+    } else {
+      mbar_arrive(&M.page_full[b]);
+    }
   }
-  for (int b = threadIdx.x; b < pipe::kBins2 / 4; b += kThreads)
-    reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < pipe::kBins2 / 4; i += kThreads)
+    reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0u, 0u, 0u, 0u);
   pipe::cbar();
   if (S.sample != 0u) pipe::sample_threshold(S, p, r, nq);  // ends with a barrier, hist2 zero
 }
 
-// Finishing threads, entered after S's streamed row R has been handed over:
-// selects and writes row R.  R2 is the row S serves next (num_rows: none),
-// the target of the hint.  Ends with a finishing barrier.
-__device__ __forceinline__ void finish_row(pipe::Shared& S, const Params& p, int64_t R, int64_t R2) {
+// Finishing warp w (whole warp): streaming warps 2w and 2w + 1 filled parts
+// 2w and 2w + 1 of the buffer (kPart entries each, in window order, part 2w
+// first); moves part 2w + 1's entries down to follow part 2w's, which makes
+// them region w of the selection, and publishes its count.  The moved range
+// only ever goes down, batch by batch, so a batch is read whole before any of
+// it is overwritten.
+__device__ __forceinline__ void merge_parts(pipe::Shared& S) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t c0 = S.scnt[2 * w], c1 = S.scnt[2 * w + 1];
+  uint32_t* key = S.bkey + w * kRegion;
+  int32_t* jj = S.bj + w * kRegion;
+  if (c0 < (uint32_t)kPart) {
+    for (uint32_t i0 = 0; i0 < c1; i0 += 32) {
+      const uint32_t i = i0 + (uint32_t)lane;
+      uint32_t kv = 0u;
+      int32_t jv = 0;
+      if (i < c1) {
+        kv = key[kPart + i];
+        jv = jj[kPart + i];
+      }
+      __syncwarp();
+      if (i < c1) {
+        key[c0 + i] = kv;
+        jj[c0 + i] = jv;
+      }
+      __syncwarp();
+    }
+  }
+  if (lane == 0) {
+    S.rbase[w] = (uint32_t)(w * kRegion);
+    S.rcnt[w] = c0 + c1;
+  }
+}
+
+// Finishing threads, entered after set b's streamed row R (descriptor d) has
+// been handed over: selects and writes row R.  next_len is the window length
+// of the row set b serves next (0: none), the target of the hint; `parity`
+// the phase of page_full[b] that stages R's pages.  Ends with a finishing
+// barrier.
+__device__ __forceinline__ void finish_row(SplitSmem& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
+                                           int32_t next_len, uint32_t parity, bool& timed_out) {
+  pipe::Shared& S = M.set[b];
   const int tid = threadIdx.x;
   const uint32_t k = (uint32_t)p.k;
-  const Row r = load_row(p, (int32_t)R);
+  const Row r = make_row(p, R, d);
   const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
+  if constexpr (kSW > kWarps) merge_parts(S);
+  pipe::keys_and_histogram(S);
   if (tid == 0) {
-    const int32_t nl = R2 < p.num_rows ? __ldg(p.seq_lens + R2) : 0;
-    S.next_len = nl > p.k ? nl : 0;
+    S.next_len = next_len > p.k ? next_len : 0;
     // rank of about 1.25 k in a row of the next length
     S.hint_rank = S.next_len > 0
                       ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)S.next_len) + 1, (int64_t)kCap)
@@ -135,8 +357,8 @@ __device__ __forceinline__ void finish_row(pipe::Shared& S, const Params& p, int
   } else {
     // the threshold was off: the row again, from global memory, exactly
     pipe::cbar();
-    for (int b = tid; b < pipe::kBins2 / 4; b += kThreads)
-      reinterpret_cast<uint4*>(S.hist2)[b] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < pipe::kBins2 / 4; i += kThreads)
+      reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
       S.count = 0u;
       S.rule = pipe::rule_all();
@@ -156,12 +378,19 @@ __device__ __forceinline__ void finish_row(pipe::Shared& S, const Params& p, int
   if (tid == 0 && !emitted) pipe::publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
   if (!redo) {
     if (!emitted) pipe::emit_ordered(S, stage, k, sel);
-    pipe::cbar();  // the staged row is complete
+  }
+  // the page stage of this row (every prepared row's phase is consumed here,
+  // so that the next copy into the stage starts only after this one landed)
+  wait_bounded(&M.page_full[b], parity, timed_out);
+  pipe::cbar();  // the staged row is complete
+  if (!redo) {
     // page transform (section 1 of the page): each thread 8 positions, the
-    // index reads, the page loads and the stores each issued together
+    // index reads, the page reads and the stores each issued together
     constexpr int U = kKMax / kThreads;
     int32_t* o = p.out + R * p.k;
     const int32_t* pr = r.page_row;
+    const PageStage ps = M.pstage[b];
+    const int32_t* pst = M.pages[b] + ps.off;
     const int32_t pb = p.page_bits, pm = (1 << pb) - 1;
     int32_t jv[U], pg[U];
 #pragma unroll
@@ -174,7 +403,8 @@ __device__ __forceinline__ void finish_row(pipe::Shared& S, const Params& p, int
       const int t = tid + u * kThreads;
       // a staged index is always inside the window; the test only keeps a
       // broken hand-over from reading outside the page-table row
-      pg[u] = (t < (int)k && pr != nullptr && (uint32_t)jv[u] < (uint32_t)r.L) ? __ldg(pr + (jv[u] >> pb)) : 0;
+      const bool ok = t < (int)k && pr != nullptr && (uint32_t)jv[u] < (uint32_t)r.L;
+      pg[u] = ok ? (ps.staged ? pst[jv[u] >> pb] : __ldg(pr + (jv[u] >> pb))) : 0;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -185,6 +415,25 @@ __device__ __forceinline__ void finish_row(pipe::Shared& S, const Params& p, int
     pipe::emit_selected(S, p, r, R, sel);  // final values, straight to the output
   }
   pipe::cbar();  // every finishing thread is done with S
+}
+
+// Whole warp: this warp's positions of a row whose window is not longer than
+// k (every index taken, -1 past the window).
+__device__ __forceinline__ void emit_short_row(const Params& p, int64_t row) {
+  const Row r = make_row(p, row, load_row_raw(p, row));
+  emit_whole_window<kThreads>(p, (int32_t)row, r, 0u, 1u);
+}
+
+// Whole warp: waits for the phase `parity` of bar; while it is incomplete the
+// warp emits the range's rows that need no selection (`sh`: the next one).
+__device__ __forceinline__ void wait_emitting(uint64_t* bar, uint32_t parity, bool& timed_out, const Params& p,
+                                              const uint32_t* bits, int64_t lo, int64_t hi, int64_t& sh) {
+  while (sh < hi) {
+    if (__any_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) break;
+    emit_short_row(p, sh);
+    sh = sched::next_row_where<false>(p, bits, lo, hi, sh + 1);
+  }
+  wait_bounded(bar, parity, timed_out);
 }
 
 __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __grid_constant__ Params p) {
@@ -199,79 +448,98 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
     for (int b = 0; b < 2; ++b) {
       mbar_init(&M.set_full[b], 1);
       mbar_init(&M.set_free[b], 1);
+      mbar_init(&M.page_full[b], 1);
       M.set[b].hint_valid = 0u;
       M.set[b].hint_sh = 0u;
+      M.pstage[b].trow = -1;
+      M.pstage[b].off = 0;
+      M.pstage[b].count = 0;
+      M.pstage[b].staged = 0;
     }
   }
   if (lane == 0) fence_barrier_init();
   __syncthreads();
+  int64_t lo, hi;
+  sched::balanced_range<kBlockThreads>(p, blockIdx.x, gridDim.x, kSplitCostFloor, M.range, lo, hi);
+  const uint32_t* bits = M.range.bits;
 
   uint32_t g = 0;  // streaming warps: chunks taken from the ring
-  WCursor cur;
-  cur.src = nullptr;
-  cur.left = 0;
-  cur.row = (int32_t)blockIdx.x - (int32_t)gridDim.x;
+  SCursor cur;
   cur.issued = 0;
+  uint32_t page_armed[2] = {0u, 0u}, page_seen[2] = {0u, 0u};  // finishing thread 0: page_full phases
 
   if (finishing) {
     // ---- finishing warps
-    int64_t rcur = next_streamed(p, blockIdx.x);
-    int64_t rnext = rcur < p.num_rows ? next_streamed(p, rcur + gridDim.x) : p.num_rows;
-    // the first two streamed rows' rules
-    if (rcur < p.num_rows) {
-      prepare_set(M.set[0], p, rcur);
-      if (tid == 0) mbar_arrive(&M.set_free[0]);
+    if constexpr (kRegSplit) regs_raise<kFinishRegs>();
+    int64_t rc = sched::next_selected_row(p, bits, lo, hi, lo);
+    int64_t rn = rc < hi ? sched::next_selected_row(p, bits, lo, hi, rc + 1) : hi;
+    RowRaw dc = {0, 0, 0}, dn = {0, 0, 0};
+    if (rc < hi) dc = load_row_raw(p, rc);
+    if (rn < hi) dn = load_row_raw(p, rn);
+    // the first two streamed rows' sets
+    prepare_set(M, 0u, p, rc, dc, hi);
+    if (tid == 0) {
+      if (rc < hi) ++page_armed[0];
+      mbar_arrive(&M.set_free[0]);
     }
-    if (rnext < p.num_rows) {
-      prepare_set(M.set[1], p, rnext);
-      if (tid == 0) mbar_arrive(&M.set_free[1]);
+    if (rc < hi) {
+      prepare_set(M, 1u, p, rn, dn, hi);
+      if (tid == 0) {
+        if (rn < hi) ++page_armed[1];
+        mbar_arrive(&M.set_free[1]);
+      }
     }
-    uint32_t s = 0;  // streamed rows finished
-    for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
-      if (row != rcur) {  // a window not longer than k: every index, no selection
-        const Row r = load_row(p, (int32_t)row);
-        emit_whole_window<kThreads>(p, (int32_t)row, r, 0u, 1u);
-        continue;
+    int64_t sh = sched::next_row_where<false>(p, bits, lo, hi, lo);  // next row needing no selection
+    for (uint32_t s = 0; rc < hi; ++s) {
+      const uint32_t b = s & 1u, par = (s >> 1) & 1u;
+      const int64_t r2 = rn < hi ? sched::next_selected_row(p, bits, lo, hi, rn + 1) : hi;
+      RowRaw d2 = {0, 0, 0};
+      if (r2 < hi) d2 = load_row_raw(p, r2);  // in flight while the set streams
+      wait_emitting(&M.set_full[b], par, timed_out, p, bits, lo, hi, sh);
+      finish_row(M, b, p, rc, dc, r2 < hi ? d2.L : 0, par, timed_out);
+      if (tid == 0) ++page_seen[b];
+      prepare_set(M, b, p, r2, d2, hi);
+      if (tid == 0) {
+        if (r2 < hi) ++page_armed[b];
+        mbar_arrive(&M.set_free[b]);
       }
-      const uint32_t b = s & 1u;
-      wait_bounded(&M.set_full[b], (s >> 1) & 1u, timed_out);
-      const int64_t r2 = rnext < p.num_rows ? next_streamed(p, rnext + gridDim.x) : p.num_rows;
-      finish_row(M.set[b], p, rcur, r2);
-      if (r2 < p.num_rows) {
-        prepare_set(M.set[b], p, r2);
-        if (tid == 0) mbar_arrive(&M.set_free[b]);
-      }
-      ++s;
-      rcur = rnext;
-      rnext = r2;
+      rc = rn;
+      dc = dn;
+      rn = r2;
+      dn = d2;
+    }
+    while (sh < hi) {  // rows needing no selection not yet emitted
+      emit_short_row(p, sh);
+      sh = sched::next_row_where<false>(p, bits, lo, hi, sh + 1);
     }
   } else {
     // ---- streaming warps
+    if constexpr (kRegSplit) regs_lower<kStreamRegs>();
     const int sw = warp - kWarps;
     const uint64_t policy = l2_evict_first_policy();
-    RowRaw nx = load_row_raw(p, blockIdx.x);  // the grid never exceeds num_rows
-    for (int s = 0; s < kStages; ++s) warp_issue(M.ring, cur, p, sw, policy, blockIdx.x, nx);
-    Deferred none;
-    none.o = nullptr;
-    uint32_t s = 0;  // streamed rows handed over
-    for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
-      const Row r = make_row(p, row, nx);
-      if (row + gridDim.x < p.num_rows) nx = load_row_raw(p, row + gridDim.x);
-      if (r.L <= p.k) continue;
+    scursor_init(cur, p, lo, hi, bits);
+    for (int s = 0; s < kStages; ++s) scursor_issue(M.ring, cur, p, sw, policy);
+    for (uint32_t s = 0;; ++s) {
       const uint32_t b = s & 1u;
       wait_bounded(&M.set_free[b], (s >> 1) & 1u, timed_out);
+      const SetRow sr = M.srow[b];
+      if (sbar_or(sr.row >= hi || sr.row < lo)) break;  // uniform over the streaming warps
+      const Row r = make_row(p, sr.row, RowRaw{sr.L, sr.start, sr.trow});
       const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
-      stream_row_wb(M.set[b], M.ring, sw, p, r, nq, g, cur, policy, timed_out, none, row + gridDim.x, nx);
+      stream_row_wb(M.set[b], M.ring, sw, r, nq, g, timed_out, stream_wait_limit(p), [&] { scursor_issue(M.ring, cur, p, sw, policy); });
       sbar();  // every streaming warp has written its region
       if (tid == kThreads) mbar_arrive(&M.set_full[b]);
-      ++s;
     }
   }
 
-  // Every issued chunk was taken -- unless a wait gave up; then each
-  // streaming warp waits (bounded) for its outstanding copies.
+  // Every issued chunk was taken, and every staged page row waited for --
+  // unless a wait gave up; then each waits (bounded) for what is outstanding.
   if (__syncthreads_or(timed_out ? 1 : 0)) {
-    if (tid == 0) atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
+    if (tid == 0) {
+      atomicOr(&g_device_flags, kFlagStreamWaitTimeout);
+      for (int b = 0; b < 2; ++b)
+        for (uint32_t c = page_seen[b]; c < page_armed[b]; ++c) mbar_wait_bounded(&M.page_full[b], c & 1u);
+    }
     if (!finishing && lane == 0)
       for (uint32_t c = g; c < cur.issued; ++c)
         mbar_wait_bounded(&M.ring.full[warp - kWarps][c % kStages], (c / kStages) & 1u);

@@ -165,16 +165,16 @@ def test_zero_rows_launches_nothing(cuda_device):
 
 
 def test_plan_reports_the_launch(cuda_device):
-    plan = binding.topk_packed_plan(140000, 2048, 4096)
-    assert plan["path"] == binding.PATHS["pipe"]
-    assert plan["threads_per_cta"] == 256, "8 warps, each streaming its own block"
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert plan["grid_ctas"] == 2 * sms, "two pipelined CTAs per SM"
+    plan = binding.topk_packed_plan(140000, 2048, 4096)
+    assert plan["path"] == binding.PATHS["split"]
+    assert plan["threads_per_cta"] == 512, "8 streaming and 8 finishing warps"
+    assert plan["grid_ctas"] == sms, "one CTA per SM"
     small = binding.topk_packed_plan(140000, 2048, 7)
     assert small["grid_ctas"] == 7 and small["path"] == binding.PATHS["split"], "decode-like batches"
-    assert small["threads_per_cta"] == 512
-    assert binding.topk_packed_plan(140000, 2048, sms)["path"] == binding.PATHS["split"]
-    assert binding.topk_packed_plan(140000, 2048, sms + 1)["path"] == binding.PATHS["pipe"]
+    pipe = binding.topk_packed_plan(140000, 2048, 4096, path="pipe")
+    assert pipe["threads_per_cta"] == 256, "8 warps, each streaming its own block"
+    assert pipe["grid_ctas"] == 2 * sms, "two pipelined CTAs per SM"
     st = binding.topk_packed_plan(140000, 2048, 4096, path="stream")
     assert st["threads_per_cta"] == 1024
     assert st["grid_ctas"] % st["cluster_size"] == 0
