@@ -123,10 +123,16 @@ typedef struct {
   int32_t max_ctas;        /* STREAM, PIPE, SPLIT, MULTIPASS: upper bound on the grid; 0 = auto */
   uint32_t stream_wait_ns; /* PIPE, SPLIT: bound of each wait for a streamed chunk of the window, in
                               ns; 0 = the default of about 2 s.  A wait that runs out sets bit 0 of
-                              the diagnostics word and leaves the affected rows unspecified; the
-                              kernel still waits, with the default bound, for every copy it issued
-                              before it exits.  Meant for testing that path. */
+                              the diagnostics word; the warp then stops taking chunks and the rows it
+                              streams are finished exactly from global memory instead (slower, same
+                              result).  The kernel still waits, with the default bound, for every
+                              copy it issued before it exits. */
+  uint32_t test_flags;     /* 0, or TOPK_TEST_UNSATISFIED_WAIT (for testing the path above): each
+                              streaming warp first waits on a barrier that nothing completes, so that
+                              the wait runs out after stream_wait_ns.  Other bits: INVALID_ARG. */
 } topk_launch_config_t;
+
+#define TOPK_TEST_UNSATISFIED_WAIT 1u
 
 /*
  * topk_packed_ex -- topk_packed with explicit launch choices.  `config` may be

@@ -54,11 +54,19 @@ struct Params {
   int32_t* out;
   int32_t num_rows;
   uint32_t stream_wait_ns;  // bound of a wait for a streamed chunk (0: kWaitLimitNs)
+  uint32_t test_flags;      // kTestUnsatisfiedWait: see below
 };
+
+// Test switch: each streaming warp first waits, bounded by the stream-chunk
+// limit, on an mbarrier that nothing completes, so that the wait runs out and
+// the give-up path runs (diagnostic bit 0, rows finished by the exact path,
+// outstanding copies drained at exit).
+constexpr uint32_t kTestUnsatisfiedWait = 1u;
 
 __device__ __forceinline__ uint64_t stream_wait_limit(const Params& p) {
   return p.stream_wait_ns ? (uint64_t)p.stream_wait_ns : kWaitLimitNs;
 }
+
 
 // ---------------------------------------------------------------------------
 // Keys.  key(x) orders like x for every non-NaN float; -0.0 is first turned
@@ -241,11 +249,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+  const uint32_t hint = limit_ns < 20000u ? (uint32_t)limit_ns : 20000u;
+  while (!mbar_try_wait_sleep(bar, parity, hint)) {
     if (global_timer_ns() - t0 > limit_ns) return false;
     __nanosleep(64);
   }
   return true;
+}
+
+// Streaming warp, before its first chunk: under kTestUnsatisfiedWait, waits
+// on `never` (initialised, never arrived on) until the stream-chunk limit runs
+// out, and records the give-up.
+__device__ __forceinline__ void test_unsatisfied_wait(const Params& p, uint64_t* never, bool& timed_out) {
+  if ((p.test_flags & kTestUnsatisfiedWait) && !mbar_wait_bounded(never, 0u, stream_wait_limit(p))) timed_out = true;
 }
 
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.

@@ -154,6 +154,7 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
     const int c = cfg->cluster_size;
     if (!(c == 0 || c == 1 || c == 2 || c == 4 || c == 8)) return TOPK_ERR_INVALID_ARG;
     if (cfg->max_ctas < 0) return TOPK_ERR_INVALID_ARG;
+    if ((cfg->test_flags & ~(uint32_t)TOPK_TEST_UNSATISFIED_WAIT) != 0u) return TOPK_ERR_INVALID_ARG;
   }
   if (k > TOPK_K_MAX) return TOPK_ERR_UNSUPPORTED;
   if (has_table && page_size > (1 << 30)) return TOPK_ERR_UNSUPPORTED;
@@ -256,6 +257,7 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   prm.out = out;
   prm.num_rows = num_rows;
   prm.stream_wait_ns = config ? config->stream_wait_ns : 0u;
+  prm.test_flags = config ? config->test_flags : 0u;
 
   const Plan pl = make_plan(*d, row_stride, num_rows, config);
   if (pl.grid <= 0) return TOPK_ERR_UNSUPPORTED;  // the split kernel cannot be resident here

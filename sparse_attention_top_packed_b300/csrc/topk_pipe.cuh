@@ -780,9 +780,11 @@ __device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
 // (keys_and_histogram).
 //
 // A chunk is taken only once its copy has landed.  If a wait gives up
-// (`limit_ns`), the warp records it in timed_out and leaves the row: the
-// chunk stays outstanding and its stage is not refilled, so no stage ever
-// holds two copies in flight; the kernel's exit waits for what is left.
+// (`limit_ns`), the warp records it in timed_out and stops taking chunks, for
+// this row and every later one: its chunks stay outstanding and their stages
+// are not refilled, so no stage ever holds two copies in flight; the kernel's
+// exit waits for what is left.  Such a warp marks each of its rows as
+// overflowed, so they are finished exactly from global memory.
 template <int NS, int NW, int CQ, class AfterChunk>
 __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, int w, const Row& r, int64_t nq,
                                               uint32_t& g, bool& timed_out, uint64_t limit_ns,
@@ -805,11 +807,10 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
   bool full = false;
   uint32_t s = g % NS, ph = (g / NS) & 1u;
   for (int64_t cq = q0; cq < q1; cq += CQ, ++g) {
-    if (!mbar_try_wait(&R.full[w][s], ph)) {
-      if (timed_out || !mbar_wait_bounded(&R.full[w][s], ph, limit_ns)) {
-        timed_out = true;
-        break;
-      }
+    if (timed_out || (!mbar_try_wait(&R.full[w][s], ph) && !mbar_wait_bounded(&R.full[w][s], ph, limit_ns))) {
+      timed_out = true;
+      if (lane == 0) S.overflow = 1u;  // the row is finished from global memory
+      break;
     }
     const float4* st = R.st[w][s];
     // the lane's kBits consecutive floats; bit 4u+c of mr is element 4*((u+rot)%QPL)+c
@@ -844,11 +845,17 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
           full = true;
           if (lane == 0) S.overflow = 1u;
         } else {
-          // exclusive prefix of n over the lanes, from the bits of n
+          // exclusive prefix of n over the lanes, from the bits of n (the
+          // low three suffice unless a lane admitted 8 or more)
           uint32_t pos = wcnt;
 #pragma unroll
-          for (int b = 0; b < (QPL == 8 ? 6 : 7); ++b)
+          for (int b = 0; b < 3; ++b)
             pos += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (n >> b) & 1u) & lt) << b;
+          if (__any_sync(0xFFFFFFFFu, n >= 8u)) {
+#pragma unroll
+            for (int b = 3; b < (QPL == 8 ? 6 : 7); ++b)
+              pos += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (n >> b) & 1u) & lt) << b;
+          }
           const uint32_t* sf = reinterpret_cast<const uint32_t*>(st) + kBits * lane;
           // ascending e: window order within the lane; two at a time, so the
           // two loads are in flight together
@@ -902,17 +909,38 @@ __device__ __forceinline__ void keys_and_histogram(Shared& S) {
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
   const uint32_t tk = S.fh_tk, sh = S.fh_sh;
   uint32_t top = 0;
-  for (uint32_t i = lane; i < cnt; i += 32) {
-    const uint32_t key = key_of(__uint_as_float(S.bkey[base + i]));
-    S.bkey[base + i] = key;
-    const uint32_t fb = (key - tk) >> sh;
-    if (fb < (uint32_t)kFineTop)
-      atomicAdd(&S.hist2[fb], 1u);
-    else
-      ++top;
+  for (uint32_t i0 = 0; i0 < cnt; i0 += 128) {  // 4 entries a lane, loads issued together
+    uint32_t raw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t i = i0 + 32u * u + (uint32_t)lane;
+      raw[u] = i < cnt ? S.bkey[base + i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t i = i0 + 32u * u + (uint32_t)lane;
+      if (i < cnt) {
+        const uint32_t key = key_of(__uint_as_float(raw[u]));
+        S.bkey[base + i] = key;
+        const uint32_t fb = (key - tk) >> sh;
+        if (fb < (uint32_t)kFineTop)
+          atomicAdd(&S.hist2[fb], 1u);
+        else
+          ++top;
+      }
+    }
   }
   top = __reduce_add_sync(0xFFFFFFFFu, top);
   if (lane == 0) S.wtop[w] = top;
+}
+
+// Rank the next row's admission threshold should reach in this row: about
+// 1.15 k in a row of the next row's length (binomial noise at that rank is a
+// few percent of k, so the next row still admits at least k), capped by the
+// buffer.  0 when there is no next row.
+__device__ __forceinline__ uint32_t hint_rank_for(uint32_t k, int32_t L, int32_t next_len) {
+  if (next_len <= 0) return 0u;
+  return (uint32_t)min((int64_t)23 * k * L / (20 * (int64_t)next_len) + 1, (int64_t)kCap);
 }
 
 // Fine shift for a row whose threshold key sits about `d` keys below its k-th
@@ -1005,6 +1033,39 @@ __device__ __forceinline__ void publish_hint(Shared& S, uint32_t hr, uint32_t hi
   }
 }
 
+// Where an emission puts the t-th selected window index j of a row.
+// OutRaw: j itself, into the output row in global memory (the page transform
+// follows separately).
+struct OutRaw {
+  int32_t* o;
+  __device__ __forceinline__ void put(uint32_t q, int32_t j) const { __stcg(o + q, j); }
+};
+
+// OutShared: j itself, into a staging row in shared memory.
+struct OutShared {
+  int32_t* o;
+  __device__ __forceinline__ void put(uint32_t q, int32_t j) const { o[q] = j; }
+};
+
+// OutPaged: the final value, page_row[j >> page_bits] * page_size + the
+// offset (section 1 of the page), the page read from a shared-memory copy of
+// the page-table row when there is one, else from global memory; j itself
+// without a page table.
+struct OutPaged {
+  int32_t* o;
+  const int32_t* stage;     // page_row[0 ..] in shared memory, or null
+  const int32_t* page_row;  // the row's page-table row, or null (raw indices)
+  int32_t page_bits;
+  __device__ __forceinline__ void put(uint32_t q, int32_t j) const {
+    int32_t v = j;
+    if (page_row != nullptr) {
+      const int32_t pg = stage != nullptr ? stage[j >> page_bits] : __ldg(page_row + (j >> page_bits));
+      v = pg * (1 << page_bits) + (j & ((1 << page_bits) - 1));
+    }
+    __stcg(o + q, v);
+  }
+};
+
 // Fast rows, entered through a barrier after the stream: the exact k-th
 // largest pair from the fine histogram, and the row's selected window indices
 // written to out[row] in ascending order.
@@ -1020,10 +1081,9 @@ __device__ __forceinline__ void publish_hint(Shared& S, uint32_t hr, uint32_t hi
 // cannot settle it: the rank lies above its range, or more than 32 candidates
 // share its bin.  Also proposes the next row's hint (rank hr) and fine shift.
 //
-// `o`: where the row's k window indices go -- its output row in global memory
-// (kToShared false: streaming stores) or a staging row in shared memory.
-template <bool kToShared = false>
-__device__ __forceinline__ bool select_emit_fine(Shared& S, int32_t* o, int32_t L, uint32_t n, uint32_t k,
+// `out`: where the row's k selected window indices go (OutRaw, OutPaged).
+template <class Out>
+__device__ __forceinline__ bool select_emit_fine(Shared& S, const Out& out, int32_t L, uint32_t n, uint32_t k,
                                                  uint32_t hr) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t top = 0;
@@ -1207,12 +1267,7 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, int32_t* o, int32_t 
     for (int u = 0; u < 4; ++u) {
       const uint32_t q = pos + __popc(bm[u] & lt);
       if ((bm[u] >> lane) & 1u) {
-        if (q < k) {
-          if constexpr (kToShared)
-            o[q] = jj[u];
-          else
-            __stcg(o + q, jj[u]);
-        }
+        if (q < k) out.put(q, jj[u]);
         bad |= q >= k;
       }
       pos += __popc(bm[u]);
@@ -1224,10 +1279,10 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, int32_t* o, int32_t 
 
 // Fast rows whose selection took the generic path: every warp's region is in
 // ascending window index and the regions follow each other in warp order, so
-// the selected entries' output positions are prefix counts.  Writes the
-// window indices; the page transform follows (Deferred).
-// `o`: the output row in global memory or a staging row in shared memory.
-__device__ __forceinline__ void emit_ordered(Shared& S, int32_t* o, uint32_t k, const Rule sel) {
+// the selected entries' output positions are prefix counts.
+// `out`: where the selected window indices go (OutRaw, OutPaged).
+template <class Out>
+__device__ __forceinline__ void emit_ordered(Shared& S, const Out& out, uint32_t k, const Rule sel) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
   const uint32_t lt = lanemask_lt();
@@ -1252,7 +1307,7 @@ __device__ __forceinline__ void emit_ordered(Shared& S, int32_t* o, uint32_t k, 
     if (take) {
       const uint32_t q = pos + __popc(b & lt);
       if (q < k)
-        o[q] = j;
+        out.put(q, j);
       else
         atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
     }
@@ -1350,6 +1405,7 @@ struct PipeSmem {
   Ring<kWStages> ring;
   Shared s;
   sched::RangeSmem range;
+  uint64_t never;  // an mbarrier nothing arrives on (kTestUnsatisfiedWait)
 };
 
 // Cost floor of a row in the balanced split (elements): the end of a row
@@ -1372,6 +1428,8 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
   if (tid == 0) {
     S.hint_valid = 0u;
     S.hint_sh = 0u;
+    mbar_init(&M.never, 1);
+    fence_barrier_init();
   }
   __syncthreads();
   int64_t lo, hi;
@@ -1388,6 +1446,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
   cur.hi = (int32_t)hi;
   cur.bits = M.range.bits;
   for (int s = 0; s < kWStages; ++s) warp_issue(R, cur, p, w, policy, lo, nx);
+  test_unsatisfied_wait(p, &M.never, timed_out);
 
   uint32_t g = 0;  // chunks this warp took from its ring
   Deferred dfr;
@@ -1440,8 +1499,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
       }
       if (lane == 0) {
         S.next_len = nl;
-        // rank of about 1.25 k in a row of the next row's length
-        S.hint_rank = nl > 0 ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)nl) + 1, (int64_t)kCap) : 0u;
+        S.hint_rank = hint_rank_for(k, r.L, nl);
       }
     }
     cbar();
@@ -1454,7 +1512,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     uint32_t hint_ok = 0u, hint_sh = S.fh_sh;
     bool emitted = false;
     if (!redo) {
-      emitted = select_emit_fine(S, p.out + row * p.k, r.L, n, k, hr);
+      emitted = select_emit_fine(S, OutRaw{p.out + row * p.k}, r.L, n, k, hr);
       if (!emitted) {
         n = 0u;  // the regions may have been compacted (every entry at or above the k-th key's bin kept)
 #pragma unroll
@@ -1487,7 +1545,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     }
     if (tid == 0 && !emitted) publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
     if (!redo) {
-      if (!emitted) emit_ordered(S, p.out + row * p.k, k, sel);
+      if (!emitted) emit_ordered(S, OutRaw{p.out + row * p.k}, k, sel);
       if (r.page_row != nullptr) deferred_start(dfr, p.out + row * p.k, r.page_row, k);  // else j is final
     } else {
       emit_selected(S, p, r, row, sel);

@@ -91,6 +91,7 @@ struct SplitSmem {
   uint64_t set_full[2];   // streaming -> finishing warps: the set holds its streamed row
   uint64_t set_free[2];   // finishing -> streaming warps: the set is ready for its next row
   uint64_t page_full[2];  // the set's page stage is written (one phase per prepared row)
+  uint64_t never;         // an mbarrier nothing arrives on (kTestUnsatisfiedWait)
   sched::RangeSmem range;
 };
 
@@ -327,23 +328,21 @@ __device__ __forceinline__ void finish_row(SplitSmem& M, uint32_t b, const Param
   pipe::keys_and_histogram(S);
   if (tid == 0) {
     S.next_len = next_len > p.k ? next_len : 0;
-    // rank of about 1.25 k in a row of the next length
-    S.hint_rank = S.next_len > 0
-                      ? (uint32_t)min((int64_t)5 * k * r.L / (4 * (int64_t)S.next_len) + 1, (int64_t)kCap)
-                      : 0u;
+    S.hint_rank = pipe::hint_rank_for(k, r.L, S.next_len);
   }
   pipe::cbar();
+  int32_t* stage = reinterpret_cast<int32_t*>(S.hist2);  // the row's indices, before the page transform
+  const pipe::OutShared out{stage};
   uint32_t n = 0;
 #pragma unroll
   for (int i = 0; i < kWarps; ++i) n += S.rcnt[i];
   const bool redo = n < k || S.overflow != 0u;
   const uint32_t hr = S.hint_rank;
-  int32_t* stage = reinterpret_cast<int32_t*>(S.hist2);  // the row's indices, before the page transform
   pipe::Rule sel, hint;
   uint32_t hint_ok = 0u, hint_sh = S.fh_sh;
   bool emitted = false;
   if (!redo) {
-    emitted = pipe::select_emit_fine<true>(S, stage, r.L, n, k, hr);
+    emitted = pipe::select_emit_fine(S, out, r.L, n, k, hr);
     if (!emitted) {
       n = 0u;  // the regions may have been compacted
 #pragma unroll
@@ -377,7 +376,7 @@ __device__ __forceinline__ void finish_row(SplitSmem& M, uint32_t b, const Param
   }
   if (tid == 0 && !emitted) pipe::publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
   if (!redo) {
-    if (!emitted) pipe::emit_ordered(S, stage, k, sel);
+    if (!emitted) pipe::emit_ordered(S, out, k, sel);
   }
   // the page stage of this row (every prepared row's phase is consumed here,
   // so that the next copy into the stage starts only after this one landed)
@@ -456,6 +455,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
       M.pstage[b].count = 0;
       M.pstage[b].staged = 0;
     }
+    mbar_init(&M.never, 1);
   }
   if (lane == 0) fence_barrier_init();
   __syncthreads();
@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
     const uint64_t policy = l2_evict_first_policy();
     scursor_init(cur, p, lo, hi, bits);
     for (int s = 0; s < kStages; ++s) scursor_issue(M.ring, cur, p, sw, policy);
+    test_unsatisfied_wait(p, &M.never, timed_out);
     for (uint32_t s = 0;; ++s) {
       const uint32_t b = s & 1u;
       wait_bounded(&M.set_free[b], (s >> 1) & 1u, timed_out);

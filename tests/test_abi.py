@@ -82,6 +82,10 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert _call(cfg=bad) == INVALID
     bad = binding.LaunchConfig(2, 0, -1)
     assert _call(cfg=bad) == INVALID
+    bad = binding.LaunchConfig(3, 0, 0, 0, 2)  # an unknown test flag
+    assert _call(cfg=bad) == INVALID
+    known = binding.LaunchConfig(3, 0, 0, 1000, binding.TEST_UNSATISFIED_WAIT)
+    assert _call(cfg=known, scores=0x1002) == UNSUPPORTED  # accepted; the next check answers
 
 
 def test_null_page_table_means_raw_indices_and_frees_page_arguments(lib):

@@ -327,3 +327,29 @@ def test_repeated_launches_are_identical(cuda_device, name, path):
     first = run(w, path=path)
     for _ in range(3):
         assert torch.equal(first, run(w, path=path)), "two launches on the same input disagree"
+
+
+# ---------------------------------------------------------------------------
+# The give-up path of a bounded wait, made to run on purpose: each streaming
+# warp first waits on a barrier that nothing completes, with a 50 us bound.
+# The wait runs out, bit 0 of the diagnostics word is raised, the warps stop
+# taking chunks, the rows are finished exactly from global memory, and every
+# copy already issued is waited for before the kernel exits.  Nothing faults:
+# the result must still be the oracle's, and the next normal call too.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("path", ["pipe", "split"])
+def test_stream_wait_give_up_is_recorded_and_the_result_stays_exact(cuda_device, path):
+    rng = np.random.default_rng(77)
+    p = wl.random_problem(rng, rows=24, max_len=20000, k=2048, page_size=64, values="normal", slack=13)
+    w = host_problem_to_device(p, cuda_device)
+    want = oracle_host(p)
+    binding.topk_packed_device_flags(reset=True)
+    out = torch.full((w.num_rows, w.k), -7, dtype=torch.int32, device=cuda_device)
+    binding.topk_packed_ex(w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch, w.page_table,
+                           w.pt_stride, w.page_size, w.k, out, w.num_rows, path=path, stream_wait_ns=50_000,
+                           test_flags=binding.TEST_UNSATISFIED_WAIT)
+    torch.cuda.synchronize()
+    flags = binding.topk_packed_device_flags(reset=True)
+    assert flags & 1, "the wait that nothing completes must be recorded as given up"
+    assert np.array_equal(out.cpu().numpy(), want)
+    assert np.array_equal(run(w, path=path).cpu().numpy(), want)
