@@ -232,12 +232,14 @@ def run_ours(a, rank: int, world: int, device) -> dict:
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         step_ms, kernel_ms = float(t[0]), float(t[1])
 
-    # parity spot check of the timed output against the oracle (first rows)
+    # the diagnostics word after the timed launches: a bounded wait that gave
+    # up would show here (the run is then rejected)
+    flags = binding.topk_packed_device_flags(reset=True)
     out = args[9]
     e2e = run_e2e(a, w, device) if rank == 0 else None
     result = {
         "step_ms": step_ms, "kernel_ms": kernel_ms, "alg_bytes": alg_bytes, "flush": flush,
-        "clocks": clocks, "e2e": e2e, "workload": w, "out": out,
+        "clocks": clocks, "e2e": e2e, "workload": w, "out": out, "device_flags": flags,
     }
     return result
 
@@ -283,69 +285,81 @@ def run_e2e(a, w, device) -> dict:
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
 
 
-def cpu_baseline(w, target_s: float = 12.0) -> dict:
-    """The CPU oracle, as it stands, on a bounded sample of the workload's rows
-    (windows copied to the host first, outside the timing), all host cores.
-    A small probe sizes the sample to about `target_s` seconds of oracle work,
-    or the whole workload when that takes less."""
-    from oracle import default_threads, topk_packed_reference
+def oracle_sample(w, n: int, seed: int):
+    """Host copies of the windows of a sample of n rows (first, last and
+    evenly spread), and the arguments the CPU oracle takes for them."""
     from sparse_attention_top_packed_b300.workloads import gather_windows, sample_rows
 
+    rows = sample_rows(w.num_rows, n, seed=seed)
+    win, L = gather_windows(w, rows)
+    b = (rows.numpy() if w.row_to_batch is None
+         else w.row_to_batch[rows.to(w.row_to_batch.device)].cpu().numpy()).astype(np.int32)
+    table = w.page_table.reshape(-1).cpu().numpy()
+    return rows, (win.reshape(-1), win.shape[1], L, np.zeros(len(L), np.int32), b, table,
+                  w.pt_stride, w.page_size, w.k)
+
+
+def time_oracle(args, cores: int):
+    """One call of the CPU oracle as it stands (all rows of the sample, `cores`
+    threads): seconds and its [rows, k] result."""
+    from oracle import topk_packed_reference
+
+    t0 = time.perf_counter()
+    res = topk_packed_reference(*args, nthreads=cores)
+    return time.perf_counter() - t0, res
+
+
+def cpu_baseline(w, out, target_s: float = 12.0) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of the workload's rows
+    (windows copied to the host first, outside the timing), all host cores,
+    in one call.  A small probe sizes the sample to about `target_s` seconds
+    of oracle work, or the whole workload when that takes less.  The oracle's
+    result for those rows is also compared with the timed launch's output
+    (`spot_check`)."""
+    from oracle import default_threads
+
     cores = default_threads()
-
-    def run_rows(n):
-        rows = sample_rows(w.num_rows, n, seed=1)
-        win, L = gather_windows(w, rows)
-        b = (rows.numpy() if w.row_to_batch is None
-             else w.row_to_batch[rows.to(w.row_to_batch.device)].cpu().numpy()).astype(np.int32)
-        table = w.page_table.reshape(-1).cpu().numpy()
-        t0 = time.perf_counter()
-        topk_packed_reference(win.reshape(-1), win.shape[1], L, np.zeros(len(L), np.int32), b, table,
-                              w.pt_stride, w.page_size, w.k, nthreads=cores)
-        return time.perf_counter() - t0, int(rows.numel())
-
-    dt, n = run_rows(min(w.num_rows, max(2 * cores, 16)))
+    rows, args = oracle_sample(w, min(w.num_rows, max(2 * cores, 16)), seed=1)
+    dt, res = time_oracle(args, cores)
+    n = int(rows.numel())
     if n < w.num_rows:
         want = int(n * target_s / max(dt, 1e-4))
         n2 = min(w.num_rows, max(n, want))
         if n2 > n:
-            dt, n = run_rows(n2)
+            del args, res
+            rows, args = oracle_sample(w, n2, seed=1)
+            dt, res = time_oracle(args, cores)
+            n = int(rows.numel())
+    got = out[rows.to(out.device)].cpu().numpy()
+    bad = int((got != res).any(axis=1).sum())
     return {"value": n / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {w.num_rows} rows (first, last and evenly spread), "
-                      f"{dt:.2f} s on {cores} threads; windows copied to the host beforehand"}
+            "sample": f"{n} of {w.num_rows} rows (first, last and evenly spread) in one call, "
+                      f"{dt:.2f} s on {cores} threads; windows copied to the host beforehand",
+            "spot_check": {"rows": n, "mismatched_rows": bad,
+                           "what": "the timed launch's output rows against the oracle's, int32 equality"}}
 
 
 def run_reference(a, rank: int, world: int) -> None:
     """The reference arm: the CPU oracle, timed as it stands on the host cores,
-    on the same workload and metric.  Each step is a bounded sample of rows."""
+    on the same workload and metric.  Every step is one call of the oracle on
+    the same bounded sample of rows (about 512 MB of windows), as in the
+    cpu_baseline leg, so the two figures measure the same thing."""
     if rank != 0:
         return
-    from oracle import default_threads, topk_packed_reference
-    from sparse_attention_top_packed_b300.workloads import gather_windows, sample_rows
+    from oracle import default_threads
 
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     w = make_workload(a.workload, device, a.rows)
     cores = default_threads()
-    rows_per_step = max(1, min(w.num_rows, cores))
+    avg_row_bytes = max(w.window_bytes_all() / max(w.num_rows, 1), 4.0)
+    rows_per_step = int(min(w.num_rows, max(16 * cores, (512 << 20) // avg_row_bytes)))
+    rows, args = oracle_sample(w, rows_per_step, seed=1)
+    rows_per_step = int(rows.numel())
     steps = []
-    total = a.warmup + a.steps
-    batches = []
-    for s in range(total):
-        rows = sample_rows(w.num_rows, rows_per_step, seed=100 + s)
-        win, L = gather_windows(w, rows)
-        b = (rows.numpy() if w.row_to_batch is None
-             else w.row_to_batch[rows.to(w.row_to_batch.device)].cpu().numpy()).astype(np.int32)
-        batches.append((win, L, b))
-        if len(batches) >= 8:
-            break
-    table = w.page_table.reshape(-1).cpu().numpy()
-    for s in range(total):
-        win, L, b = batches[s % len(batches)]
-        t0 = time.perf_counter()
-        topk_packed_reference(win.reshape(-1), win.shape[1], L, np.zeros(len(L), np.int32), b, table,
-                              w.pt_stride, w.page_size, w.k, nthreads=cores)
+    for s in range(a.warmup + a.steps):
+        dt, _ = time_oracle(args, cores)
         if s >= a.warmup:
-            steps.append(time.perf_counter() - t0)
+            steps.append(dt)
     sec = sum(steps) / len(steps)
     value = rows_per_step / sec
     line = {
@@ -354,7 +368,7 @@ def run_reference(a, rank: int, world: int) -> None:
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_block(a, w, None),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows_per_step} rows per step of {w.num_rows}"},
+                         "sample": f"the same {rows_per_step} of {w.num_rows} rows every step, one call each"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -408,6 +422,7 @@ def main():
 
     r = run_ours(a, rank, world, device)
     w = r["workload"]
+    mismatched = 0
     if rank == 0:
         peaks = measured_peaks()
         plan = binding.topk_packed_plan(w.row_stride, w.k, w.num_rows, path=a.path)
@@ -430,13 +445,19 @@ def main():
             "gpu_launches": a.steps,
             "clocks": r["clocks"],
             "e2e": r["e2e"],
+            "device_flags": r["device_flags"],
         }
         if world == 1 and not a.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w)
+            line["cpu_baseline"] = cpu_baseline(w, r["out"])
+            mismatched = line["cpu_baseline"]["spot_check"]["mismatched_rows"]
         print(json.dumps(line), flush=True)
+    failed = r["device_flags"] != 0 or bool(mismatched)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+    if failed:
+        log("bench: the timed output failed its check (diagnostics word or oracle spot check); see the JSON line")
+        sys.exit(1)
 
 
 if __name__ == "__main__":

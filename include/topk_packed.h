@@ -94,7 +94,9 @@ typedef enum {
  *   TOPK_ERR_DEVICE       the current device is not sm_103a or cannot be queried.
  *   TOPK_ERR_LAUNCH       the kernel launch was rejected.
  * Thread safety: safe to call from several host threads; calls on different
- * streams may run concurrently (they share no device state).
+ * streams may run concurrently.  The only device state they share is the
+ * per-device diagnostics word (topk_packed_device_flags), which every launch
+ * may set bits in.
  */
 TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                           const int32_t* row_starts, const int32_t* row_to_batch,
@@ -164,13 +166,22 @@ TOPK_API const char* topk_status_string(topk_status_t status);
 TOPK_API int topk_last_cuda_error(void);
 
 /*
- * Device-side diagnostics.  Every wait inside the kernels is bounded; a wait
- * that runs out records a bit here instead of hanging (the kernel then
- * finishes its control flow and the affected rows are unspecified):
- *   bit 0: a wait for a TMA chunk of the score stream gave up.
- * topk_packed_device_flags copies the flags of the current device into *flags
+ * Device-side diagnostics: one 32-bit word per device, shared by every launch
+ * of the library on that device (whatever the stream).  Every wait inside the
+ * kernels is bounded; a wait that runs out records a bit here instead of
+ * hanging, and the kernel finishes its control flow:
+ *   bit 0: a wait for a TMA chunk of the score stream gave up.  In the PIPE and
+ *          SPLIT kernels the affected rows are then finished exactly from
+ *          global memory (same result, slower); in the others they are
+ *          unspecified.  Every copy a kernel issued has landed before it exits.
+ *   bit 1: an output position at or past k was computed (a selection that is
+ *          not exact); the position is not written.  Never expected.
+ * topk_packed_device_flags copies the word of the current device into *flags
  * (after the work queued on `stream` so far) and, when `reset` is non-zero,
- * clears them.  It synchronizes `stream`.
+ * clears it.  It synchronizes `stream`.  A reset races with launches running
+ * on other streams of the same device: a bit one of them sets between the
+ * copy and the clear is lost, so read with reset only when no other launch
+ * is in flight.
  */
 TOPK_API topk_status_t topk_packed_device_flags(uint32_t* flags, int32_t reset, topk_stream_t stream);
 

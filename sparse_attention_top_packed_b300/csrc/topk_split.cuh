@@ -66,7 +66,7 @@ static_assert(kSW == kWarps || 2 * kPart == kRegion, "two streaming parts make o
 constexpr int kPageStage = 1536;             // page-table entries a set can stage (6 KB)
 // Cost floor of a row in the balanced split (elements): the finishing warps
 // need about as long per row as the stream takes for this many elements.
-constexpr uint32_t kSplitCostFloor = 32768;
+constexpr uint32_t kSplitCostFloor = 98304;
 
 // The row a set is prepared for, as the streaming warps read it.
 struct SetRow {
