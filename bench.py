@@ -339,6 +339,44 @@ def cpu_baseline(w, out, target_s: float = 12.0) -> dict:
                            "what": "the timed launch's output rows against the oracle's, int32 equality"}}
 
 
+def run_pdl_gap(a, device) -> None:
+    """Times pairs of (producer kernel, topk_packed_ex) on one stream, with and
+    without the dependent launch, and prints one JSON line.  The producer is a
+    stand-in for the kernel writing the scores (a copy of them, no added
+    delay) that lets its dependents start at once."""
+    from sparse_attention_top_packed_b300 import binding
+    from sparse_attention_top_packed_b300.producer import produce_scores
+
+    torch.cuda.set_device(device)
+    w = make_workload(a.workload, device, a.rows)
+    src = w.scores.clone()
+    out = torch.empty((w.num_rows, w.k), dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device)
+    args = (w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch, w.page_table,
+            w.pt_stride, w.page_size, w.k, out, w.num_rows)
+    res = {}
+    for dep in (False, True, False, True):
+        def pair():
+            produce_scores(w.scores, src, 0, stream)
+            binding.topk_packed_ex(*args, path=a.path, dependent_launch=dep, stream=stream)
+        for _ in range(a.warmup):
+            pair()
+        stream.synchronize()
+        b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b.record(stream)
+        for _ in range(a.steps):
+            pair()
+        e.record(stream)
+        stream.synchronize()
+        res.setdefault(dep, []).append(b.elapsed_time(e) * 1e3 / a.steps)
+    plain, dep = min(res[False]), min(res[True])
+    print(json.dumps({"pdl_gap": {"workload": WORKLOAD_TEXT[a.workload], "pairs": a.steps,
+                                  "us_per_pair_plain": plain, "us_per_pair_dependent": dep,
+                                  "saving_us": plain - dep,
+                                  "what": "producer kernel (score copy) then topk_packed_ex on one stream, "
+                                          "CUDA events over the pairs, best of two runs"}}), flush=True)
+
+
 def run_reference(a, rank: int, world: int) -> None:
     """The reference arm: the CPU oracle, timed as it stands on the host cores,
     on the same workload and metric.  Every step is one call of the oracle on
@@ -403,6 +441,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "pipe", "split", "stream", "multipass"],
                     help="kernel family (auto: the choice topk_packed makes)")
+    ap.add_argument("--pdl-gap", action="store_true",
+                    help="time producer + top-k pairs with and without the dependent launch instead")
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3
@@ -415,6 +455,10 @@ def main():
         return
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if a.pdl_gap:
+        if rank == 0:
+            run_pdl_gap(a, device)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
 

@@ -132,6 +132,14 @@ typedef struct {
   uint32_t test_flags;     /* 0, or TOPK_TEST_UNSATISFIED_WAIT (for testing the path above): each
                               streaming warp first waits on a barrier that nothing completes, so that
                               the wait runs out after stream_wait_ns.  Other bits: INVALID_ARG. */
+  int32_t dependent_launch; /* 1: launch with programmatic stream serialization (programmatic
+                              dependent launch), so that the kernel can be scheduled and set up
+                              while the previous kernel on `stream` -- typically the one writing the
+                              scores -- is still running; it waits for that kernel to complete
+                              (griddepcontrol.wait) before reading any argument array, and lets the
+                              next kernel on the stream start its own set-up early.  0: an ordinary
+                              stream-ordered launch.  Other values: INVALID_ARG.  (Page section 2,
+                              PDLWaitPrimary before the scores are read.) */
 } topk_launch_config_t;
 
 #define TOPK_TEST_UNSATISFIED_WAIT 1u

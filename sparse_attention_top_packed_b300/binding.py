@@ -31,7 +31,7 @@ class TopkError(RuntimeError):
 class LaunchConfig(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("stream_wait_ns", ctypes.c_uint32),
-                ("test_flags", ctypes.c_uint32)]
+                ("test_flags", ctypes.c_uint32), ("dependent_launch", ctypes.c_int32)]
 
 
 _lib = None
@@ -104,9 +104,9 @@ TEST_UNSATISFIED_WAIT = 1
 
 
 def _config(path="auto", cluster_size: int = 0, max_ctas: int = 0,
-            stream_wait_ns: int = 0, test_flags: int = 0) -> LaunchConfig:
+            stream_wait_ns: int = 0, test_flags: int = 0, dependent_launch: bool = False) -> LaunchConfig:
     return LaunchConfig(PATHS[path] if isinstance(path, str) else int(path), int(cluster_size),
-                        int(max_ctas), int(stream_wait_ns), int(test_flags))
+                        int(max_ctas), int(stream_wait_ns), int(test_flags), 1 if dependent_launch else 0)
 
 
 def topk_packed(scores, row_stride: int, seq_lens, row_starts, row_to_batch, page_table,
@@ -122,9 +122,9 @@ def topk_packed(scores, row_stride: int, seq_lens, row_starts, row_to_batch, pag
 def topk_packed_ex(scores, row_stride: int, seq_lens, row_starts, row_to_batch, page_table,
                    pt_stride: int, page_size: int, k: int, out, num_rows: int,
                    path="auto", cluster_size: int = 0, max_ctas: int = 0, stream_wait_ns: int = 0,
-                   test_flags: int = 0, stream=None) -> None:
+                   test_flags: int = 0, dependent_launch: bool = False, stream=None) -> None:
     lib = _load()
-    cfg = _config(path, cluster_size, max_ctas, stream_wait_ns, test_flags)
+    cfg = _config(path, cluster_size, max_ctas, stream_wait_ns, test_flags, dependent_launch)
     st = lib.topk_packed_ex(_ptr(scores), int(row_stride), _ptr(seq_lens), _ptr(row_starts),
                             _ptr(row_to_batch), _ptr(page_table), int(pt_stride), int(page_size),
                             int(k), _ptr(out), int(num_rows), ctypes.byref(cfg),

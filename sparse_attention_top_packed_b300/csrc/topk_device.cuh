@@ -257,6 +257,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Programmatic dependent launch.  The page's section 2 has the kernel wait for
+// the grid that produces the scores (its PDLWaitPrimary) before it touches
+// them.  Here every kernel calls wait_for_producer after the part of its
+// prologue that reads no input (shared-memory and barrier set-up) and before
+// its first read of any argument array; launched with programmatic stream
+// serialization it can then start while the previous kernel on the stream
+// still runs.  Without that launch attribute the wait returns at once.
+// allow_dependents lets the next kernel on the stream start its own prologue;
+// that kernel's wait still holds it until this grid has completed.
+__device__ __forceinline__ void wait_for_producer() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Streaming warp, before its first chunk: under kTestUnsatisfiedWait, waits
 // on `never` (initialised, never arrived on) until the stream-chunk limit runs
 // out, and records the give-up.

@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(kMultipassThreads, 2) topk_multipass_kernel(Pa
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelectShared& S = *reinterpret_cast<SelectShared*>(smem_raw);
   ScanParity par;
+  wait_for_producer();
+  allow_dependents();
   for (int64_t row = blockIdx.x; row < p.num_rows; row += gridDim.x) {
     const Row r = load_row(p, (int32_t)row);
     if (row_is_whole(r, p.k)) {
@@ -347,6 +349,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
   const int32_t cid = (int32_t)(blockIdx.x / CLUSTER), ncl = (int32_t)(gridDim.x / CLUSTER);
   const uint32_t k = (uint32_t)p.k;
   const uint64_t policy = l2_evict_first_policy();
+  wait_for_producer();  // the prologue below already reads the inputs
+  allow_dependents();
 
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&S.full[w][s], 1);

@@ -155,6 +155,7 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
     if (!(c == 0 || c == 1 || c == 2 || c == 4 || c == 8)) return TOPK_ERR_INVALID_ARG;
     if (cfg->max_ctas < 0) return TOPK_ERR_INVALID_ARG;
     if ((cfg->test_flags & ~(uint32_t)TOPK_TEST_UNSATISFIED_WAIT) != 0u) return TOPK_ERR_INVALID_ARG;
+    if (cfg->dependent_launch != 0 && cfg->dependent_launch != 1) return TOPK_ERR_INVALID_ARG;
   }
   if (k > TOPK_K_MAX) return TOPK_ERR_UNSUPPORTED;
   if (has_table && page_size > (1 << 30)) return TOPK_ERR_UNSUPPORTED;
@@ -207,21 +208,34 @@ Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t num_rows,
   return pl;
 }
 
-template <int C>
-cudaError_t launch_stream(const Params& prm, int64_t grid, cudaStream_t stream) {
+// One launch through cudaLaunchKernelEx: optional thread-block cluster and
+// programmatic stream serialization (the kernel may start while the previous
+// kernel on the stream still runs; it waits for it before reading inputs).
+template <class Kernel>
+cudaError_t launch(Kernel kernel, int64_t grid, int threads, size_t smem, int cluster, bool dependent,
+                   cudaStream_t stream, const Params& prm) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(topk::kStreamThreads, 1, 1);
-  cfg.dynamicSmemBytes = sizeof(topk::StreamShared);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk::topk_stream_kernel<C>, prm);
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (dependent) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, prm);
 }
 
 static_assert(topk::pipe::kKMax == TOPK_K_MAX, "the pipelined kernel is sized for TOPK_K_MAX");
@@ -262,29 +276,27 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   const Plan pl = make_plan(*d, row_stride, num_rows, config);
   if (pl.grid <= 0) return TOPK_ERR_UNSUPPORTED;  // the split kernel cannot be resident here
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool dep = config && config->dependent_launch != 0;
   cudaError_t e;
   if (pl.path == TOPK_PATH_PIPE) {
-    topk::pipe::topk_pipe_kernel<<<(unsigned)pl.grid, topk::pipe::kBlock, sizeof(topk::pipe::PipeSmem), s>>>(prm);
-    e = cudaGetLastError();
+    e = launch(topk::pipe::topk_pipe_kernel, pl.grid, topk::pipe::kBlock, sizeof(topk::pipe::PipeSmem), 1, dep, s,
+               prm);
   } else if (pl.path == TOPK_PATH_SPLIT) {
-    topk::split::topk_split_kernel<<<(unsigned)pl.grid, topk::split::kBlockThreads, sizeof(topk::split::SplitSmem),
-                                     s>>>(prm);
-    e = cudaGetLastError();
+    e = launch(topk::split::topk_split_kernel, pl.grid, topk::split::kBlockThreads, sizeof(topk::split::SplitSmem), 1,
+               dep, s, prm);
   } else if (pl.path == TOPK_PATH_MULTIPASS) {
-    topk::topk_multipass_kernel<<<(unsigned)pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), s>>>(prm);
-    e = cudaGetLastError();
+    e = launch(topk::topk_multipass_kernel, pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), 1, dep, s,
+               prm);
   } else {
+    const size_t sm = sizeof(topk::StreamShared);
     switch (pl.cluster) {
-      case 1:
-        topk::topk_stream_kernel<1><<<(unsigned)pl.grid, topk::kStreamThreads, sizeof(topk::StreamShared), s>>>(prm);
-        e = cudaGetLastError();
-        break;
-      case 2: e = launch_stream<2>(prm, pl.grid, s); break;
-      case 4: e = launch_stream<4>(prm, pl.grid, s); break;
-      default: e = launch_stream<8>(prm, pl.grid, s); break;
+      case 1: e = launch(topk::topk_stream_kernel<1>, pl.grid, topk::kStreamThreads, sm, 1, dep, s, prm); break;
+      case 2: e = launch(topk::topk_stream_kernel<2>, pl.grid, topk::kStreamThreads, sm, 2, dep, s, prm); break;
+      case 4: e = launch(topk::topk_stream_kernel<4>, pl.grid, topk::kStreamThreads, sm, 4, dep, s, prm); break;
+      default: e = launch(topk::topk_stream_kernel<8>, pl.grid, topk::kStreamThreads, sm, 8, dep, s, prm); break;
     }
-    if (e == cudaSuccess) e = cudaGetLastError();
   }
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, TOPK_ERR_LAUNCH);
   return TOPK_OK;
 }

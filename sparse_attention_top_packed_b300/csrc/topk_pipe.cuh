@@ -1432,6 +1432,8 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     fence_barrier_init();
   }
   __syncthreads();
+  wait_for_producer();
+  allow_dependents();
   int64_t lo, hi;
   sched::balanced_range<kThreads>(p, blockIdx.x, gridDim.x, kPipeCostFloor, M.range, lo, hi);
   // each warp starts its ring

@@ -459,6 +459,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
   }
   if (lane == 0) fence_barrier_init();
   __syncthreads();
+  wait_for_producer();
+  allow_dependents();
   int64_t lo, hi;
   sched::balanced_range<kBlockThreads>(p, blockIdx.x, gridDim.x, kSplitCostFloor, M.range, lo, hi);
   const uint32_t* bits = M.range.bits;

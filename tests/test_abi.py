@@ -84,6 +84,10 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert _call(cfg=bad) == INVALID
     bad = binding.LaunchConfig(3, 0, 0, 0, 2)  # an unknown test flag
     assert _call(cfg=bad) == INVALID
+    bad = binding.LaunchConfig(3, 0, 0, 0, 0, 2)  # dependent_launch is 0 or 1
+    assert _call(cfg=bad) == INVALID
+    dep = binding.LaunchConfig(4, 0, 0, 0, 0, 1)
+    assert _call(cfg=dep, scores=0x1002) == UNSUPPORTED  # accepted; the next check answers
     known = binding.LaunchConfig(3, 0, 0, 1000, binding.TEST_UNSATISFIED_WAIT)
     assert _call(cfg=known, scores=0x1002) == UNSUPPORTED  # accepted; the next check answers
 

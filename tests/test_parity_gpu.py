@@ -353,3 +353,33 @@ def test_stream_wait_give_up_is_recorded_and_the_result_stays_exact(cuda_device,
     assert flags & 1, "the wait that nothing completes must be recorded as given up"
     assert np.array_equal(out.cpu().numpy(), want)
     assert np.array_equal(run(w, path=path).cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------------------
+# Dependent launch (page section 2: the top-k kernel waits on the grid that
+# produced its scores).  The producer lets its dependents start at once, waits
+# 100 us, then writes the real scores over a buffer holding their negation.
+# A top-k kernel that read a score before its wait returned would select from
+# the negated values.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("launch", [dict(path="split"), dict(path="pipe"), dict(path="multipass"),
+                                    dict(path="stream", cluster_size=2)], ids=["split", "pipe", "multipass", "stream2"])
+def test_dependent_launch_waits_for_the_producing_kernel(cuda_device, launch):
+    from sparse_attention_top_packed_b300.producer import produce_scores
+
+    rng = np.random.default_rng(5)
+    p = wl.random_problem(rng, rows=24, max_len=20000, k=2048, page_size=64, values="normal", slack=13)
+    w = host_problem_to_device(p, cuda_device)
+    real = w.scores.clone()
+    want = oracle_host(p)
+    stream = torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            w.scores.copy_(-real)
+        out = torch.full((w.num_rows, w.k), -7, dtype=torch.int32, device=cuda_device)
+        produce_scores(w.scores, real, delay_ns=100_000, stream=stream)
+        binding.topk_packed_ex(w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch, w.page_table,
+                               w.pt_stride, w.page_size, w.k, out, w.num_rows, dependent_launch=True,
+                               stream=stream, **launch)
+        stream.synchronize()
+        assert np.array_equal(out.cpu().numpy(), want)
