@@ -54,8 +54,11 @@ typedef enum {
   TOPK_ERR_DEVICE = 4       /* no usable sm_103a device, or a CUDA query failed */
 } topk_status_t;
 
-/* Largest k the library accepts. */
-#define TOPK_K_MAX 2048
+/* Largest k the library accepts.  Up to TOPK_K_FAST (the sizes the DSA
+ * configurations use) the single-pass kernels run; a larger k is served by the
+ * multipass kernel, which reads each window several times. */
+#define TOPK_K_MAX (1 << 20)
+#define TOPK_K_FAST 2048
 
 /*
  * topk_packed -- the operation above, launched asynchronously on `stream`.
@@ -90,7 +93,8 @@ typedef enum {
  *                         page_size <= 0 or not a power of two, or pt_stride < 0;
  *                         scores, seq_lens, row_starts or out NULL while num_rows > 0.
  *   TOPK_ERR_UNSUPPORTED  k > TOPK_K_MAX; scores not 4-byte aligned; with a page
- *                         table, page_size > 2^30.
+ *                         table, page_size > 2^30; (topk_packed_ex) a k above
+ *                         TOPK_K_FAST with the PIPE or SPLIT kernel chosen.
  *   TOPK_ERR_DEVICE       the current device is not sm_103a or cannot be queried.
  *   TOPK_ERR_LAUNCH       the kernel launch was rejected.
  * Thread safety: safe to call from several host threads; calls on different
@@ -105,8 +109,9 @@ TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, cons
 
 /* Kernel families behind topk_packed_ex. */
 typedef enum {
-  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: TOPK_PATH_SPLIT (TOPK_PATH_PIPE if the split
-                              kernel cannot be resident on the device) */
+  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: for k <= TOPK_K_FAST, TOPK_PATH_SPLIT
+                              (TOPK_PATH_PIPE if the split kernel cannot be resident on the device);
+                              for a larger k, TOPK_PATH_MULTIPASS */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
   TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
   TOPK_PATH_PIPE = 3,      /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over

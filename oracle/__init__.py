@@ -45,6 +45,12 @@ def _load():
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
             ctypes.c_int32, ctypes.c_int32,
         ]
+        lib.topk_oracle_typed.restype = ctypes.c_int
+        lib.topk_oracle_typed.argtypes = [
+            ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+            ctypes.c_int32, ctypes.c_int32,
+        ]
         lib.topk_oracle_default_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -59,18 +65,31 @@ def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
+DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
+
+
 def topk_packed_reference(scores, row_stride: int, seq_lens, row_starts, row_to_batch,
                           page_table, pt_stride: int, page_size: int, k: int,
-                          num_rows: int | None = None, nthreads: int = 0) -> np.ndarray:
+                          num_rows: int | None = None, nthreads: int = 0, dtype: str = "f32") -> np.ndarray:
     """Returns the [num_rows, k] int32 result of the definition for host arrays.
 
-    ``scores`` is a float32 array read at ``i*row_stride + row_starts[i] + j``;
+    ``scores`` is read at ``i*row_stride + row_starts[i] + j``: a float32
+    array (dtype "f32"), or the 16-bit patterns of bfloat16 ("bf16") or IEEE
+    binary16 ("f16") values as a uint16 (or float16) array;
     ``row_to_batch`` may be None (identity); ``page_table`` is read at
     ``b*pt_stride + page``, or is None for raw window indices (no page
     transform).  ``nthreads <= 0`` uses every online core.
     """
     lib = _load()
-    sc = np.ascontiguousarray(np.asarray(scores, dtype=np.float32)).reshape(-1)
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    if dtype == "f32":
+        sc = np.ascontiguousarray(np.asarray(scores, dtype=np.float32)).reshape(-1)
+    else:
+        a = np.asarray(scores)
+        if a.dtype not in (np.uint16, np.int16, np.float16):
+            raise ValueError("16-bit scores must be given as their bit patterns (uint16) or float16")
+        sc = np.ascontiguousarray(a.view(np.uint16)).reshape(-1)
     sl = _i32(seq_lens)
     rs = _i32(row_starts)
     rb = None if row_to_batch is None else _i32(row_to_batch)
@@ -83,7 +102,7 @@ def topk_packed_reference(scores, row_stride: int, seq_lens, row_starts, row_to_
     out = np.empty((n, k), dtype=np.int32)
     if pt is not None and pt.size == 0:
         pt = np.zeros(1, dtype=np.int32)
-    rc = lib.topk_oracle(sc.ctypes.data, int(row_stride), sl.ctypes.data, rs.ctypes.data,
+    rc = lib.topk_oracle_typed(sc.ctypes.data, DTYPES[dtype], int(row_stride), sl.ctypes.data, rs.ctypes.data,
                          None if rb is None else rb.ctypes.data, None if pt is None else pt.ctypes.data,
                          int(pt_stride),
                          int(page_size), int(k), out.ctypes.data, n, int(nthreads))

@@ -17,7 +17,7 @@ LIBRARY = os.path.join(HERE, "liboracle_topk.so")
 def build(source: str = SOURCE, output: str = LIBRARY, extra_flags: tuple[str, ...] = ()) -> str:
     """Compiles ``source`` with gcc into the shared library ``output`` and returns its path."""
     cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-shared", "-fPIC", "-pthread",
-           *extra_flags, source, "-o", output]
+           *extra_flags, source, "-o", output, "-lm"]
     subprocess.run(cmd, check=True)
     return output
 

@@ -36,11 +36,46 @@
  *   3. keep the first m = min(k, n) indices and sort them ascending;
  *   4. map each through the page transform; pad with -1 up to k.
  * NaN scores are outside the contract (the comparison order is undefined).
+ *
+ * Score buffers of 16-bit floats (bfloat16 or IEEE binary16) are read element
+ * by element and turned into their exact value as a float in step 1; every
+ * other step is the same.  Both formats' values are all exactly representable
+ * in binary32, so the order, the ties and the result are those of the same
+ * values stored as 32-bit floats.
  */
+#include <math.h>
 #include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 #include <unistd.h>
+
+/* Element types of the score buffer. */
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+
+/* bfloat16: the upper 16 bits of an IEEE binary32 pattern (sign, 8 exponent
+ * bits, 7 fraction bits); the lower 16 bits are zero. */
+static float bf16_value(uint16_t h) {
+  const uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* IEEE binary16: sign bit, 5 exponent bits with bias 15, 10 fraction bits.
+ * Exponent field 0: subnormal, fraction * 2^-24; field 31: infinity (fraction
+ * 0) or NaN; otherwise (1024 + fraction) * 2^(exponent - 15 - 10). */
+static float f16_value(uint16_t h) {
+  const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+  float mag;
+  if (e == 0)
+    mag = ldexpf((float)m, -24);
+  else if (e == 31)
+    mag = m == 0 ? INFINITY : NAN;
+  else
+    mag = ldexpf((float)(1024 + m), e - 25);
+  return sign ? -mag : mag;
+}
 
 typedef struct {
   float v;
@@ -48,7 +83,8 @@ typedef struct {
 } scored_index;
 
 typedef struct {
-  const float* scores;
+  const void* scores;
+  int32_t dtype; /* ORACLE_F32, ORACLE_BF16 or ORACLE_F16 */
   int64_t row_stride;
   const int32_t* seq_lens;
   const int32_t* row_starts;
@@ -84,9 +120,14 @@ static int32_t log2_exact(int32_t p) {
 /* One row, steps 1-4.  `work` holds at least n entries, `chosen` at least k. */
 static void oracle_row(const oracle_problem* p, int32_t i, scored_index* work, int32_t* chosen) {
   const int32_t n = p->seq_lens[i] > 0 ? p->seq_lens[i] : 0;
-  const float* window = p->scores + (int64_t)i * p->row_stride + p->row_starts[i];
+  const int64_t first = (int64_t)i * p->row_stride + p->row_starts[i];
   for (int32_t j = 0; j < n; ++j) {
-    work[j].v = window[j];
+    if (p->dtype == ORACLE_BF16)
+      work[j].v = bf16_value(((const uint16_t*)p->scores)[first + j]);
+    else if (p->dtype == ORACLE_F16)
+      work[j].v = f16_value(((const uint16_t*)p->scores)[first + j]);
+    else
+      work[j].v = ((const float*)p->scores)[first + j];
     work[j].j = j;
   }
   qsort(work, (size_t)n, sizeof(scored_index), by_score_desc_then_index);
@@ -134,22 +175,24 @@ static void* oracle_worker(void* varg) {
 }
 
 /*
- * Computes out[num_rows * k] for the problem above, rows split over
+ * Computes out[num_rows * k] for the problem above (scores of element type
+ * `dtype`), rows split over
  * `nthreads` POSIX threads (<= 0: one per online core).  All pointers are
  * host memory; page_table may be NULL (raw window indices, page_size and
  * pt_stride unused).  Returns 0 on success, -1 on invalid arguments (k <= 0,
  * with a page table: page_size not a positive power of two; negative sizes),
  * -2 when memory for the per-thread work arrays cannot be had.
  */
-int topk_oracle(const float* scores, int64_t row_stride, const int32_t* seq_lens,
-                const int32_t* row_starts, const int32_t* row_to_batch, const int32_t* page_table,
-                int64_t pt_stride, int32_t page_size, int32_t k, int32_t* out, int32_t num_rows,
-                int32_t nthreads) {
+int topk_oracle_typed(const void* scores, int32_t dtype, int64_t row_stride, const int32_t* seq_lens,
+                      const int32_t* row_starts, const int32_t* row_to_batch, const int32_t* page_table,
+                      int64_t pt_stride, int32_t page_size, int32_t k, int32_t* out, int32_t num_rows,
+                      int32_t nthreads) {
   if (k <= 0 || num_rows < 0 || row_stride < 0) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
   if (page_table != NULL && (pt_stride < 0 || page_size <= 0 || (page_size & (page_size - 1)) != 0)) return -1;
   if (num_rows == 0) return 0;
 
-  oracle_problem p = {scores, row_stride, seq_lens, row_starts, row_to_batch,
+  oracle_problem p = {scores, dtype, row_stride, seq_lens, row_starts, row_to_batch,
                       page_table, pt_stride, page_size, k, out, num_rows};
   int64_t max_window = 0;
   for (int32_t i = 0; i < num_rows; ++i)
@@ -185,6 +228,15 @@ int topk_oracle(const float* scores, int64_t row_stride, const int32_t* seq_lens
   free(threads);
   free(args);
   return status;
+}
+
+/* The same for a buffer of 32-bit floats. */
+int topk_oracle(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                const int32_t* row_starts, const int32_t* row_to_batch, const int32_t* page_table,
+                int64_t pt_stride, int32_t page_size, int32_t k, int32_t* out, int32_t num_rows,
+                int32_t nthreads) {
+  return topk_oracle_typed(scores, ORACLE_F32, row_stride, seq_lens, row_starts, row_to_batch, page_table,
+                           pt_stride, page_size, k, out, num_rows, nthreads);
 }
 
 /* Number of threads topk_oracle uses when asked for <= 0. */

@@ -164,14 +164,20 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
 
 int cluster_index(int c) { return c == 2 ? 1 : c == 4 ? 2 : 3; }
 
-Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t num_rows,
+Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t k, int32_t num_rows,
                const topk_launch_config_t* cfg) {
   (void)row_stride;
   Plan pl;
   const int32_t want = cfg ? cfg->path : TOPK_PATH_AUTO;
   // the warp-specialised split kernel, whose stream never waits for the end
-  // of a row; the pipelined kernel when the split one cannot be resident
-  pl.path = want != TOPK_PATH_AUTO ? want : d.split_ctas_per_sm > 0 ? TOPK_PATH_SPLIT : TOPK_PATH_PIPE;
+  // of a row; the pipelined kernel when the split one cannot be resident; the
+  // multipass kernel for a k beyond the single-pass kernels' buffers
+  if (want != TOPK_PATH_AUTO)
+    pl.path = want;
+  else if (k > TOPK_K_FAST)
+    pl.path = TOPK_PATH_MULTIPASS;
+  else
+    pl.path = d.split_ctas_per_sm > 0 ? TOPK_PATH_SPLIT : TOPK_PATH_PIPE;
   pl.cluster = 1;
   if (pl.path == TOPK_PATH_PIPE) {
     const int64_t cap = (int64_t)d.sms * d.pipe_ctas_per_sm;
@@ -238,7 +244,7 @@ cudaError_t launch(Kernel kernel, int64_t grid, int threads, size_t smem, int cl
   return cudaLaunchKernelEx(&cfg, kernel, prm);
 }
 
-static_assert(topk::pipe::kKMax == TOPK_K_MAX, "the pipelined kernel is sized for TOPK_K_MAX");
+static_assert(topk::pipe::kKMax == TOPK_K_FAST, "the single-pass kernels are sized for TOPK_K_FAST");
 
 }  // namespace
 
@@ -273,8 +279,9 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   prm.stream_wait_ns = config ? config->stream_wait_ns : 0u;
   prm.test_flags = config ? config->test_flags : 0u;
 
-  const Plan pl = make_plan(*d, row_stride, num_rows, config);
+  const Plan pl = make_plan(*d, row_stride, k, num_rows, config);
   if (pl.grid <= 0) return TOPK_ERR_UNSUPPORTED;  // the split kernel cannot be resident here
+  if (k > TOPK_K_FAST && (pl.path == TOPK_PATH_PIPE || pl.path == TOPK_PATH_SPLIT)) return TOPK_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool dep = config && config->dependent_launch != 0;
   cudaError_t e;
@@ -317,8 +324,9 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
   if (st != TOPK_OK) return st;
   const DeviceInfo* d = device_info(st);
   if (!d) return st;
-  const Plan pl = make_plan(*d, row_stride, num_rows, config);
+  const Plan pl = make_plan(*d, row_stride, k, num_rows, config);
   if (pl.grid <= 0 && num_rows > 0) return TOPK_ERR_UNSUPPORTED;
+  if (k > TOPK_K_FAST && (pl.path == TOPK_PATH_PIPE || pl.path == TOPK_PATH_SPLIT)) return TOPK_ERR_UNSUPPORTED;
   if (path) *path = pl.path;
   if (cluster_size) *cluster_size = pl.cluster;
   if (grid_ctas) *grid_ctas = (int32_t)pl.grid;

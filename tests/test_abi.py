@@ -72,7 +72,7 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert _call(seq=None) == INVALID
     assert _call(starts=None) == INVALID
     assert _call(out=None) == INVALID
-    assert _call(k=2049) == UNSUPPORTED
+    assert _call(k=(1 << 20) + 1) == UNSUPPORTED
     assert _call(scores=0x1002) == UNSUPPORTED  # not 4-byte aligned
     # nothing to do: success without a device
     assert _call(num_rows=0, scores=None, seq=None, starts=None, table=None, out=None) == OK
@@ -100,9 +100,9 @@ def test_null_page_table_means_raw_indices_and_frees_page_arguments(lib):
     # a NULL table passes the pointer checks: the next check (alignment) answers
     assert _call(table=None, scores=0x1002) == UNSUPPORTED
     # page_size and pt_stride are ignored without a table, checked with one
-    assert _call(table=None, page_size=48, pt_stride=-5, k=2049) == UNSUPPORTED
-    assert _call(page_size=48, k=2049) == INVALID
-    assert _call(pt_stride=-5, k=2049) == INVALID
+    assert _call(table=None, page_size=48, pt_stride=-5, k=(1 << 20) + 1) == UNSUPPORTED
+    assert _call(page_size=48, k=(1 << 20) + 1) == INVALID
+    assert _call(pt_stride=-5, k=(1 << 20) + 1) == INVALID
     assert _call(table=None, num_rows=0, page_size=0) == OK
 
 

@@ -97,6 +97,25 @@ def test_oracle_matches_rank_on_ten_thousand_tiny_rows():
         rows_checked += p.num_rows
 
 
+def test_oracle_matches_rank_for_k_above_2048():
+    """k of 2049, 4096 and 5000 on windows of up to 6000 (so the selection is
+    neither trivial nor the whole window), against the closed-form rank."""
+    rng = np.random.default_rng(2049)
+    for k, values in [(2049, "normal"), (4096, "bf16"), (5000, "int")]:
+        p = random_problem(rng, rows=4, max_len=6000, k=k, page_size=64, values=values,
+                           forced_lens=[6000, 5999, k + 1, k - 1])
+        got = run_oracle(p)
+        for i in range(p.num_rows):
+            L = int(p.seq_lens[i])
+            base = i * p.row_stride + int(p.row_starts[i])
+            chosen = brute_force.select_by_rank_np(p.scores[base: base + L], k)
+            b = int(p.row_to_batch[i])
+            page_row = p.page_table[b * p.pt_stride:(b + 1) * p.pt_stride]
+            expect = [brute_force.page_slot(page_row, p.page_size, int(j)) for j in chosen]
+            expect += [-1] * (k - len(expect))
+            assert got[i].tolist() == expect, (k, values, i)
+
+
 def test_k_at_least_window_is_identity_selection():
     rng = np.random.default_rng(3)
     p = random_problem(rng, rows=30, max_len=200, k=256, page_size=16, values="normal")
@@ -281,3 +300,103 @@ def test_reversed_windows_mirror_the_selection_up_to_ties():
         m = min(L, 30)
         want = sorted(L - 1 - int(j) for j in raw[i, :m])
         assert rev[i, :m].tolist() == want and (rev[i, m:] == -1).all()
+
+
+# ---------------------------------------------------------------------------
+# 16-bit score buffers (bfloat16, IEEE binary16): the oracle turns each element
+# into its exact value first.  Pinned by hand-encoded examples, by the
+# libraries' own decoders (numpy float16, torch bfloat16) and by the
+# closed-form rank on tie-heavy rows with special values.
+# ---------------------------------------------------------------------------
+HALF_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "half_width_example.json")
+
+
+def test_half_width_golden_examples():
+    data = json.load(open(HALF_GOLDEN))
+    checked = 0
+    for ex in data["examples"]:
+        for dtype in ("bf16", "f16"):
+            if dtype not in ex:
+                continue
+            bits = np.array([int(h, 16) for h in ex[dtype]], dtype=np.uint16)
+            for case in ex["cases"]:
+                got = topk_packed_reference(bits, 0, [len(bits)], [0], None, np.array(ex["page_row"], np.int32),
+                                            0, ex["page_size"], case["k"], dtype=dtype)
+                assert got[0].tolist() == case["expected"], (ex["name"], dtype, case)
+                checked += 1
+    assert checked >= 10
+
+
+def _half_problem(rng, dtype, rows=16, max_len=300, k=None):
+    """Random 16-bit patterns (no NaN) in ragged windows; cells outside the
+    windows hold the pattern of +inf."""
+    stride = max_len + 5
+    inf = 0x7C00 if dtype == "f16" else 0x7F80
+    bits = np.full(rows * stride, inf, dtype=np.uint16)
+    seq = rng.integers(0, max_len + 1, size=rows).astype(np.int32)
+    starts = np.array([rng.integers(0, stride - L + 1) for L in seq], dtype=np.int32)
+    for i in range(rows):
+        L = int(seq[i])
+        b = rng.integers(0, 1 << 16, size=L).astype(np.uint16)
+        # NaN patterns (exponent all ones, fraction non-zero) become the
+        # infinity of the same sign: NaN is outside the contract
+        frac = 0x03FF if dtype == "f16" else 0x007F
+        nan = ((b & (0x7FFF ^ frac)) == (0x7FFF ^ frac)) & ((b & frac) != 0)
+        b[nan] &= np.uint16(0xFFFF ^ frac)
+        # a few repeated values to make ties
+        if L > 4:
+            b[rng.integers(0, L, size=L // 4)] = b[rng.integers(0, L)]
+        bits[i * stride + starts[i]: i * stride + starts[i] + L] = b
+    table = rng.choice(1 << 20, size=4 * (-(-stride // 16)), replace=False).astype(np.int32)
+    rtb = rng.integers(0, 4, size=rows).astype(np.int32)
+    kk = int(k if k is not None else rng.integers(1, max_len))
+    return bits, stride, seq, starts, rtb, table, -(-stride // 16), 16, kk
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_f16_buffer_equals_numpy_float16_values(seed):
+    """numpy's float16 decoder (a library routine) against the oracle's own."""
+    rng = np.random.default_rng(seed)
+    bits, stride, seq, starts, rtb, table, pts, ps, k = _half_problem(rng, "f16")
+    as_f32 = bits.view(np.float16).astype(np.float32)
+    a = topk_packed_reference(bits, stride, seq, starts, rtb, table, pts, ps, k, dtype="f16")
+    b = topk_packed_reference(as_f32, stride, seq, starts, rtb, table, pts, ps, k)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("seed", [4, 5, 6])
+def test_bf16_buffer_equals_torch_bfloat16_values(seed):
+    """torch's bfloat16 decoder (a library routine) against the oracle's own."""
+    import torch
+
+    rng = np.random.default_rng(seed)
+    bits, stride, seq, starts, rtb, table, pts, ps, k = _half_problem(rng, "bf16")
+    as_f32 = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    a = topk_packed_reference(bits, stride, seq, starts, rtb, table, pts, ps, k, dtype="bf16")
+    b = topk_packed_reference(as_f32, stride, seq, starts, rtb, table, pts, ps, k)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_half_width_oracle_matches_rank(dtype):
+    """The closed-form rank on rows of 16-bit values drawn from a tie-heavy set
+    with signed zeros, infinities, subnormals and the extremes (values decoded
+    by the libraries), against the oracle reading the bit patterns."""
+    import torch
+
+    if dtype == "f16":
+        pool = np.array([0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x3C00, 0xBC00, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00,
+                         0x3C01], dtype=np.uint16)
+        decode = lambda b: b.view(np.float16).astype(np.float64)
+    else:
+        pool = np.array([0x0000, 0x8000, 0x0001, 0x007F, 0x0080, 0x3F80, 0xBF80, 0x7F7F, 0xFF7F, 0x7F80, 0xFF80,
+                         0x3F81], dtype=np.uint16)
+        decode = lambda b: torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    rng = np.random.default_rng(99)
+    for trial in range(200):
+        n = int(rng.integers(0, 40))
+        k = int(rng.integers(1, 44))
+        b = pool[rng.integers(0, pool.shape[0], size=n)]
+        got = topk_packed_reference(b, 0, [n], [0], None, None, 0, 1, k, dtype=dtype)[0].tolist()
+        chosen = brute_force.select_by_rank_np(decode(b), k).tolist()
+        assert got == chosen + [-1] * (k - len(chosen)), (dtype, trial)

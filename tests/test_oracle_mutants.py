@@ -44,6 +44,17 @@ MUTANTS = {
 }
 
 
+# planted mistakes in the decoding of 16-bit buffers (each changes the order
+# of some values, so a correct pin must notice)
+HALF_MUTANTS = {
+    "binary16 subnormals decoded as normals": ("if (e == 0)\n    mag = ldexpf((float)m, -24);\n  else if",
+                                               "if (0)\n    mag = ldexpf((float)m, -24);\n  else if"),
+    "binary16 exponent field misread": ("e = (h >> 10) & 31", "e = (h >> 11) & 31"),
+    "bfloat16 pattern shifted one bit short": ("(uint32_t)h << 16", "(uint32_t)h << 15"),
+}
+HALF_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "half_width_example.json")
+
+
 def _compile(tmp_path, name, find, replace):
     src = open(oracle_build.SOURCE).read()
     assert src.count(find) == 1, f"mutation site for {name!r} not found exactly once"
@@ -52,6 +63,11 @@ def _compile(tmp_path, name, find, replace):
     lib_path = str(tmp_path / (name.replace(" ", "_") + ".so"))
     oracle_build.build(str(path), lib_path, extra_flags=("-w",))
     lib = ctypes.CDLL(lib_path)
+    lib.topk_oracle_typed.restype = ctypes.c_int
+    lib.topk_oracle_typed.argtypes = [
+        ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+        ctypes.c_int32, ctypes.c_int32]
     lib.topk_oracle.restype = ctypes.c_int
     lib.topk_oracle.argtypes = [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -114,3 +130,57 @@ def test_mutant_is_caught(tmp_path, name):
     find, replace = MUTANTS[name]
     lib = _compile(tmp_path, name, find, replace)
     assert not _passes_pins(lib), f"pins did not catch the planted mistake: {name}"
+
+
+def _passes_half_pins(lib) -> bool:
+    """The 16-bit pins of test_oracle.py: the hand-encoded examples and the
+    libraries' decoders."""
+    import torch
+
+    def call(bits, dtype, page_row, page_size, k):
+        b = np.ascontiguousarray(bits, dtype=np.uint16)
+        pt = np.ascontiguousarray(page_row, dtype=np.int32)
+        sl = np.array([b.shape[0]], np.int32)
+        rs = np.zeros(1, np.int32)
+        out = np.full((1, k), 12345, dtype=np.int32)
+        lib.topk_oracle_typed(b.ctypes.data, {"bf16": 1, "f16": 2}[dtype], 0, sl.ctypes.data, rs.ctypes.data, None,
+                              pt.ctypes.data, 0, page_size, k, out.ctypes.data, 1, 1)
+        return out[0].tolist()
+
+    data = json.load(open(HALF_GOLDEN))
+    for ex in data["examples"]:
+        for dtype in ("bf16", "f16"):
+            if dtype in ex:
+                bits = [int(h, 16) for h in ex[dtype]]
+                for case in ex["cases"]:
+                    if call(bits, dtype, ex["page_row"], ex["page_size"], case["k"]) != case["expected"]:
+                        return False
+    rng = np.random.default_rng(5)
+    for dtype in ("f16", "bf16"):
+        for _ in range(20):
+            n = int(rng.integers(1, 60))
+            b = rng.integers(0, 1 << 16, size=n).astype(np.uint16)
+            if dtype == "f16":
+                b = b[((b >> 10) & 31) != 31]
+                vals = b.view(np.float16).astype(np.float64)
+            else:
+                b = b[((b >> 7) & 255) != 255]
+                vals = torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+            k = int(rng.integers(1, n + 2))
+            want = brute_force.select_by_rank_np(vals, k).tolist()
+            want = want + [-1] * (k - len(want))
+            if call(b, dtype, np.arange(max(len(b), 1)), 1, k) != want:
+                return False
+    return True
+
+
+def test_unmutated_source_passes_half_width_pins(tmp_path):
+    lib = _compile(tmp_path, "clean_half", "int topk_oracle_typed(", "int topk_oracle_typed(")
+    assert _passes_half_pins(lib)
+
+
+@pytest.mark.parametrize("name", sorted(HALF_MUTANTS))
+def test_half_width_mutant_is_caught(tmp_path, name):
+    find, replace = HALF_MUTANTS[name]
+    lib = _compile(tmp_path, name, find, replace)
+    assert not _passes_half_pins(lib), f"pins did not catch the planted mistake: {name}"

@@ -383,3 +383,22 @@ def test_dependent_launch_waits_for_the_producing_kernel(cuda_device, launch):
                                stream=stream, **launch)
         stream.synchronize()
         assert np.array_equal(out.cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------------------
+# k above the single-pass kernels' size (2048): the automatic choice is the
+# multipass kernel; the stream kernel also serves it; pipe and split refuse.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("k", [2049, 4096, 10000])
+def test_large_k(cuda_device, k):
+    rng = np.random.default_rng(k + 17)
+    p = wl.random_problem(rng, rows=12, max_len=30000, k=k, page_size=64, values="bf16", slack=11,
+                          forced_lens=[30000, 20000, k + 1, k, k - 1, 0, 12345, 29999, min(4 * k, 30000), 1, 7777, 25000])
+    w = host_problem_to_device(p, cuda_device)
+    want = oracle_host(p)
+    assert binding.topk_packed_plan(w.row_stride, k, w.num_rows)["path"] == binding.PATHS["multipass"]
+    assert np.array_equal(run(w).cpu().numpy(), want)
+    assert np.array_equal(run(w, path="stream", cluster_size=2).cpu().numpy(), want)
+    for path in ("pipe", "split"):
+        with pytest.raises(binding.TopkError):
+            run(w, path=path)
