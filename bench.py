@@ -146,22 +146,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_workload(name: str, device, rows: int = 0):
+def make_workload(name: str, device, rows: int = 0, dtype: str = "f32"):
     from sparse_attention_top_packed_b300 import workloads
 
     w = workloads.named(name, device=device)
-    return w.head(rows) if rows else w
+    w = w.head(rows) if rows else w
+    return w if dtype == "f32" else workloads.with_dtype(w, dtype)
 
 
 def l2_flush_buffer(device):
     return torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
 
 
-def make_launch(path: str):
-    """The timed call: topk_packed (the automatic choice) or topk_packed_ex with
-    an explicit kernel family."""
+def make_launch(path: str, dtype: str = "f32"):
+    """The timed call: topk_packed (the automatic choice), topk_packed_ex with
+    an explicit kernel family, or topk_packed_typed for a 16-bit buffer."""
     from sparse_attention_top_packed_b300 import binding
 
+    if dtype != "f32":
+        return lambda args, stream: binding.topk_packed_typed(args[0], dtype, *args[1:], path=path, stream=stream)
     if path == "auto":
         return lambda args, stream: binding.topk_packed(*args, stream=stream)
     return lambda args, stream: binding.topk_packed_ex(*args, path=path, stream=stream)
@@ -189,12 +192,12 @@ def run_ours(a, rank: int, world: int, device) -> dict:
     from sparse_attention_top_packed_b300 import binding
 
     torch.cuda.set_device(device)
-    w = make_workload(a.workload, device, a.rows)
+    w = make_workload(a.workload, device, a.rows, a.dtype)
     torch.cuda.synchronize(device)
     alg_bytes = w.algorithmic_bytes()
     big = w.window_bytes() > 4 * L2_BYTES
     flush = not big
-    launch = make_launch(a.path)
+    launch = make_launch(a.path, a.dtype)
     args, stream, scratch, starts, ends = prepare_timing(w, a.steps, a.warmup, flush, device, launch)
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -263,12 +266,13 @@ def run_e2e(a, w, device) -> dict:
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * 4
 
+    launch = make_launch(a.path, a.dtype)
+
     def step():
         for n in host:
             dev[n].copy_(host[n], non_blocking=True)
-        binding.topk_packed(dev["scores"], w.row_stride, dev["seq_lens"], dev["row_starts"],
-                            dev.get("row_to_batch"), dev["page_table"], w.pt_stride, w.page_size,
-                            w.k, out_dev, w.num_rows, stream=stream)
+        launch((dev["scores"], w.row_stride, dev["seq_lens"], dev["row_starts"], dev.get("row_to_batch"),
+                dev["page_table"], w.pt_stride, w.page_size, w.k, out_dev, w.num_rows), stream)
         out_host.copy_(out_dev, non_blocking=True)
 
     step()
@@ -387,7 +391,7 @@ def run_reference(a, rank: int, world: int) -> None:
     from oracle import default_threads
 
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    w = make_workload(a.workload, device, a.rows)
+    w = make_workload(a.workload, device, a.rows, a.dtype)
     cores = default_threads()
     avg_row_bytes = max(w.window_bytes_all() / max(w.num_rows, 1), 4.0)
     rows_per_step = int(min(w.num_rows, max(16 * cores, (512 << 20) // avg_row_bytes)))
@@ -403,7 +407,7 @@ def run_reference(a, rank: int, world: int) -> None:
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": a.gpus,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": config_block(a, w, None),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
                          "sample": f"the same {rows_per_step} of {w.num_rows} rows every step, one call each"},
@@ -417,7 +421,8 @@ METRIC = "packed top-k rows/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
 
 
 def config_block(a, w, plan) -> dict:
-    d = {"workload": WORKLOAD_TEXT[a.workload], "rows": w.num_rows, "row_stride": w.row_stride,
+    d = {"workload": WORKLOAD_TEXT[a.workload] + ("" if w.dtype == "f32" else f", scores held as {w.dtype}"),
+         "rows": w.num_rows, "row_stride": w.row_stride,
          "k": w.k, "page_size": w.page_size,
          "window_bytes_per_step": w.window_bytes(), "output_bytes_per_step": w.output_bytes(),
          "l2": ("inputs larger than L2: each step reads %.2f GB, no flush" % (w.window_bytes() / 1e9))
@@ -441,6 +446,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "pipe", "split", "stream", "multipass"],
                     help="kernel family (auto: the choice topk_packed makes)")
+    ap.add_argument("--dtype", default="f32", choices=["f32", "bf16", "f16"],
+                    help="element type of the score buffer (16-bit: the values rounded to it)")
     ap.add_argument("--pdl-gap", action="store_true",
                     help="time producer + top-k pairs with and without the dependent launch instead")
     a = ap.parse_args()
@@ -476,7 +483,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": r["step_ms"], "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded N(0,1) scores, distinct random pages)",
             "config": config_block(a, w, plan),
             "achieved_hbm_gbs": achieved,

@@ -161,6 +161,33 @@ TOPK_API topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, c
                              int32_t k, int32_t* out, int32_t num_rows,
                              const topk_launch_config_t* config, topk_stream_t stream);
 
+/* Element types of a score buffer (topk_packed_typed). */
+typedef enum {
+  TOPK_F32 = 0,  /* IEEE binary32 (float), as in topk_packed */
+  TOPK_BF16 = 1, /* bfloat16: the upper 16 bits of a binary32 */
+  TOPK_F16 = 2   /* IEEE binary16 (half) */
+} topk_dtype_t;
+
+/*
+ * topk_packed_typed -- topk_packed_ex on a score buffer of `dtype` elements
+ * (topk_dtype_t): element (i, c) at ((const T*)scores)[i * row_stride + c],
+ * row_stride and row_starts counted in elements.  A 16-bit buffer halves the
+ * bytes read; the selection is that of the same values held as 32-bit floats
+ * (every bfloat16 and binary16 value is exactly a binary32 value; -0.0 and
+ * +0.0 are equal; NaN outside the contract).  The page's TopKPackedParams
+ * (section 1) declares the buffer as float*; the 16-bit types are this
+ * library's extension.
+ * Extra errors: TOPK_ERR_INVALID_ARG for an unknown dtype; TOPK_ERR_UNSUPPORTED
+ * for scores not aligned to the element size, and, for a 16-bit dtype, a k
+ * above TOPK_K_FAST or a kernel family other than AUTO and SPLIT.
+ */
+TOPK_API topk_status_t topk_packed_typed(const void* scores, int32_t dtype, int64_t row_stride,
+                                         const int32_t* seq_lens, const int32_t* row_starts,
+                                         const int32_t* row_to_batch, const int32_t* page_table,
+                                         int64_t pt_stride, int32_t page_size, int32_t k, int32_t* out,
+                                         int32_t num_rows, const topk_launch_config_t* config,
+                                         topk_stream_t stream);
+
 /*
  * topk_packed_plan -- the launch topk_packed_ex would make for these sizes,
  * without launching: path, cluster size, grid (in CTAs) and threads per CTA.

@@ -61,6 +61,8 @@ def _load():
     lib.topk_packed.argtypes = common + [vp]
     lib.topk_packed_ex.restype = ctypes.c_int
     lib.topk_packed_ex.argtypes = common + [ctypes.POINTER(LaunchConfig), vp]
+    lib.topk_packed_typed.restype = ctypes.c_int
+    lib.topk_packed_typed.argtypes = [vp, i32] + common[1:] + [ctypes.POINTER(LaunchConfig), vp]
     lib.topk_packed_plan.restype = ctypes.c_int
     lib.topk_packed_plan.argtypes = [i64, i32, i32, ctypes.POINTER(LaunchConfig)] + \
         [ctypes.POINTER(ctypes.c_int32)] * 4
@@ -133,6 +135,22 @@ def topk_packed_ex(scores, row_stride: int, seq_lens, row_starts, row_to_batch, 
     _check(st, "topk_packed_ex")
 
 
+DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
+
+
+def topk_packed_typed(scores, dtype: str, row_stride: int, seq_lens, row_starts, row_to_batch, page_table,
+                      pt_stride: int, page_size: int, k: int, out, num_rows: int, path="auto",
+                      cluster_size: int = 0, max_ctas: int = 0, dependent_launch: bool = False,
+                      stream=None) -> None:
+    """topk_packed_ex on a buffer of `dtype` ("f32", "bf16", "f16") elements."""
+    lib = _load()
+    cfg = _config(path, cluster_size, max_ctas, 0, 0, dependent_launch)
+    st = lib.topk_packed_typed(_ptr(scores), DTYPES[dtype], int(row_stride), _ptr(seq_lens), _ptr(row_starts),
+                               _ptr(row_to_batch), _ptr(page_table), int(pt_stride), int(page_size), int(k),
+                               _ptr(out), int(num_rows), ctypes.byref(cfg), _stream_handle(stream))
+    _check(st, "topk_packed_typed")
+
+
 def topk_packed_plan(row_stride: int, k: int, num_rows: int, path="auto", cluster_size: int = 0,
                      max_ctas: int = 0) -> dict:
     lib = _load()
@@ -169,6 +187,10 @@ def run_workload(w, out=None, stream=None, **launch) -> "object":
 
     if out is None:
         out = torch.empty((w.num_rows, w.k), dtype=torch.int32, device=w.scores.device)
+    if w.scores.dtype != torch.float32:
+        topk_packed_typed(w.scores, w.dtype, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch,
+                          w.page_table, w.pt_stride, w.page_size, w.k, out, w.num_rows, stream=stream, **launch)
+        return out
     topk_packed_ex(w.scores, w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch,
                    w.page_table, w.pt_stride, w.page_size, w.k, out, w.num_rows,
                    stream=stream, **launch)

@@ -19,6 +19,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace topk {
@@ -93,6 +94,58 @@ __device__ __forceinline__ float key_floor_float(uint32_t key) {
 // The float at the lower edge of level-1 bin b:
 //   x >= edge_float(b)  <=>  key(x) >= (b << 20)   for every non-NaN x.
 __device__ __forceinline__ float edge_float(uint32_t b) { return key_floor_float(b << kShift1); }
+
+// ---------------------------------------------------------------------------
+// Element types of the score buffer (the page's `float* scores`, or a 16-bit
+// buffer of the same values).  A 16-byte quad holds kPerQuad elements; decode
+// gives their exact values as floats -- every bfloat16 and binary16 value is a
+// binary32 value -- so keys, order and ties are those of the same values
+// stored as 32-bit floats.  bits_at gives the binary32 pattern of element e of
+// a run of elements.
+// ---------------------------------------------------------------------------
+struct ElemF32 {
+  static constexpr int kPerQuad = 4, kBytes = 4;
+  __device__ __forceinline__ static void decode(const float4& q, float (&x)[4]) {
+    x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+  }
+  __device__ __forceinline__ static uint32_t bits_at(const void* run, int e) {
+    return static_cast<const uint32_t*>(run)[e];
+  }
+};
+
+// bfloat16: the upper half of a binary32 pattern.
+struct ElemBF16 {
+  static constexpr int kPerQuad = 8, kBytes = 2;
+  __device__ __forceinline__ static float value(uint32_t h) { return __uint_as_float(h << 16); }
+  __device__ __forceinline__ static void decode(const float4& q, float (&x)[8]) {
+    const uint32_t w[4] = {__float_as_uint(q.x), __float_as_uint(q.y), __float_as_uint(q.z), __float_as_uint(q.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);            // element 2i: the low half (little endian)
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ static uint32_t bits_at(const void* run, int e) {
+    return (uint32_t)static_cast<const uint16_t*>(run)[e] << 16;
+  }
+};
+
+// IEEE binary16, decoded by the CUDA conversion.
+struct ElemF16 {
+  static constexpr int kPerQuad = 8, kBytes = 2;
+  __device__ __forceinline__ static float value(uint32_t h) { return __half2float(__ushort_as_half((unsigned short)h)); }
+  __device__ __forceinline__ static void decode(const float4& q, float (&x)[8]) {
+    const uint32_t w[4] = {__float_as_uint(q.x), __float_as_uint(q.y), __float_as_uint(q.z), __float_as_uint(q.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = value(w[i] & 0xFFFFu);
+      x[2 * i + 1] = value(w[i] >> 16);
+    }
+  }
+  __device__ __forceinline__ static uint32_t bits_at(const void* run, int e) {
+    return __float_as_uint(value(static_cast<const uint16_t*>(run)[e]));
+  }
+};
 
 // ---------------------------------------------------------------------------
 // Row addressing (section 1 and section 2 of the page).  The window start is

@@ -92,12 +92,21 @@ void init_device(int dev) {
   if (e == cudaSuccess) {
     // the split kernel is optional: if it cannot be made resident, its path
     // reports TOPK_ERR_UNSUPPORTED and the others are unaffected
-    const size_t split_smem = sizeof(topk::split::SplitSmem);
-    cudaError_t es = cudaFuncSetAttribute(topk::split::topk_split_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)split_smem);
+    using topk::ElemBF16;
+    using topk::ElemF16;
+    using topk::ElemF32;
+    using topk::split::SplitSmem;
+    cudaError_t es = cudaFuncSetAttribute(topk::split::topk_split_kernel<ElemF32>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SplitSmem<ElemF32>));
     if (es == cudaSuccess)
-      es = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.split_ctas_per_sm, topk::split::topk_split_kernel,
-                                                         topk::split::kBlockThreads, split_smem);
+      es = cudaFuncSetAttribute(topk::split::topk_split_kernel<ElemBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(SplitSmem<ElemBF16>));
+    if (es == cudaSuccess)
+      es = cudaFuncSetAttribute(topk::split::topk_split_kernel<ElemF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(SplitSmem<ElemF16>));
+    if (es == cudaSuccess)
+      es = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.split_ctas_per_sm, topk::split::topk_split_kernel<ElemBF16>,
+                                                         topk::split::kBlockThreads, sizeof(SplitSmem<ElemBF16>));
     if (es != cudaSuccess) {
       d.split_ctas_per_sm = 0;
       (void)cudaGetLastError();  // clear it: the other kernels stay usable
@@ -250,22 +259,26 @@ static_assert(topk::pipe::kKMax == TOPK_K_FAST, "the single-pass kernels are siz
 
 extern "C" {
 
-topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int32_t* seq_lens,
-                             const int32_t* row_starts, const int32_t* row_to_batch,
-                             const int32_t* page_table, int64_t pt_stride, int32_t page_size,
-                             int32_t k, int32_t* out, int32_t num_rows,
-                             const topk_launch_config_t* config, topk_stream_t stream) {
+topk_status_t topk_packed_typed(const void* scores, int32_t dtype, int64_t row_stride, const int32_t* seq_lens,
+                                const int32_t* row_starts, const int32_t* row_to_batch,
+                                const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                                int32_t k, int32_t* out, int32_t num_rows,
+                                const topk_launch_config_t* config, topk_stream_t stream) {
   g_last_cuda_error = 0;
+  if (dtype != TOPK_F32 && dtype != TOPK_BF16 && dtype != TOPK_F16) return TOPK_ERR_INVALID_ARG;
   topk_status_t st = check_sizes(row_stride, pt_stride, page_size, k, num_rows, config, page_table != nullptr);
   if (st != TOPK_OK) return st;
+  const bool half = dtype != TOPK_F32;
+  const int32_t want = config ? config->path : TOPK_PATH_AUTO;
+  if (half && ((want != TOPK_PATH_AUTO && want != TOPK_PATH_SPLIT) || k > TOPK_K_FAST)) return TOPK_ERR_UNSUPPORTED;
   if (num_rows == 0) return TOPK_OK;
   if (!scores || !seq_lens || !row_starts || !out) return TOPK_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(scores) & 3u) != 0) return TOPK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(scores) & (half ? 1u : 3u)) != 0) return TOPK_ERR_UNSUPPORTED;
   const DeviceInfo* d = device_info(st);
   if (!d) return st;
 
   Params prm;
-  prm.scores = scores;
+  prm.scores = static_cast<const float*>(scores);  // element type: dtype
   prm.row_stride = row_stride;
   prm.seq_lens = seq_lens;
   prm.row_starts = row_starts;
@@ -282,6 +295,7 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   const Plan pl = make_plan(*d, row_stride, k, num_rows, config);
   if (pl.grid <= 0) return TOPK_ERR_UNSUPPORTED;  // the split kernel cannot be resident here
   if (k > TOPK_K_FAST && (pl.path == TOPK_PATH_PIPE || pl.path == TOPK_PATH_SPLIT)) return TOPK_ERR_UNSUPPORTED;
+  if (half && pl.path != TOPK_PATH_SPLIT) return TOPK_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool dep = config && config->dependent_launch != 0;
   cudaError_t e;
@@ -289,8 +303,15 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
     e = launch(topk::pipe::topk_pipe_kernel, pl.grid, topk::pipe::kBlock, sizeof(topk::pipe::PipeSmem), 1, dep, s,
                prm);
   } else if (pl.path == TOPK_PATH_SPLIT) {
-    e = launch(topk::split::topk_split_kernel, pl.grid, topk::split::kBlockThreads, sizeof(topk::split::SplitSmem), 1,
-               dep, s, prm);
+    using topk::split::SplitSmem;
+    using topk::split::topk_split_kernel;
+    const int nt = topk::split::kBlockThreads;
+    if (dtype == TOPK_BF16)
+      e = launch(topk_split_kernel<topk::ElemBF16>, pl.grid, nt, sizeof(SplitSmem<topk::ElemBF16>), 1, dep, s, prm);
+    else if (dtype == TOPK_F16)
+      e = launch(topk_split_kernel<topk::ElemF16>, pl.grid, nt, sizeof(SplitSmem<topk::ElemF16>), 1, dep, s, prm);
+    else
+      e = launch(topk_split_kernel<topk::ElemF32>, pl.grid, nt, sizeof(SplitSmem<topk::ElemF32>), 1, dep, s, prm);
   } else if (pl.path == TOPK_PATH_MULTIPASS) {
     e = launch(topk::topk_multipass_kernel, pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), 1, dep, s,
                prm);
@@ -306,6 +327,15 @@ topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int3
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, TOPK_ERR_LAUNCH);
   return TOPK_OK;
+}
+
+topk_status_t topk_packed_ex(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                             const int32_t* row_starts, const int32_t* row_to_batch,
+                             const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                             int32_t k, int32_t* out, int32_t num_rows,
+                             const topk_launch_config_t* config, topk_stream_t stream) {
+  return topk_packed_typed(scores, TOPK_F32, row_stride, seq_lens, row_starts, row_to_batch, page_table, pt_stride,
+                           page_size, k, out, num_rows, config, stream);
 }
 
 topk_status_t topk_packed(const float* scores, int64_t row_stride, const int32_t* seq_lens,

@@ -437,17 +437,41 @@ __device__ __noinline__ void compact(Shared& S, uint32_t n, uint32_t k, int atte
   cbar();
 }
 
-// Exact mode's view of a chunk of kChunkQuads quads: the thread's quads 2h and
-// 2h + 1 (8 floats) of half h, read from global memory.
+// Exact mode reads a chunk from global memory as two halves of 8 elements a
+// thread: with 32-bit elements a thread's quads 2h and 2h + 1 (kThreads
+// apart), with 16-bit ones its quad h.  A chunk is exact_chunk_quads<E>()
+// quads.
+template <class E>
+__device__ __forceinline__ constexpr int64_t exact_chunk_quads() {
+  return (int64_t)kThreads * 2 * (8 / E::kPerQuad);
+}
+
+template <class E>
 __device__ __forceinline__ void take_half(const Row& r, int64_t nq, int64_t cq, int h, float x[8]) {
-  float4 v[2];
+  if constexpr (E::kPerQuad == 4) {
+    float4 v[2];
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int64_t q = cq + threadIdx.x + (2 * h + u) * kThreads;
-    v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < 2; ++u) {
+      const int64_t q = cq + threadIdx.x + (2 * h + u) * kThreads;
+      v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    x[0] = v[0].x; x[1] = v[0].y; x[2] = v[0].z; x[3] = v[0].w;
+    x[4] = v[1].x; x[5] = v[1].y; x[6] = v[1].z; x[7] = v[1].w;
+  } else {
+    const int64_t q = cq + threadIdx.x + h * kThreads;
+    const float4 v = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float y[8];
+    E::decode(v, y);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = y[e];
   }
-  x[0] = v[0].x; x[1] = v[0].y; x[2] = v[0].z; x[3] = v[0].w;
-  x[4] = v[1].x; x[5] = v[1].y; x[6] = v[1].z; x[7] = v[1].w;
+}
+
+// Window index of the thread's element 0 of half h of the chunk at quad cq.
+template <class E>
+__device__ __forceinline__ int64_t half_first_index(const Row& r, int64_t cq, int h) {
+  if constexpr (E::kPerQuad == 4) return (cq + threadIdx.x) * 4 - r.head + (int64_t)h * 8 * kThreads;
+  return (cq + threadIdx.x + (int64_t)h * kThreads) * 8 - r.head;
 }
 
 // x[e] for a run-time e in [0, 8), as a tree of selects (indexing the array
@@ -459,15 +483,19 @@ __device__ __forceinline__ float pick8(const float x[8], int e) {
   return (e & 4) ? hi : lo;
 }
 
-// Window index of element e of 8 consecutive x whose first element has index
-// jb0: elements 0-3 are one quad (index jb0 + e), elements 4-7 the quad
-// kThreads further on (index jb0 + 4 * kThreads + e - 4).
+// Window index of element e of a half whose element 0 has index jb0.  With
+// 32-bit elements, elements 0-3 are one quad (index jb0 + e) and 4-7 the quad
+// kThreads further on (index jb0 + 4 * kThreads + e - 4); with 16-bit ones
+// the 8 elements are one quad.
+template <class E>
 __device__ __forceinline__ int32_t index8(int64_t jb0, int e) {
-  return (int32_t)(jb0 + (e & 3) + ((e & 4) ? 4 * kThreads : 0));
+  if constexpr (E::kPerQuad == 4) return (int32_t)(jb0 + (e & 3) + ((e & 4) ? 4 * kThreads : 0));
+  return (int32_t)(jb0 + e);
 }
 
-// Bit e set when element e of 8 consecutive x (laid out as index8) passes
-// `rule` and lies in the window [0, L).
+// Bit e set when element e of a half (laid out as index8) passes `rule` and
+// lies in the window [0, L).
+template <class E>
 __device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8], int64_t jb0, bool edge,
                                                int32_t L) {
   uint32_t m = 0u;
@@ -477,7 +505,7 @@ __device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8
     uint32_t valid = 0u;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int64_t j = jb0 + (e & 3) + ((e & 4) ? 4 * kThreads : 0);
+      const int64_t j = index8<E>(jb0, e);
       valid |= (j >= 0 && j < L ? 1u : 0u) << e;
     }
     m &= valid;
@@ -485,20 +513,21 @@ __device__ __forceinline__ uint32_t admit_mask(const Rule& rule, const float x[8
   if (rule.exact && m) {
     for (uint32_t mm = m; mm; mm &= mm - 1u) {
       const int e = __ffs(mm) - 1;
-      if (!rule_pass(rule, key_of(pick8(x, e)), index8(jb0, e))) m &= ~(1u << e);
+      if (!rule_pass(rule, key_of(pick8(x, e)), index8<E>(jb0, e))) m &= ~(1u << e);
     }
   }
   return m;
 }
 
-// Exact mode: appends the flagged elements (8 consecutive x) at pos, pos+1, ...
-// and counts them in the histogram of the key's top 11 bits (hist2).
+// Exact mode: appends the flagged elements of a half at pos, pos+1, ... and
+// counts them in the histogram of the key's top 11 bits (hist2).
+template <class E>
 __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, uint32_t pos, int64_t jb0) {
   for (uint32_t mm = m; mm; mm &= mm - 1u) {
     const int e = __ffs(mm) - 1;
     const uint32_t key = key_of(pick8(x, e));
     S.bkey[pos] = key;
-    S.bj[pos] = index8(jb0, e);
+    S.bj[pos] = index8<E>(jb0, e);
     ++pos;
     atomicAdd(&S.hist2[key >> 21], 1u);
   }
@@ -508,20 +537,22 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
 // threshold starting at -inf; the buffer (one shared region, kCap entries) is
 // compacted whenever a half chunk would overflow it.  One block-wide vote per
 // half chunk.  For rows whose fast pass failed (rare).
+template <class E = ElemF32>
 __device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const Row r, int64_t nq) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t k = (uint32_t)p.k;
-  const int64_t nch = (nq + kChunkQuads - 1) / kChunkQuads;
+  constexpr int64_t kCQ = exact_chunk_quads<E>();
+  const int64_t nch = (nq + kCQ - 1) / kCQ;
   Rule rule = S.rule;
   for (int64_t c = 0; c < nch; ++c) {
-    const int64_t cq = c * kChunkQuads;
+    const int64_t cq = c * kCQ;
     const bool edge = c == 0 || c == nch - 1;
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       float xh[8];
-      take_half(r, nq, cq, h, xh);
-      const int64_t jb0 = (cq + tid) * 4 - r.head + (int64_t)h * 8 * kThreads;
-      uint32_t m = admit_mask(rule, xh, jb0, edge, r.L);
+      take_half<E>(r, nq, cq, h, xh);
+      const int64_t jb0 = half_first_index<E>(r, cq, h);
+      uint32_t m = admit_mask<E>(rule, xh, jb0, edge, r.L);
       uint32_t pos;
       for (int attempt = 0;; ++attempt) {
         const uint32_t n = __popc(m);
@@ -545,10 +576,10 @@ __device__ __noinline__ void stream_row_exact(Shared& S, const Params& p, const 
         rule = S.rule;
         for (uint32_t mm = m; mm; mm &= mm - 1u) {
           const int e = __ffs(mm) - 1;
-          if (!rule_pass(rule, key_of(pick8(xh, e)), index8(jb0, e))) m &= ~(1u << e);
+          if (!rule_pass(rule, key_of(pick8(xh, e)), index8<E>(jb0, e))) m &= ~(1u << e);
         }
       }
-      append(S, xh, m, pos, jb0);
+      append<E>(S, xh, m, pos, jb0);
     }
   }
 }
@@ -645,11 +676,24 @@ __device__ __forceinline__ RowRaw load_row_raw(const Params& p, int64_t row) {
   return x;
 }
 
+// Address of element `col` of buffer row `row` (elements of type E).
+template <class E = ElemF32>
+__device__ __forceinline__ uintptr_t elem_addr(const Params& p, int64_t row, int64_t col) {
+  return reinterpret_cast<uintptr_t>(p.scores) + (uintptr_t)((row * p.row_stride + col) * E::kBytes);
+}
+
+// Quads of 16 bytes that hold the window of r (from its rounded-down start).
+template <class E = ElemF32>
+__device__ __forceinline__ int64_t quads_of(const Row& r) {
+  return ((int64_t)r.L + r.head + E::kPerQuad - 1) / E::kPerQuad;
+}
+
+template <class E = ElemF32>
 __device__ __forceinline__ Row make_row(const Params& p, int64_t row, const RowRaw& x) {
   Row r;
   r.L = x.L > 0 ? x.L : 0;
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + x.start);
-  r.head = (int32_t)((a & 15u) >> 2);
+  const uintptr_t a = elem_addr<E>(p, row, x.start);
+  r.head = (int32_t)((a & 15u) / E::kBytes);
   r.base4 = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
   r.page_row = p.page_table ? p.page_table + (int64_t)x.table_row * p.pt_stride : nullptr;
   return r;
@@ -785,15 +829,16 @@ __device__ __forceinline__ void deferred_flush(Deferred& d, int32_t page_bits) {
 // are not refilled, so no stage ever holds two copies in flight; the kernel's
 // exit waits for what is left.  Such a warp marks each of its rows as
 // overflowed, so they are finished exactly from global memory.
-template <int NS, int NW, int CQ, class AfterChunk>
+template <int NS, int NW, int CQ, class E = ElemF32, class AfterChunk>
 __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, int w, const Row& r, int64_t nq,
                                               uint32_t& g, bool& timed_out, uint64_t limit_ns,
                                               AfterChunk&& after_chunk) {
   static_assert(NW == kWarps || NW <= kMaxStreamWarps, "streaming warps");
   constexpr int QPL = CQ / 32;  // quads per lane: 8 (4 KB chunks) or 16 (8 KB chunks)
-  static_assert(QPL == 8 || QPL == 16, "chunk size");
-  using Mask = typename std::conditional<QPL == 8, uint32_t, uint64_t>::type;
-  constexpr int kBits = 4 * QPL;   // elements per lane per chunk
+  constexpr int EPQ = E::kPerQuad;
+  constexpr int kBits = EPQ * QPL;  // elements per lane per chunk
+  static_assert((QPL == 8 || QPL == 16) && kBits <= 64, "chunk size");
+  using Mask = typename std::conditional<kBits <= 32, uint32_t, uint64_t>::type;
   constexpr int kReg = kCap / NW;  // this warp's region
   const int lane = threadIdx.x & 31;
   int64_t q0, q1;
@@ -813,32 +858,34 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
       break;
     }
     const float4* st = R.st[w][s];
-    // the lane's kBits consecutive floats; bit 4u+c of mr is element 4*((u+rot)%QPL)+c
+    // the lane's kBits consecutive elements; bit EPQ*u+c of mr is element
+    // EPQ*((u+rot)%QPL)+c
     Mask mr = 0u;
 #pragma unroll
     for (int u = 0; u < QPL; ++u) {
       const float4 v = st[QPL * lane + ((u + rot) & (QPL - 1))];
-      if (v.x >= tf) mr |= (Mask)1u << (4 * u);
-      if (v.y >= tf) mr |= (Mask)2u << (4 * u);
-      if (v.z >= tf) mr |= (Mask)4u << (4 * u);
-      if (v.w >= tf) mr |= (Mask)8u << (4 * u);
+      float x[EPQ];
+      E::decode(v, x);
+#pragma unroll
+      for (int c = 0; c < EPQ; ++c)
+        if (x[c] >= tf) mr |= (Mask)1u << (EPQ * u + c);
     }
-    // bit e: element e of the lane's kBits (rotate left by 4 rot)
-    Mask m = rot == 0 ? mr : (Mask)((mr << (4 * rot)) | (mr >> (kBits - 4 * rot)));
+    // bit e: element e of the lane's kBits (rotate left by EPQ rot)
+    Mask m = rot == 0 ? mr : (Mask)((mr << (EPQ * rot)) | (mr >> (kBits - EPQ * rot)));
     // window index of the lane's element 0 (window indices fit in 32 bits;
     // lanes before the window start get negative ones, masked below)
-    const int32_t jb = (int32_t)((cq + QPL * lane) * 4 - r.head);
+    const int32_t jb = (int32_t)((cq + QPL * lane) * EPQ - r.head);
     if (cq == 0 || cq + CQ >= q1) {  // the row's first or the block's last chunk
       // keep the window [0, L) and the block's quads [.., q1) (the rest of a
       // partial chunk's stage is stale)
       const int64_t lo = max(-(int64_t)jb, (int64_t)0);
-      const int64_t hi = min(min((int64_t)r.L - jb, (q1 - cq - QPL * lane) * 4), (int64_t)kBits);
+      const int64_t hi = min(min((int64_t)r.L - jb, (q1 - cq - QPL * lane) * EPQ), (int64_t)kBits);
       const Mask below_hi = hi >= kBits ? ~(Mask)0 : (((Mask)1 << (hi > 0 ? hi : 0)) - 1u);
       const Mask from_lo = lo >= kBits ? (Mask)0 : ~(((Mask)1 << lo) - 1u);
       m &= lo >= hi ? (Mask)0 : (below_hi & from_lo);
     }
     if (!full) {
-      const uint32_t n = (uint32_t)(QPL == 8 ? __popc((uint32_t)m) : __popcll((unsigned long long)m));
+      const uint32_t n = (uint32_t)(kBits <= 32 ? __popc((uint32_t)m) : __popcll((unsigned long long)m));
       const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, n);
       if (tot != 0u) {
         if (wcnt + tot > (uint32_t)kReg) {
@@ -846,26 +893,28 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
           if (lane == 0) S.overflow = 1u;
         } else {
           // exclusive prefix of n over the lanes, from the bits of n (the
-          // low three suffice unless a lane admitted 8 or more)
+          // low three suffice unless a lane admitted 8 or more; n <= kBits
+          // needs up to 6 bits for 32 elements a lane, 7 for 64)
+          constexpr int kCountBits = kBits <= 32 ? 6 : 7;
           uint32_t pos = wcnt;
 #pragma unroll
           for (int b = 0; b < 3; ++b)
             pos += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (n >> b) & 1u) & lt) << b;
           if (__any_sync(0xFFFFFFFFu, n >= 8u)) {
 #pragma unroll
-            for (int b = 3; b < (QPL == 8 ? 6 : 7); ++b)
+            for (int b = 3; b < kCountBits; ++b)
               pos += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (n >> b) & 1u) & lt) << b;
           }
-          const uint32_t* sf = reinterpret_cast<const uint32_t*>(st) + kBits * lane;
+          const void* sf = reinterpret_cast<const char*>(st) + 16 * QPL * lane;  // the lane's elements
           // ascending e: window order within the lane; two at a time, so the
           // two loads are in flight together
           Mask mm = m;
           while (mm) {
-            const int e0 = (int)(QPL == 8 ? __ffs((uint32_t)mm) : __ffsll((unsigned long long)mm)) - 1;
+            const int e0 = (int)(kBits <= 32 ? __ffs((uint32_t)mm) : __ffsll((unsigned long long)mm)) - 1;
             mm &= mm - 1u;
-            const int e1 = (int)(QPL == 8 ? __ffs((uint32_t)mm) : __ffsll((unsigned long long)mm)) - 1;
-            const uint32_t x0 = sf[e0];
-            const uint32_t x1 = e1 >= 0 ? sf[e1] : 0u;
+            const int e1 = (int)(kBits <= 32 ? __ffs((uint32_t)mm) : __ffsll((unsigned long long)mm)) - 1;
+            const uint32_t x0 = E::bits_at(sf, e0);
+            const uint32_t x1 = e1 >= 0 ? E::bits_at(sf, e1) : 0u;
             rraw[pos] = x0;
             rj[pos] = jb + e0;
             if (e1 >= 0) {
@@ -1329,8 +1378,10 @@ constexpr int kSamples = 4096;
 static_assert(kSamples <= kCap, "the sample is kept in the candidate buffer");
 static_assert(2 * kBins2 <= kCap, "the second digit's histograms use the index buffer");
 
+template <class E = ElemF32>
 __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const Row r, int64_t nq) {
-  constexpr int kSampleQuads = kSamples / 4;
+  constexpr int EPQ = E::kPerQuad;
+  constexpr int kSampleQuads = kSamples / EPQ;
   constexpr int U = kSampleQuads / kThreads;
   const int t = threadIdx.x;
   uint32_t* h1a = reinterpret_cast<uint32_t*>(S.bj);  // second digit under the rank-R digit
@@ -1346,12 +1397,13 @@ __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const 
   for (int u = 0; u < U; ++u) {
     const int s = t + u * kThreads;
     const int64_t q = ((2 * (int64_t)s + 1) * nq) / (2 * kSampleQuads);
-    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+    float f[EPQ];
+    E::decode(v[u], f);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int64_t j = q * 4 - r.head + e;
+    for (int e = 0; e < EPQ; ++e) {
+      const int64_t j = q * EPQ - r.head + e;
       const uint32_t key = (j >= 0 && j < r.L) ? key_of(f[e]) : 0u;
-      S.bkey[4 * s + e] = key;
+      S.bkey[EPQ * s + e] = key;
       atomicAdd(&S.hist2[key >> 21], 1u);
     }
   }
@@ -1367,8 +1419,8 @@ __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const 
 #pragma unroll
   for (int u = 0; u < U; ++u)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t key = S.bkey[4 * (t + u * kThreads) + e];  // this thread's own entries
+    for (int e = 0; e < EPQ; ++e) {
+      const uint32_t key = S.bkey[EPQ * (t + u * kThreads) + e];  // this thread's own entries
       const uint32_t d = key >> 21;
       if (d == a.bin)
         atomicAdd(&h1a[(key >> 10) & (kBins2 - 1)], 1u);

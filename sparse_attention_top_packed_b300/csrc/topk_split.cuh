@@ -48,8 +48,13 @@ namespace split {
 using namespace topk::pipe;
 
 constexpr int kSW = 8;                       // streaming warps (8 or 16)
-constexpr int kSChunk = 512;                 // quads per stage: 8 KB, 64 floats a lane
-constexpr int kStages = 16 / kSW;            // their ring depth: 128 KB in flight
+// Stage size and ring depth per element type: 64 elements a lane per chunk,
+// 128 KB in flight per SM.  32-bit: 8 KB stages, 2 of them; 16-bit: 4 KB, 4.
+template <class E>
+struct Shape {
+  static constexpr int kChunk = 16 * 32 * 4 / E::kPerQuad;  // quads per stage
+  static constexpr int kStages = (131072 / kSW) / (16 * kChunk);
+};
 constexpr int kBlockThreads = kThreads + kSW * 32;  // 8 finishing warps, then the streaming warps
 constexpr int kPart = kCap / kSW;            // buffer entries of one streaming warp
 // Register split (setmaxnreg, per warpgroup of 128 threads): launched with
@@ -82,8 +87,10 @@ struct PageStage {
   int32_t staged;  // the row the set is prepared for reads its pages from the stage
 };
 
+template <class E>
 struct SplitSmem {
-  pipe::Ring<kStages, kSW, kSChunk> ring;
+  using RingT = pipe::Ring<Shape<E>::kStages, kSW, Shape<E>::kChunk>;
+  RingT ring;
   pipe::Shared set[2];
   int32_t pages[2][kPageStage];
   SetRow srow[2];
@@ -166,13 +173,14 @@ __device__ __forceinline__ void scursor_init(SCursor& c, const Params& p, int64_
 
 // Moves to the block of row c.nrow and loads the descriptor of the row after
 // it (used at the next move).  False past the last row.
+template <class E>
 __device__ __forceinline__ bool scursor_advance(SCursor& c, const Params& p, int w) {
   if (c.nrow >= c.hi) return false;
   const int64_t row = c.nrow;
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + c.nstart);
-  const int32_t head = (int32_t)((a & 15u) >> 2);
+  const uintptr_t a = elem_addr<E>(p, row, c.nstart);
+  const int32_t head = (int32_t)((a & 15u) / E::kBytes);
   int64_t q0, q1;
-  warp_block_of<kSW>(((int64_t)c.nL + head + 3) >> 2, w, q0, q1);
+  warp_block_of<kSW>(((int64_t)c.nL + head + E::kPerQuad - 1) / E::kPerQuad, w, q0, q1);
   c.src = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u) + q0;
   c.left = (int32_t)(q1 - q0);
   c.nrow = sched::next_selected_row(p, c.bits, c.lo, c.hi, row + 1);
@@ -185,12 +193,14 @@ __device__ __forceinline__ bool scursor_advance(SCursor& c, const Params& p, int
 
 // Whole warp: lane 0 issues the warp's next chunk into stage issued % kStages
 // (whose previous chunk the warp has taken and fenced).  False past the last row.
-__device__ __forceinline__ bool scursor_issue(pipe::Ring<kStages, kSW, kSChunk>& R, SCursor& c, const Params& p, int w,
+template <class E>
+__device__ __forceinline__ bool scursor_issue(typename SplitSmem<E>::RingT& R, SCursor& c, const Params& p, int w,
                                               uint64_t policy) {
+  constexpr int kStages = Shape<E>::kStages, kChunk = Shape<E>::kChunk;
   while (c.left == 0)
-    if (!scursor_advance(c, p, w)) return false;
+    if (!scursor_advance<E>(c, p, w)) return false;
   const uint32_t s = c.issued % kStages;
-  const uint32_t nquads = (uint32_t)min(kSChunk, c.left);
+  const uint32_t nquads = (uint32_t)min(kChunk, c.left);
   if ((threadIdx.x & 31) == 0) {
     mbar_arrive_expect_tx(&R.full[w][s], nquads * 16u);
     bulk_copy_g2s(&R.st[w][s][0], c.src, nquads * 16u, &R.full[w][s], policy);
@@ -209,7 +219,8 @@ __device__ __forceinline__ bool scursor_issue(pipe::Ring<kStages, kSW, kSChunk>&
 // of set b by its previous row: prepares set b for row R (descriptor d), or
 // marks it as the end when R >= hi.  Thread 0 then arrives on set_free[b]
 // (done by the caller).  Ends with a finishing barrier.
-__device__ __forceinline__ void prepare_set(SplitSmem& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
+template <class E>
+__device__ __forceinline__ void prepare_set(SplitSmem<E>& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
                                             int64_t hi) {
   pipe::Shared& S = M.set[b];
   if (R >= hi) {
@@ -217,9 +228,9 @@ __device__ __forceinline__ void prepare_set(SplitSmem& M, uint32_t b, const Para
     pipe::cbar();
     return;
   }
-  const Row r = make_row(p, R, d);
-  const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
-  const bool small = nq * 4 <= kPart;  // every element fits its streaming warp's part
+  const Row r = make_row<E>(p, R, d);
+  const int64_t nq = quads_of<E>(r);
+  const bool small = r.L + r.head <= kPart;  // every element fits its streaming warp's part
   if (threadIdx.x == 0) {
     const bool hinted = !small && S.hint_valid != 0u;  // thread 0's own write
     S.sample = (!small && !hinted) ? 1u : 0u;
@@ -275,7 +286,7 @@ __device__ __forceinline__ void prepare_set(SplitSmem& M, uint32_t b, const Para
   for (int i = threadIdx.x; i < pipe::kBins2 / 4; i += kThreads)
     reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0u, 0u, 0u, 0u);
   pipe::cbar();
-  if (S.sample != 0u) pipe::sample_threshold(S, p, r, nq);  // ends with a barrier, hist2 zero
+  if (S.sample != 0u) pipe::sample_threshold<E>(S, p, r, nq);  // ends with a barrier, hist2 zero
 }
 
 // Finishing warp w (whole warp): streaming warps 2w and 2w + 1 filled parts
@@ -317,13 +328,14 @@ __device__ __forceinline__ void merge_parts(pipe::Shared& S) {
 // of the row set b serves next (0: none), the target of the hint; `parity`
 // the phase of page_full[b] that stages R's pages.  Ends with a finishing
 // barrier.
-__device__ __forceinline__ void finish_row(SplitSmem& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
+template <class E>
+__device__ __forceinline__ void finish_row(SplitSmem<E>& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
                                            int32_t next_len, uint32_t parity, bool& timed_out) {
   pipe::Shared& S = M.set[b];
   const int tid = threadIdx.x;
   const uint32_t k = (uint32_t)p.k;
-  const Row r = make_row(p, R, d);
-  const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
+  const Row r = make_row<E>(p, R, d);
+  const int64_t nq = quads_of<E>(r);
   if constexpr (kSW > kWarps) merge_parts(S);
   pipe::keys_and_histogram(S);
   if (tid == 0) {
@@ -363,7 +375,7 @@ __device__ __forceinline__ void finish_row(SplitSmem& M, uint32_t b, const Param
       S.rule = pipe::rule_all();
     }
     pipe::cbar();
-    pipe::stream_row_exact(S, p, r, nq);
+    pipe::stream_row_exact<E>(S, p, r, nq);
     pipe::cbar();
     n = S.count;
     pipe::set_regions_contiguous(S, n);
@@ -435,9 +447,11 @@ __device__ __forceinline__ void wait_emitting(uint64_t* bar, uint32_t parity, bo
   wait_bounded(bar, parity, timed_out);
 }
 
+template <class E>
 __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  SplitSmem& M = *reinterpret_cast<SplitSmem*>(smem_raw);
+  SplitSmem<E>& M = *reinterpret_cast<SplitSmem<E>*>(smem_raw);
+  constexpr int kStages = Shape<E>::kStages;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool finishing = warp < kWarps;
   bool timed_out = false;
@@ -520,16 +534,17 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
     const int sw = warp - kWarps;
     const uint64_t policy = l2_evict_first_policy();
     scursor_init(cur, p, lo, hi, bits);
-    for (int s = 0; s < kStages; ++s) scursor_issue(M.ring, cur, p, sw, policy);
+    for (int s = 0; s < kStages; ++s) scursor_issue<E>(M.ring, cur, p, sw, policy);
     test_unsatisfied_wait(p, &M.never, timed_out);
     for (uint32_t s = 0;; ++s) {
       const uint32_t b = s & 1u;
       wait_bounded(&M.set_free[b], (s >> 1) & 1u, timed_out);
       const SetRow sr = M.srow[b];
       if (sbar_or(sr.row >= hi || sr.row < lo)) break;  // uniform over the streaming warps
-      const Row r = make_row(p, sr.row, RowRaw{sr.L, sr.start, sr.trow});
-      const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
-      stream_row_wb(M.set[b], M.ring, sw, r, nq, g, timed_out, stream_wait_limit(p), [&] { scursor_issue(M.ring, cur, p, sw, policy); });
+      const Row r = make_row<E>(p, sr.row, RowRaw{sr.L, sr.start, sr.trow});
+      const int64_t nq = quads_of<E>(r);
+      stream_row_wb<kStages, kSW, Shape<E>::kChunk, E>(M.set[b], M.ring, sw, r, nq, g, timed_out, stream_wait_limit(p),
+                                                      [&] { scursor_issue<E>(M.ring, cur, p, sw, policy); });
       sbar();  // every streaming warp has written its region
       if (tid == kThreads) mbar_arrive(&M.set_full[b]);
     }

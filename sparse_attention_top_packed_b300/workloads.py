@@ -60,13 +60,22 @@ class Workload:
     k: int
     num_rows: int
 
+    @property
+    def dtype(self) -> str:
+        """Element type of the score buffer: "f32", "bf16" or "f16"."""
+        return {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[self.scores.dtype]
+
+    @property
+    def elem_bytes(self) -> int:
+        return self.scores.element_size()
+
     def window_bytes(self) -> int:
         """Bytes of the windows that must be read: rows with seq_len <= k need no scores."""
         L = self.seq_lens.to(torch.int64).clamp_min(0)
-        return int((L * (L > self.k)).sum().item()) * 4
+        return int((L * (L > self.k)).sum().item()) * self.elem_bytes
 
     def window_bytes_all(self) -> int:
-        return int(self.seq_lens.to(torch.int64).clamp_min(0).sum().item()) * 4
+        return int(self.seq_lens.to(torch.int64).clamp_min(0).sum().item()) * self.elem_bytes
 
     def output_bytes(self) -> int:
         return self.num_rows * self.k * 4
@@ -94,6 +103,15 @@ class Workload:
         if self.row_to_batch is None:
             return torch.arange(self.num_rows, dtype=torch.int32, device=self.seq_lens.device)
         return self.row_to_batch
+
+
+def with_dtype(w: Workload, dtype: str) -> Workload:
+    """The same problem with the score buffer held as `dtype` ("f32", "bf16",
+    "f16"): each value rounded to the nearest of the type (ties to even), by
+    torch's conversion.  The layout, lengths, offsets and tables are shared."""
+    t = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    return Workload(w.name, w.scores.to(t), w.row_stride, w.seq_lens, w.row_starts, w.row_to_batch,
+                    w.page_table, w.pt_stride, w.page_size, w.k, w.num_rows)
 
 
 def distinct_pages(rows: int, cols: int, seed: int) -> torch.Tensor:
@@ -240,7 +258,7 @@ def gather_windows(w: Workload, rows: torch.Tensor, chunk: int = 256):
         base = r * w.row_stride + starts[a:a + chunk]
         valid = ar[None, :] < L[a:a + chunk, None]
         idx = torch.where(valid, base[:, None] + ar[None, :], torch.zeros_like(base[:, None]))
-        vals = flat[idx]
+        vals = flat[idx].float()
         vals = torch.where(valid, vals, torch.full_like(vals, float("inf")))
         out[a:a + r.numel()] = vals.cpu().numpy()
     return out, L.cpu().numpy().astype(np.int32)

@@ -111,3 +111,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(binding.TopkError):
         binding.topk_status_string(0)
+
+
+def _typed(dtype, scores=0x1000, k=8, cfg=None):
+    args = [scores, dtype, 16, 0x2000, 0x3000, None, 0x4000, 1, 64, k, 0x5000, 1]
+    return binding.raw_call("topk_packed_typed", *args, None if cfg is None else ctypes.byref(cfg), None)
+
+
+def test_typed_entry_point_checks(lib):
+    INVALID, UNSUPPORTED = 1, 2
+    assert _typed(3) == INVALID  # unknown element type
+    assert _typed(-1) == INVALID
+    assert _typed(1, scores=0x1001) == UNSUPPORTED  # bf16 needs 2-byte alignment
+    assert _typed(2, k=2049) == UNSUPPORTED         # 16-bit buffers: k <= TOPK_K_FAST
+    for path in (1, 2, 3):                           # 16-bit buffers: split kernel only
+        assert _typed(1, cfg=binding.LaunchConfig(path, 0, 0)) == UNSUPPORTED
+    assert _typed(0, scores=0x1002) == UNSUPPORTED  # f32 needs 4-byte alignment

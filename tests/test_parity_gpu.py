@@ -402,3 +402,93 @@ def test_large_k(cuda_device, k):
     for path in ("pipe", "split"):
         with pytest.raises(binding.TopkError):
             run(w, path=path)
+
+
+# ---------------------------------------------------------------------------
+# 16-bit score buffers (bfloat16, IEEE binary16).  The oracle reads the same
+# bit patterns; ragged windows at every element offset (a 16-byte quad holds 8
+# elements, so the head runs 0..7), odd strides, tie-heavy and special values.
+# ---------------------------------------------------------------------------
+def _half_host_problem(rng, dtype, rows, max_len, k, values):
+    p = wl.random_problem(rng, rows=rows, max_len=max_len, k=k, page_size=64, values=values, slack=29)
+    t = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    half = torch.from_numpy(p.scores).to(t)  # rounded to the type; +inf outside the windows stays +inf
+    return p, half
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("values,rows,max_len,k", [("normal", 24, 20000, 2048), ("ties", 30, 9000, 300),
+                                                   ("int", 16, 20000, 2048), ("normal", 40, 5000, 1),
+                                                   ("bf16", 50, 3000, 32), ("equal", 8, 10000, 2048),
+                                                   ("ascending", 10, 25000, 2048)])
+def test_half_width_random_problems(cuda_device, dtype, values, rows, max_len, k):
+    rng = np.random.default_rng(zlib.crc32(f"{dtype}-{values}-{max_len}-{k}".encode()))
+    p, half = _half_host_problem(rng, dtype, rows, max_len, k, values)
+    w = wl.Workload("random", half.to(cuda_device).reshape(rows, p.row_stride), p.row_stride,
+                    torch.from_numpy(p.seq_lens).to(cuda_device), torch.from_numpy(p.row_starts).to(cuda_device),
+                    torch.from_numpy(p.row_to_batch).to(cuda_device), torch.from_numpy(p.page_table).to(cuda_device),
+                    p.pt_stride, p.page_size, p.k, rows)
+    before = w.scores.clone()
+    out = run(w)
+    assert torch.equal(before, w.scores), "the score buffer was written"
+    bits = half.view(torch.int16).numpy().view(np.uint16)
+    want = topk_packed_reference(bits, p.row_stride, p.seq_lens, p.row_starts, p.row_to_batch, p.page_table,
+                                 p.pt_stride, p.page_size, p.k, dtype=dtype)
+    assert np.array_equal(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_half_width_edge_lengths_offsets_and_specials(cuda_device, dtype):
+    """Every element offset mod 8, an odd stride, lengths around k and around
+    the chunk sizes, signed zeros, infinities and (binary16) subnormals."""
+    k = 64
+    lens = [0, 1, k - 1, k, k + 1, 2047, 2048, 2049, 8191, 8193, 3 * 2048 * 8 + 5, -3]
+    rng = np.random.default_rng(31)
+    rows = [(L, off) for L in lens for off in range(8)]
+    n = len(rows)
+    stride = max(L for L, _ in rows) + 11
+    stride += 1 - stride % 2
+    vals = np.full(n * stride, np.inf, dtype=np.float32)
+    seq = np.zeros(n, np.int32)
+    st = np.zeros(n, np.int32)
+    for i, (L, off) in enumerate(rows):
+        Lp = max(L, 0)
+        v = rng.standard_normal(Lp).astype(np.float32)
+        if Lp > 10:
+            v[rng.integers(0, Lp, size=Lp // 10)] = -0.0
+            v[rng.integers(0, Lp, size=Lp // 10)] = 0.0
+            v[rng.integers(0, Lp, size=3)] = np.inf
+            v[rng.integers(0, Lp, size=3)] = -np.inf
+            v[rng.integers(0, Lp, size=5)] = 3e-7  # a binary16 subnormal
+        seq[i] = L
+        st[i] = off + (i % 3)
+        vals[i * stride + st[i]: i * stride + st[i] + Lp] = v
+    t = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    half = torch.from_numpy(vals).to(t)
+    pages = -(-stride // 16)
+    table = rng.choice(1 << 24, size=n * pages, replace=False).astype(np.int32)
+    w = wl.Workload("edge", half.to(cuda_device).reshape(n, stride), stride, torch.from_numpy(seq).to(cuda_device),
+                    torch.from_numpy(st).to(cuda_device), None, torch.from_numpy(table).to(cuda_device), pages, 16,
+                    k, n)
+    bits = half.view(torch.int16).numpy().view(np.uint16)
+    want = topk_packed_reference(bits, stride, seq, st, None, table, pages, 16, k, dtype=dtype)
+    assert np.array_equal(run(w).cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "long", "mixed"])
+def test_bf16_buffer_gives_the_fp32_result_on_bf16_values(cuda_device, name):
+    """Every configuration with its scores rounded to bfloat16: the bf16 buffer
+    (half the bytes) must give the bits of the fp32 buffer holding the same
+    values (the mixed configuration's values are bf16 already), and the
+    oracle's result on sampled rows."""
+    w32 = wl.named(name, device=cuda_device)
+    w16 = wl.with_dtype(w32, "bf16")
+    del w32
+    w32 = wl.with_dtype(w16, "f32")  # the bf16 values, held as fp32
+    out16 = run(w16)
+    out32 = run(w32)
+    assert torch.equal(out16, out32)
+    rows = sample_rows(w16.num_rows, 192)
+    want = oracle_rows(w16, rows)
+    got = out16[rows.to(out16.device)].cpu().numpy()
+    assert np.array_equal(got, want)
