@@ -199,6 +199,15 @@ def run_ours(a, rank: int, world: int, device) -> dict:
     flush = not big
     launch = make_launch(a.path, a.dtype)
     args, stream, scratch, starts, ends = prepare_timing(w, a.steps, a.warmup, flush, device, launch)
+    if a.graph:
+        # the launch captured once in a CUDA graph; the timed steps replay it
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            launch(args, torch.cuda.current_stream(device))
+        for _ in range(a.warmup):
+            graph.replay()
+        torch.cuda.synchronize(device)
+        launch = lambda args_, stream_: graph.replay()  # noqa: E731
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -416,7 +425,8 @@ def run_reference(a, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
-KERNEL_NAMES = {1: "topk_multipass_kernel", 2: "topk_stream_kernel", 3: "topk_pipe_kernel", 4: "topk_split_kernel"}
+KERNEL_NAMES = {1: "topk_multipass_kernel", 2: "topk_stream_kernel", 3: "topk_pipe_kernel", 4: "topk_split_kernel",
+                5: "topk_decode_kernel"}
 METRIC = "packed top-k rows/s and achieved HBM GB/s (% of B300 peak), 1 GPU"
 
 
@@ -430,6 +440,8 @@ def config_block(a, w, plan) -> dict:
          "parallelism": f"dp{a.gpus} (independent replicas of the batch)"}
     if plan is not None:
         d["launch"] = plan
+    if getattr(a, "graph", False):
+        d["timing"] = "each step replays a CUDA graph holding the launch"
     return d
 
 
@@ -444,10 +456,12 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="keep only the first N rows of the workload (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="auto", choices=["auto", "pipe", "split", "stream", "multipass"],
+    ap.add_argument("--path", default="auto", choices=["auto", "pipe", "split", "stream", "multipass", "decode"],
                     help="kernel family (auto: the choice topk_packed makes)")
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16", "f16"],
                     help="element type of the score buffer (16-bit: the values rounded to it)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the launch in a CUDA graph and time graph replays")
     ap.add_argument("--pdl-gap", action="store_true",
                     help="time producer + top-k pairs with and without the dependent launch instead")
     a = ap.parse_args()

@@ -94,7 +94,9 @@ typedef enum {
  *                         scores, seq_lens, row_starts or out NULL while num_rows > 0.
  *   TOPK_ERR_UNSUPPORTED  k > TOPK_K_MAX; scores not 4-byte aligned; with a page
  *                         table, page_size > 2^30; (topk_packed_ex) a k above
- *                         TOPK_K_FAST with the PIPE or SPLIT kernel chosen.
+ *                         TOPK_K_FAST with the PIPE or SPLIT kernel chosen, or
+ *                         the DECODE kernel chosen with row_stride above
+ *                         TOPK_DECODE_MAX_STRIDE.
  *   TOPK_ERR_DEVICE       the current device is not sm_103a or cannot be queried.
  *   TOPK_ERR_LAUNCH       the kernel launch was rejected.
  * Thread safety: safe to call from several host threads; calls on different
@@ -109,25 +111,32 @@ TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, cons
 
 /* Kernel families behind topk_packed_ex. */
 typedef enum {
-  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: for k <= TOPK_K_FAST, TOPK_PATH_SPLIT
-                              (TOPK_PATH_PIPE if the split kernel cannot be resident on the device);
-                              for a larger k, TOPK_PATH_MULTIPASS */
+  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: TOPK_PATH_DECODE when row_stride <=
+                              TOPK_DECODE_MAX_STRIDE (32-bit scores); otherwise, for k <= TOPK_K_FAST,
+                              TOPK_PATH_SPLIT (TOPK_PATH_PIPE if the split kernel cannot be resident
+                              on the device), and for a larger k TOPK_PATH_MULTIPASS */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
   TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
   TOPK_PATH_PIPE = 3,      /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over
                               contiguous blocks of the row, candidates kept in window order with a
                               threshold carried from row to row, ordered emission by prefix counts */
-  TOPK_PATH_SPLIT = 4      /* persistent CTAs, one per SM, each on a contiguous range of rows
+  TOPK_PATH_SPLIT = 4,     /* persistent CTAs, one per SM, each on a contiguous range of rows
                               balanced by cost: 8 streaming warps (8 KB TMA stages, 128 KB in flight
                               per SM) hand each row's candidates, in one of two buffer sets, to 8
                               finishing warps that select and emit it while the next row streams */
+  TOPK_PATH_DECODE = 5     /* short windows (row_stride <= TOPK_DECODE_MAX_STRIDE, 32-bit scores):
+                              one CTA of 1024 threads per row holds the window in registers and runs
+                              an exact radix select on them (a single read of the window) */
 } topk_path_t;
+
+/* Largest row_stride TOPK_PATH_DECODE serves. */
+#define TOPK_DECODE_MAX_STRIDE 16381
 
 /* Launch choices; zero fields mean "choose automatically". */
 typedef struct {
   int32_t path;            /* topk_path_t */
   int32_t cluster_size;    /* STREAM: CTAs that share one row (1, 2, 4 or 8); 0 = auto */
-  int32_t max_ctas;        /* STREAM, PIPE, SPLIT, MULTIPASS: upper bound on the grid; 0 = auto */
+  int32_t max_ctas;        /* STREAM, PIPE, SPLIT, MULTIPASS, DECODE: upper bound on the grid; 0 = auto */
   uint32_t stream_wait_ns; /* PIPE, SPLIT: bound of each wait for a streamed chunk of the window, in
                               ns; 0 = the default of about 2 s.  A wait that runs out sets bit 0 of
                               the diagnostics word; the warp then stops taking chunks and the rows it

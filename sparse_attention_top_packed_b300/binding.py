@@ -18,7 +18,8 @@ LIB_NAME = "libtopk_packed.so"
 TOPK_OK = 0
 STATUS_NAMES = {0: "TOPK_OK", 1: "TOPK_ERR_INVALID_ARG", 2: "TOPK_ERR_UNSUPPORTED",
                 3: "TOPK_ERR_LAUNCH", 4: "TOPK_ERR_DEVICE"}
-PATHS = {"auto": 0, "multipass": 1, "stream": 2, "pipe": 3, "split": 4}
+PATHS = {"auto": 0, "multipass": 1, "stream": 2, "pipe": 3, "split": 4, "decode": 5}
+DECODE_MAX_STRIDE = 16381
 K_MAX = 1 << 20
 K_FAST = 2048
 

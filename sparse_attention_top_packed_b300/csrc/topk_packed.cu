@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "topk_decode.cuh"
 #include "topk_kernels.cuh"
 #include "topk_pipe.cuh"
 #include "topk_split.cuh"
@@ -32,6 +33,7 @@ struct DeviceInfo {
   int multipass_ctas_per_sm = 0;
   int pipe_ctas_per_sm = 0;
   int split_ctas_per_sm = 0;
+  int decode_ctas_per_sm = 0;
   cudaError_t error = cudaSuccess;
 };
 
@@ -112,6 +114,17 @@ void init_device(int dev) {
       (void)cudaGetLastError();  // clear it: the other kernels stay usable
     }
   }
+  if (e == cudaSuccess) {
+    const int ss = (int)sizeof(topk::SelectShared);
+    e = cudaFuncSetAttribute(topk::decode::topk_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, ss);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(topk::decode::topk_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, ss);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(topk::decode::topk_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, ss);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.decode_ctas_per_sm, topk::decode::topk_decode_kernel<4>,
+                                                        topk::decode::kThreads, ss);
+  }
   if (e == cudaSuccess) e = prepare_stream<1>(d.stream_ctas_per_sm, d.sms);
   if (e == cudaSuccess) e = prepare_stream<2>(d.stream_clusters[1], d.sms);
   if (e == cudaSuccess) e = prepare_stream<4>(d.stream_clusters[2], d.sms);
@@ -120,7 +133,8 @@ void init_device(int dev) {
     d.error = e;
     return;
   }
-  d.ok = d.multipass_ctas_per_sm > 0 && d.stream_ctas_per_sm > 0 && d.pipe_ctas_per_sm > 0;
+  d.ok = d.multipass_ctas_per_sm > 0 && d.stream_ctas_per_sm > 0 && d.pipe_ctas_per_sm > 0 &&
+         d.decode_ctas_per_sm > 0;
   if (!d.ok) d.error = cudaErrorInvalidConfiguration;
 }
 
@@ -159,7 +173,7 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
   if (has_table && (pt_stride < 0 || page_size <= 0 || (page_size & (page_size - 1)) != 0))
     return TOPK_ERR_INVALID_ARG;
   if (cfg) {
-    if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_SPLIT) return TOPK_ERR_INVALID_ARG;
+    if (cfg->path < TOPK_PATH_AUTO || cfg->path > TOPK_PATH_DECODE) return TOPK_ERR_INVALID_ARG;
     const int c = cfg->cluster_size;
     if (!(c == 0 || c == 1 || c == 2 || c == 4 || c == 8)) return TOPK_ERR_INVALID_ARG;
     if (cfg->max_ctas < 0) return TOPK_ERR_INVALID_ARG;
@@ -173,21 +187,37 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
 
 int cluster_index(int c) { return c == 2 ? 1 : c == 4 ? 2 : 3; }
 
+static_assert(topk::decode::max_stride<4>() == TOPK_DECODE_MAX_STRIDE, "decode kernel bound");
+
+// Quads a thread of the decode kernel holds for this row_stride (1, 2 or 4).
+int decode_qpt(int64_t row_stride) {
+  return row_stride <= topk::decode::max_stride<1>() ? 1 : row_stride <= topk::decode::max_stride<2>() ? 2 : 4;
+}
+
 Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t k, int32_t num_rows,
-               const topk_launch_config_t* cfg) {
-  (void)row_stride;
+               const topk_launch_config_t* cfg, bool f32) {
   Plan pl;
   const int32_t want = cfg ? cfg->path : TOPK_PATH_AUTO;
-  // the warp-specialised split kernel, whose stream never waits for the end
-  // of a row; the pipelined kernel when the split one cannot be resident; the
-  // multipass kernel for a k beyond the single-pass kernels' buffers
+  // short windows: the register-resident decode kernel (a row's time is
+  // latency there); otherwise the warp-specialised split kernel, whose stream
+  // never waits for the end of a row; the pipelined kernel when the split one
+  // cannot be resident; the multipass kernel for a k beyond the single-pass
+  // kernels' buffers
   if (want != TOPK_PATH_AUTO)
     pl.path = want;
+  else if (f32 && row_stride <= TOPK_DECODE_MAX_STRIDE)
+    pl.path = TOPK_PATH_DECODE;
   else if (k > TOPK_K_FAST)
     pl.path = TOPK_PATH_MULTIPASS;
   else
     pl.path = d.split_ctas_per_sm > 0 ? TOPK_PATH_SPLIT : TOPK_PATH_PIPE;
   pl.cluster = 1;
+  if (pl.path == TOPK_PATH_DECODE) {
+    const int64_t cap = (int64_t)d.sms * d.decode_ctas_per_sm;
+    pl.grid = num_rows < cap ? num_rows : cap;
+    if (cfg && cfg->max_ctas > 0 && pl.grid > cfg->max_ctas) pl.grid = cfg->max_ctas;
+    return pl;
+  }
   if (pl.path == TOPK_PATH_PIPE) {
     const int64_t cap = (int64_t)d.sms * d.pipe_ctas_per_sm;
     pl.grid = num_rows < cap ? num_rows : cap;
@@ -292,9 +322,10 @@ topk_status_t topk_packed_typed(const void* scores, int32_t dtype, int64_t row_s
   prm.stream_wait_ns = config ? config->stream_wait_ns : 0u;
   prm.test_flags = config ? config->test_flags : 0u;
 
-  const Plan pl = make_plan(*d, row_stride, k, num_rows, config);
+  const Plan pl = make_plan(*d, row_stride, k, num_rows, config, !half);
   if (pl.grid <= 0) return TOPK_ERR_UNSUPPORTED;  // the split kernel cannot be resident here
   if (k > TOPK_K_FAST && (pl.path == TOPK_PATH_PIPE || pl.path == TOPK_PATH_SPLIT)) return TOPK_ERR_UNSUPPORTED;
+  if (pl.path == TOPK_PATH_DECODE && row_stride > TOPK_DECODE_MAX_STRIDE) return TOPK_ERR_UNSUPPORTED;
   if (half && pl.path != TOPK_PATH_SPLIT) return TOPK_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool dep = config && config->dependent_launch != 0;
@@ -315,6 +346,15 @@ topk_status_t topk_packed_typed(const void* scores, int32_t dtype, int64_t row_s
   } else if (pl.path == TOPK_PATH_MULTIPASS) {
     e = launch(topk::topk_multipass_kernel, pl.grid, topk::kMultipassThreads, sizeof(topk::SelectShared), 1, dep, s,
                prm);
+  } else if (pl.path == TOPK_PATH_DECODE) {
+    const size_t ss = sizeof(topk::SelectShared);
+    const int nt = topk::decode::kThreads, qpt = decode_qpt(row_stride);
+    if (qpt == 1)
+      e = launch(topk::decode::topk_decode_kernel<1>, pl.grid, nt, ss, 1, dep, s, prm);
+    else if (qpt == 2)
+      e = launch(topk::decode::topk_decode_kernel<2>, pl.grid, nt, ss, 1, dep, s, prm);
+    else
+      e = launch(topk::decode::topk_decode_kernel<4>, pl.grid, nt, ss, 1, dep, s, prm);
   } else {
     const size_t sm = sizeof(topk::StreamShared);
     switch (pl.cluster) {
@@ -354,9 +394,10 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
   if (st != TOPK_OK) return st;
   const DeviceInfo* d = device_info(st);
   if (!d) return st;
-  const Plan pl = make_plan(*d, row_stride, k, num_rows, config);
+  const Plan pl = make_plan(*d, row_stride, k, num_rows, config, true);
   if (pl.grid <= 0 && num_rows > 0) return TOPK_ERR_UNSUPPORTED;
   if (k > TOPK_K_FAST && (pl.path == TOPK_PATH_PIPE || pl.path == TOPK_PATH_SPLIT)) return TOPK_ERR_UNSUPPORTED;
+  if (pl.path == TOPK_PATH_DECODE && row_stride > TOPK_DECODE_MAX_STRIDE) return TOPK_ERR_UNSUPPORTED;
   if (path) *path = pl.path;
   if (cluster_size) *cluster_size = pl.cluster;
   if (grid_ctas) *grid_ctas = (int32_t)pl.grid;
@@ -364,6 +405,7 @@ topk_status_t topk_packed_plan(int64_t row_stride, int32_t k, int32_t num_rows,
     *threads_per_cta = pl.path == TOPK_PATH_PIPE        ? topk::pipe::kBlock
                        : pl.path == TOPK_PATH_SPLIT     ? topk::split::kBlockThreads
                        : pl.path == TOPK_PATH_MULTIPASS ? topk::kMultipassThreads
+                       : pl.path == TOPK_PATH_DECODE    ? topk::decode::kThreads
                                                         : topk::kStreamThreads;
   return TOPK_OK;
 }

@@ -78,6 +78,10 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert _call(num_rows=0, scores=None, seq=None, starts=None, table=None, out=None) == OK
     bad = binding.LaunchConfig(7, 0, 0)
     assert _call(cfg=bad) == INVALID
+    bad = binding.LaunchConfig(6, 0, 0)
+    assert _call(cfg=bad) == INVALID
+    dec = binding.LaunchConfig(5, 0, 0)  # the decode kernel: accepted; the next check answers
+    assert _call(cfg=dec, scores=0x1002) == UNSUPPORTED
     bad = binding.LaunchConfig(2, 3, 0)
     assert _call(cfg=bad) == INVALID
     bad = binding.LaunchConfig(2, 0, -1)

@@ -172,6 +172,10 @@ def test_plan_reports_the_launch(cuda_device):
     assert plan["grid_ctas"] == sms, "one CTA per SM"
     small = binding.topk_packed_plan(140000, 2048, 7)
     assert small["grid_ctas"] == 7 and small["path"] == binding.PATHS["split"], "decode-like batches"
+    dec = binding.topk_packed_plan(8192, 2048, 64)
+    assert dec["path"] == binding.PATHS["decode"] and dec["grid_ctas"] == 64 and dec["threads_per_cta"] == 1024
+    assert binding.topk_packed_plan(binding.DECODE_MAX_STRIDE, 2048, 64)["path"] == binding.PATHS["decode"]
+    assert binding.topk_packed_plan(binding.DECODE_MAX_STRIDE + 1, 2048, 64)["path"] == binding.PATHS["split"]
     pipe = binding.topk_packed_plan(140000, 2048, 4096, path="pipe")
     assert pipe["threads_per_cta"] == 256, "8 warps, each streaming its own block"
     assert pipe["grid_ctas"] == 2 * sms, "two pipelined CTAs per SM"
@@ -363,12 +367,13 @@ def test_stream_wait_give_up_is_recorded_and_the_result_stays_exact(cuda_device,
 # the negated values.
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("launch", [dict(path="split"), dict(path="pipe"), dict(path="multipass"),
-                                    dict(path="stream", cluster_size=2)], ids=["split", "pipe", "multipass", "stream2"])
+                                    dict(path="stream", cluster_size=2), dict(path="decode")],
+                         ids=["split", "pipe", "multipass", "stream2", "decode"])
 def test_dependent_launch_waits_for_the_producing_kernel(cuda_device, launch):
     from sparse_attention_top_packed_b300.producer import produce_scores
 
     rng = np.random.default_rng(5)
-    p = wl.random_problem(rng, rows=24, max_len=20000, k=2048, page_size=64, values="normal", slack=13)
+    p = wl.random_problem(rng, rows=24, max_len=16000, k=2048, page_size=64, values="normal", slack=13)
     w = host_problem_to_device(p, cuda_device)
     real = w.scores.clone()
     want = oracle_host(p)
@@ -492,3 +497,76 @@ def test_bf16_buffer_gives_the_fp32_result_on_bf16_values(cuda_device, name):
     want = oracle_rows(w16, rows)
     got = out16[rows.to(out16.device)].cpu().numpy()
     assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# The register-resident decode kernel (windows of at most 16381 elements):
+# each of its three register shapes (4, 8 or 16 elements a thread), tie-heavy
+# and sorted values, k from 1 to above the window, every start offset.
+# ---------------------------------------------------------------------------
+DECODE_CASES = [
+    # values, rows, max_len, k, page_size
+    ("normal", 24, 4000, 32, 64),      # row stride <= 4093: 4 elements a thread
+    ("normal", 24, 8000, 2048, 64),    # <= 8189: 8 elements a thread
+    ("normal", 24, 16000, 2048, 64),   # <= 16381: 16 elements a thread
+    ("ties", 30, 12000, 777, 1),
+    ("bf16", 24, 16000, 2048, 64),
+    ("int", 16, 16000, 2048, 16),
+    ("equal", 8, 10000, 2048, 64),
+    ("ascending", 10, 16000, 2048, 64),
+    ("descending", 10, 16000, 300, 64),
+    ("normal", 20, 5000, 1, 4),
+    ("bf16", 12, 16000, 5000, 64),
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=[f"{c[0]}-L{c[2]}-k{c[3]}" for c in DECODE_CASES])
+def test_decode_kernel_random_problems(cuda_device, case):
+    values, rows, max_len, k, page_size = case
+    rng = np.random.default_rng(zlib.crc32(f"decode-{values}-{max_len}-{k}".encode()))
+    p = wl.random_problem(rng, rows=rows, max_len=max_len, k=k, page_size=page_size, values=values, slack=13)
+    assert p.row_stride <= binding.DECODE_MAX_STRIDE
+    w = host_problem_to_device(p, cuda_device)
+    before = w.scores.clone()
+    want = oracle_host(p)
+    assert np.array_equal(run(w, path="decode").cpu().numpy(), want)
+    assert np.array_equal(run(w).cpu().numpy(), want), "the automatic choice for short windows"
+    assert torch.equal(before, w.scores), "the score buffer was written"
+
+
+@pytest.mark.parametrize("stride_target", [4093, 8189, 16381])
+def test_decode_kernel_edge_lengths_and_offsets(cuda_device, stride_target):
+    k = 64
+    rng = np.random.default_rng(stride_target)
+    lens = [0, 1, k - 1, k, k + 1, 1023, 1024, 1025, 2049, stride_target - 8, -4]
+    rows = [(L, off) for L in lens for off in range(4)]
+    n = len(rows)
+    stride = stride_target if stride_target % 2 else stride_target - 1  # odd
+    scores = np.full(n * stride, np.inf, dtype=np.float32)
+    seq = np.zeros(n, np.int32)
+    st = np.zeros(n, np.int32)
+    for i, (L, off) in enumerate(rows):
+        Lp = max(L, 0)
+        v = rng.standard_normal(Lp).astype(np.float32)
+        if Lp > 10:
+            v[rng.integers(0, Lp, size=Lp // 10)] = -0.0
+            v[rng.integers(0, Lp, size=Lp // 10)] = 0.0
+            v[rng.integers(0, Lp, size=3)] = np.inf
+            v[rng.integers(0, Lp, size=3)] = -np.inf
+        seq[i] = L
+        st[i] = min(off + (i % 3), stride - Lp)
+        scores[i * stride + st[i]: i * stride + st[i] + Lp] = v
+    pages = -(-stride // 16)
+    table = rng.choice(1 << 24, size=n * pages, replace=False).astype(np.int32)
+    p = wl.HostProblem(scores, stride, seq, st, None, table, pages, 16, k)
+    w = host_problem_to_device(p, cuda_device)
+    assert np.array_equal(run(w, path="decode").cpu().numpy(), oracle_host(p))
+
+
+def test_decode_kernel_refuses_long_strides(cuda_device):
+    rng = np.random.default_rng(8)
+    p = wl.random_problem(rng, rows=4, max_len=binding.DECODE_MAX_STRIDE, k=64, page_size=64, slack=1)
+    w = host_problem_to_device(p, cuda_device)
+    with pytest.raises(binding.TopkError):
+        run(w, path="decode")
+    assert np.array_equal(run(w).cpu().numpy(), oracle_host(p))
