@@ -44,6 +44,7 @@ WORKLOAD_TEXT = {
              "bf16-rounded scores, k=2048, page 64",
     "decode": "decode-like: 64 rows x 8192 fp32, k=2048, page 64",
     "tiny": "tiny: 8 rows, windows 1..300 at unaligned offsets, k=32, page 64",
+    "fewlong": "few long rows: 64 rows x 327680 fp32 (fewer rows than SMs), k=2048, page 64",
 }
 L2_BYTES = 126 * 1024 * 1024
 

@@ -1364,69 +1364,110 @@ __device__ __forceinline__ void emit_ordered(Shared& S, const Out& out, uint32_t
   }
 }
 
-// A row without a hint takes its threshold from kSamples of its own elements:
-// kSamples / 4 quads spread evenly over the window, read from global memory
-// (the same bytes stream through the rings right after); lanes outside the
-// window count as the lowest key.  The threshold is the sample's rank-R key,
-// R = 1.4 k * kSamples / L, so that about 1.4 k of the row's elements reach
-// it; the rank-k key (k * kSamples / L) sizes the fine histogram.  Both come
-// from two radix digits of 11 bits (keys to 2^-13 relative precision), the
-// threshold rounded down to its digit.  It is only a guess: if it admits
-// fewer than k elements or overflows a region, the row is done again in
-// exact mode.  Entered through a barrier with hist2 zero; leaves it zero.
+// A row without a hint takes its threshold from a sample of its own
+// elements: ns quads spread evenly over the window (ns * kPerQuad elements:
+// 4096, or 16384 when 4096 would put fewer than about 128 samples above the
+// threshold, i.e. for windows longer than 44.8 k), read from global memory (the same bytes
+// stream through the rings right after); lanes outside the window count as
+// the lowest key.  The threshold is the sample's rank-R key, R = 1.4 k * n /
+// L, so that about 1.4 k of the row's elements reach it; the rank-k key
+// (k * n / L) sizes the fine histogram.  Both come from two radix digits of 11
+// bits (keys to 2^-13 relative precision), the threshold rounded down to its
+// digit.  The second digit reads the sample again (from L2).  It is only a
+// guess: if it admits fewer than k elements or overflows a region, the row is
+// done again in exact mode.  Entered through a barrier with hist2 zero;
+// leaves it zero.
 constexpr int kSamples = 4096;
-static_assert(kSamples <= kCap, "the sample is kept in the candidate buffer");
+constexpr int kSamplesLong = 16384;
+static_assert(kSamples <= kCap, "the 4096-key sample is kept in the candidate buffer");
 static_assert(2 * kBins2 <= kCap, "the second digit's histograms use the index buffer");
+
+// Quad s (of ns) of the sample of a window of nq quads.
+__device__ __forceinline__ int64_t sample_quad(int64_t s, int64_t ns, int64_t nq) {
+  return ((2 * s + 1) * nq) / (2 * ns);
+}
 
 template <class E = ElemF32>
 __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const Row r, int64_t nq) {
   constexpr int EPQ = E::kPerQuad;
-  constexpr int kSampleQuads = kSamples / EPQ;
-  constexpr int U = kSampleQuads / kThreads;
   const int t = threadIdx.x;
+  // samples above the rank-R key: 1.4 k * nsamp / L; at least ~128 of them
+  const bool long_sample = (int64_t)r.L * 128 > (int64_t)14 * p.k * kSamples / 10;
+  const int nsamp = long_sample ? kSamplesLong : kSamples;
+  const int64_t ns = nsamp / EPQ;  // quads sampled
   uint32_t* h1a = reinterpret_cast<uint32_t*>(S.bj);  // second digit under the rank-R digit
   uint32_t* h1b = h1a + kBins2;                        // ... and under the rank-k digit
-  float4 v[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int64_t q = ((2 * (int64_t)(t + u * kThreads) + 1) * nq) / (2 * kSampleQuads);
-    v[u] = __ldg(r.base4 + q);
-  }
   for (int b = t; b < 2 * kBins2 / 4; b += kThreads) reinterpret_cast<uint4*>(h1a)[b] = make_uint4(0u, 0u, 0u, 0u);
+  // first digit: the top 11 bits of every sampled key (a thread's quads are
+  // loaded 8 at a time, all in flight together)
+  for (int64_t s0 = t; s0 < ns; s0 += 8 * kThreads) {
+    float4 v[8];
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int s = t + u * kThreads;
-    const int64_t q = ((2 * (int64_t)s + 1) * nq) / (2 * kSampleQuads);
-    float f[EPQ];
-    E::decode(v[u], f);
+    for (int u = 0; u < 8; ++u) {
+      const int64_t s = s0 + (int64_t)u * kThreads;
+      v[u] = s < ns ? __ldg(r.base4 + sample_quad(s, ns, nq)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-    for (int e = 0; e < EPQ; ++e) {
-      const int64_t j = q * EPQ - r.head + e;
-      const uint32_t key = (j >= 0 && j < r.L) ? key_of(f[e]) : 0u;
-      S.bkey[EPQ * s + e] = key;
-      atomicAdd(&S.hist2[key >> 21], 1u);
+    for (int u = 0; u < 8; ++u) {
+      const int64_t s = s0 + (int64_t)u * kThreads;
+      if (s >= ns) continue;
+      const int64_t q = sample_quad(s, ns, nq);
+      float f[EPQ];
+      E::decode(v[u], f);
+#pragma unroll
+      for (int e = 0; e < EPQ; ++e) {
+        const int64_t j = q * EPQ - r.head + e;
+        const uint32_t key = (j >= 0 && j < r.L) ? key_of(f[e]) : 0u;
+        if (!long_sample) S.bkey[EPQ * s + e] = key;  // kept for the second digit
+        atomicAdd(&S.hist2[key >> 21], 1u);
+      }
     }
   }
-  const int64_t want = (7 * (int64_t)p.k * kSamples) / (5 * (int64_t)r.L) + 1;
-  const uint32_t R = (uint32_t)min(want, (int64_t)kSamples);
-  const uint32_t Rk = (uint32_t)min((int64_t)p.k * kSamples / r.L + 1, (int64_t)R);
+  const int64_t want = (7 * (int64_t)p.k * nsamp) / (5 * (int64_t)r.L) + 1;
+  const uint32_t R = (uint32_t)min(want, (int64_t)nsamp);
+  const uint32_t Rk = (uint32_t)min((int64_t)p.k * nsamp / r.L + 1, (int64_t)R);
   cbar();
   fine_publish(S, S.hist2);
   cbar();
   uint32_t tot[kWarps];
   fine_totals(S, tot);
   const FinePick a = fine_find(S, S.hist2, tot, R), b = fine_find(S, S.hist2, tot, Rk);
+  // second digit: bits 10..20 of the sampled keys in the two chosen bins (the
+  // 4096-key sample from shared memory, the larger one read again from L2)
+  auto second_digit = [&](uint32_t key) {
+    const uint32_t d = key >> 21;
+    if (d == a.bin)
+      atomicAdd(&h1a[(key >> 10) & (kBins2 - 1)], 1u);
+    else if (d == b.bin)
+      atomicAdd(&h1b[(key >> 10) & (kBins2 - 1)], 1u);
+  };
+  if (!long_sample) {
+    for (int64_t s = t; s < ns; s += kThreads)  // this thread's own entries
 #pragma unroll
-  for (int u = 0; u < U; ++u)
+      for (int e = 0; e < EPQ; ++e) second_digit(S.bkey[EPQ * s + e]);
+  } else {
+    for (int64_t s0 = t; s0 < ns; s0 += 8 * kThreads) {
+      float4 v[8];
 #pragma unroll
-    for (int e = 0; e < EPQ; ++e) {
-      const uint32_t key = S.bkey[EPQ * (t + u * kThreads) + e];  // this thread's own entries
-      const uint32_t d = key >> 21;
-      if (d == a.bin)
-        atomicAdd(&h1a[(key >> 10) & (kBins2 - 1)], 1u);
-      else if (d == b.bin)
-        atomicAdd(&h1b[(key >> 10) & (kBins2 - 1)], 1u);
+      for (int u = 0; u < 8; ++u) {
+        const int64_t s = s0 + (int64_t)u * kThreads;
+        v[u] = s < ns ? __ldg(r.base4 + sample_quad(s, ns, nq)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t s = s0 + (int64_t)u * kThreads;
+        if (s >= ns) continue;
+        const int64_t q = sample_quad(s, ns, nq);
+        float f[EPQ];
+        E::decode(v[u], f);
+#pragma unroll
+        for (int e = 0; e < EPQ; ++e) {
+          const int64_t j = q * EPQ - r.head + e;
+          second_digit((j >= 0 && j < r.L) ? key_of(f[e]) : 0u);
+        }
+      }
     }
+  }
   cbar();  // every warp is done with hist2 and the first scan
   for (int i = t; i < kBins2 / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0u, 0u, 0u, 0u);
   fine_publish(S, h1a);

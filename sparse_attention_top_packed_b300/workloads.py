@@ -183,6 +183,20 @@ def long_context(device="cpu", seed: int = 0, kv_len: int = 327680, q_rows: int 
                     rtb, pt.to(device), 0 if identity_map else pages, page_size, k, q_rows)
 
 
+def few_long(device="cpu", seed: int = 0, rows: int = 64, kv_len: int = 327680, k: int = 2048,
+             page_size: int = 64) -> Workload:
+    """Fewer rows than SMs with long windows (the case that splits a row over
+    a cluster of CTAs): `rows` decode-like queries of one request of kv_len
+    keys each, seeing the whole context, [rows, kv_len] N(0,1), one table row."""
+    seq_lens = torch.full((rows,), kv_len, dtype=torch.int32)
+    row_starts = torch.zeros(rows, dtype=torch.int32)
+    pages = -(-kv_len // page_size)
+    pt = distinct_pages(1, pages, seed + 1)
+    scores = _normal((rows, kv_len), seed, device)
+    return Workload("fewlong", scores, kv_len, seq_lens.to(device), row_starts.to(device),
+                    torch.zeros(rows, dtype=torch.int32).to(device), pt.to(device), pages, page_size, k, rows)
+
+
 def mixed_lengths(seed: int = 0, requests: int = 16, lo: int = 1024, hi: int = 65536):
     g = torch.Generator().manual_seed(seed)
     return torch.randint(lo, hi + 1, (requests,), generator=g, dtype=torch.int64)
@@ -232,7 +246,8 @@ def mixed(device="cpu", seed_lengths: int = 0, seed_scores: int = 1, total_rows:
                     row_to_batch.to(device), pt.to(device), table_pages, page_size, k, rows)
 
 
-NAMED = {"tiny": tiny, "decode": decode, "prefill": prefill, "long": long_context, "mixed": mixed}
+NAMED = {"tiny": tiny, "decode": decode, "prefill": prefill, "long": long_context, "mixed": mixed,
+         "fewlong": few_long}
 
 
 def named(name: str, device="cpu", **kw) -> Workload:
