@@ -111,12 +111,18 @@ TOPK_API topk_status_t topk_packed(const float* scores, int64_t row_stride, cons
 
 /* Kernel families behind topk_packed_ex. */
 typedef enum {
-  TOPK_PATH_AUTO = 0,      /* what topk_packed uses: TOPK_PATH_DECODE when row_stride <=
-                              TOPK_DECODE_MAX_STRIDE (32-bit scores); otherwise, for k <= TOPK_K_FAST,
+  TOPK_PATH_AUTO = 0,      /* what topk_packed uses (32-bit scores): TOPK_PATH_DECODE when row_stride
+                              <= TOPK_DECODE_MAX_STRIDE; TOPK_PATH_STREAM with rows split over a
+                              cluster of 2 CTAs (4 when num_rows <= SMs / 4) when row_stride >= 65536
+                              and num_rows <= SMs / 2; otherwise, for k <= TOPK_K_FAST,
                               TOPK_PATH_SPLIT (TOPK_PATH_PIPE if the split kernel cannot be resident
-                              on the device), and for a larger k TOPK_PATH_MULTIPASS */
+                              on the device), and for a larger k TOPK_PATH_MULTIPASS.  16-bit scores:
+                              TOPK_PATH_SPLIT */
   TOPK_PATH_MULTIPASS = 1, /* one CTA per row, radix passes straight from global memory */
-  TOPK_PATH_STREAM = 2,    /* persistent CTAs (or clusters): per-warp TMA rings + running threshold */
+  TOPK_PATH_STREAM = 2,    /* persistent CTAs, or clusters of 2/4/8 CTAs sharing each row: per-warp
+                              TMA rings, a threshold sampled per row that then only rises, per-warp
+                              candidate lists; a cluster sums its histograms through distributed
+                              shared memory and splits the tie quota by CTA rank */
   TOPK_PATH_PIPE = 3,      /* persistent CTAs, two per SM, 8 warps each: per-warp TMA rings over
                               contiguous blocks of the row, candidates kept in window order with a
                               threshold carried from row to row, ordered emission by prefix counts */

@@ -548,7 +548,7 @@ struct SelectShared {
   uint32_t pub_gt;        // published: this CTA's count of elements above the prefix
   uint32_t pub_eq;        // published: this CTA's count of prefix-equal elements
   uint32_t pub_overflow;  // published: a candidate list overflowed (streaming only)
-  uint32_t pad_;
+  uint32_t pub_count;     // published: candidates this CTA listed for the row (streaming only)
 };
 
 // Outcome of the selection, identical in every thread of a CTA.

@@ -340,6 +340,51 @@ __device__ __noinline__ void finish_from_global(const Params& p, int64_t row, co
   select_from_global<CLUSTER, kStreamThreads>(p, (int32_t)row, r, part, S, par);
 }
 
+// Whole CTA, entered through a barrier with S.sel.hist1 zero: the 22-bit key
+// prefix that about 1.4 k of the row's elements reach, estimated from a sample
+// spread evenly over the whole window (every CTA of a cluster computes the
+// same): 4096 elements, or 16384 when 4096 would put fewer than ~128 above
+// that rank.  Two digits, 12 and 10 bits, the second reading the sample again
+// (from L2).  Leaves hist1 zero; ends with a barrier.
+__device__ __noinline__ uint32_t stream_sample_threshold(StreamShared& S, const Params& p, const Row& r,
+                                                         ScanParity& par) {
+  const int tid = threadIdx.x;
+  const int64_t nq = ((int64_t)r.L + r.head + 3) >> 2;
+  const bool long_sample = (int64_t)r.L * 128 > (int64_t)14 * p.k * 4096 / 10;
+  const int64_t nsamp = long_sample ? 16384 : 4096, ns = nsamp / 4;
+  auto quad = [&](int64_t s) { return ((2 * s + 1) * nq) / (2 * ns); };
+  auto key_at = [&](int64_t q, const float4& v, int e) {
+    const int64_t j = q * 4 - r.head + e;
+    const float x = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    return (j >= 0 && j < r.L) ? key_of(x) : 0u;  // outside the window: the lowest key
+  };
+  for (int64_t s = tid; s < ns; s += kStreamThreads) {
+    const int64_t q = quad(s);
+    const float4 v = __ldg(r.base4 + q);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) atomicAdd(&S.sel.hist1[key_at(q, v, e) >> kShift1], 1u);
+  }
+  for (int b = tid; b < kBins23; b += kStreamThreads) S.sel.hist2[b] = 0u;
+  __syncthreads();
+  const uint32_t R = (uint32_t)min((7 * (int64_t)p.k * nsamp) / (5 * (int64_t)r.L) + 1, nsamp);
+  const Pick a = block_pick<kBins1, 1, kStreamThreads>(S.sel.hist1, R, par.next(S.sel), par.next_pick(S.sel));
+  for (int64_t s = tid; s < ns; s += kStreamThreads) {
+    const int64_t q = quad(s);
+    const float4 v = __ldg(r.base4 + q);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t key = key_at(q, v, e);
+      if ((key >> kShift1) == a.bin) atomicAdd(&S.sel.hist2[(key >> kShift2) & (kBins23 - 1)], 1u);
+    }
+  }
+  __syncthreads();
+  const Pick b = block_pick<kBins23, 1, kStreamThreads>(S.sel.hist2, R - a.above, par.next(S.sel),
+                                                        par.next_pick(S.sel));
+  for (int i = tid; i < kBins1; i += kStreamThreads) S.sel.hist1[i] = 0u;
+  __syncthreads();
+  return (a.bin << kShift1) | (b.bin << kShift2);
+}
+
 template <int CLUSTER>
 __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -380,8 +425,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
     const int32_t nch = (int32_t)(((sl.q1 - sl.q0) * 16 + kChunkBytes - 1) / kChunkBytes);
 
     for (int b = tid; b < kBins1; b += kStreamThreads) S.sel.hist1[b] = 0u;
+    __syncthreads();
+    // the row's starting threshold from a sample; it only rises afterwards
+    const uint32_t thr = stream_sample_threshold(S, p, r, par);
+    const float th0 = key_floor_float(thr);
     if (tid == 0) {
-      S.b0 = 0u;
+      S.b0 = thr >> kShift1;
       S.top = 0u;
       S.overflow = 0u;
     }
@@ -390,69 +439,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
     uint32_t count = 0, mbin = 0;
     bool over = false;
 
-    // ---- chunk 0 of every warp: histogram only, then one block-wide pick of
-    // the first threshold, then the chunk's survivors go to the lists.
-    uint32_t slot = 0, m = 0;
-    int32_t jb = 0;
-    float x[16];
-    if (nch > 0) {
-      slot = g % kStages;
-      if (!timed_out && !mbar_wait_bounded(&S.full[w][slot], (g / kStages) & 1u)) timed_out = true;
-      ++g;
-      load16_rotated(S, w, slot, lane, x);
-      jb = (int32_t)(sl.q0 * 4 - r.head) + 16 * lane;
-      m = element_to_rotated_order(valid16(jb, sl.lo, sl.hi), lane);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (m & (1u << i)) {
-          const uint32_t bin = key_of(x[i]) >> kShift1;
-          atomicAdd(&S.sel.hist1[bin], 1u);
-          mbin = max(mbin, bin);
-        }
-      }
-    }
-    {
-      const uint32_t mb = warp_max(mbin);
-      if (lane == 0) atomicMax(&S.top, mb);
-    }
-    __syncthreads();
-    // Pick{0,...} (threshold -inf) when the first chunks hold fewer than k elements
-    const Pick pk0 = block_pick<kBins1, 1, kStreamThreads>(S.sel.hist1, k, par.next(S.sel),
-                                                           par.next_pick(S.sel));
-    if (tid == 0) S.b0 = pk0.bin;
-    if (nch > 0) {
-      const uint32_t K0 = pk0.bin << kShift1;
-      uint32_t f = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) f |= ((m & (1u << i)) && key_of(x[i]) >= K0 ? 1u : 0u) << i;
-      f = rotated_to_element_order(f, lane);
-      const uint32_t cnt = __popc(f);
-      const uint32_t incl = warp_incl_scan(cnt);
-      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      if (total <= (uint32_t)kWarpCap) {
-        append_flagged<false>(S, w, reinterpret_cast<const float*>(&S.ring[w][slot][lane * 4]), f,
-                              incl - cnt, jb, mbin);
-        count = total;
-      } else {
-        over = true;  // more than kWarpCap of 512 elements reach the first threshold
-        if (lane == 0) S.overflow = 1u;
-      }
-      __syncwarp();
-      if (lane == 0) producer_issue<CLUSTER>(S, p, ncl, rank, w, slot, policy);
-    }
-
-    // ---- the rest of the slice: one compare per element against the running
+    // ---- the warp's slice: one compare per element against the running
     // threshold; survivors appended in order; no block-wide synchronisation.
-    for (int32_t c = 1; c < nch; ++c) {
-      slot = g % kStages;
+    for (int32_t c = 0; c < nch; ++c) {
+      const uint32_t slot = g % kStages;
       if (!timed_out && !mbar_wait_bounded(&S.full[w][slot], (g / kStages) & 1u)) timed_out = true;
       ++g;
+      float x[16];
       load16_rotated(S, w, slot, lane, x);
-      jb = (int32_t)((sl.q0 + (int64_t)c * kChunkQuads) * 4 - r.head) + 16 * lane;
+      const int32_t jb = (int32_t)((sl.q0 + (int64_t)c * kChunkQuads) * 4 - r.head) + 16 * lane;
       if (!over) {
-        const float th = edge_float(max(*reinterpret_cast<volatile uint32_t*>(&S.b0), pk0.bin));
-        m = rotated_to_element_order(flags16(x, th), lane);
-        if (c == nch - 1) m &= valid16(jb, sl.lo, sl.hi);
+        const float th = fmaxf(th0, edge_float(*reinterpret_cast<volatile uint32_t*>(&S.b0)));
+        uint32_t m = rotated_to_element_order(flags16(x, th), lane);
+        if (c == 0 || c == nch - 1) m &= valid16(jb, sl.lo, sl.hi);
         uint32_t cnt = __popc(m);
         uint32_t incl = warp_incl_scan(cnt);
         uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
@@ -461,7 +460,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
           if (count + total > (uint32_t)kWarpCap) {
             uint32_t b0;
             count = compact_warp_list(S, w, count, k, mbin, &b0);
-            const float th2 = edge_float(b0);
+            const float th2 = fmaxf(th0, edge_float(b0));
             uint32_t m2 = 0;
             for (uint32_t mm = m; mm; mm &= mm - 1) {
               const int e = __ffs(mm) - 1;
@@ -488,16 +487,26 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
     }
     if (lane == 0) S.count[w] = over ? 0u : count;
 
-    // ---- end of the row's stream: select on the lists (or fall back) ----
+    // ---- end of the row's stream: select on the lists, or fall back when a
+    // list overflowed or the sampled threshold left fewer than k candidates
+    // in the cluster ----
     __syncthreads();
-    bool any_over = S.overflow != 0u;
+    uint32_t listed = 0;
+    for (int i = 0; i < kStreamWarps; ++i) listed += S.count[i];
+    bool any_over = S.overflow != 0u || listed < k;
     if constexpr (CLUSTER > 1) {
-      if (tid == 0) S.sel.pub_overflow = S.overflow;
+      if (tid == 0) {
+        S.sel.pub_overflow = S.overflow;
+        S.sel.pub_count = listed;
+      }
       cluster_sync_all();
-      const uint32_t a = smem_addr(&S.sel.pub_overflow);
-      uint32_t o = 0;
-      for (uint32_t c = 0; c < (uint32_t)CLUSTER; ++c) o |= ld_cluster_u32(peer_addr(a, c));
-      any_over = o != 0u;
+      const uint32_t a = smem_addr(&S.sel.pub_overflow), ac = smem_addr(&S.sel.pub_count);
+      uint32_t o = 0, n = 0;
+      for (uint32_t c = 0; c < (uint32_t)CLUSTER; ++c) {
+        o |= ld_cluster_u32(peer_addr(a, c));
+        n += ld_cluster_u32(peer_addr(ac, c));
+      }
+      any_over = o != 0u || n < k;
     }
     if (any_over)
       finish_from_global<CLUSTER>(p, row, r, part, S.sel, par);

@@ -187,6 +187,9 @@ topk_status_t check_sizes(int64_t row_stride, int64_t pt_stride, int32_t page_si
 
 int cluster_index(int c) { return c == 2 ? 1 : c == 4 ? 2 : 3; }
 
+// Shortest row_stride for which the automatic choice splits rows over a cluster.
+constexpr int64_t kClusterMinStride = 65536;
+
 static_assert(topk::decode::max_stride<4>() == TOPK_DECODE_MAX_STRIDE, "decode kernel bound");
 
 // Quads a thread of the decode kernel holds for this row_stride (1, 2 or 4).
@@ -203,11 +206,19 @@ Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t k, int32_t num_r
   // never waits for the end of a row; the pipelined kernel when the split one
   // cannot be resident; the multipass kernel for a k beyond the single-pass
   // kernels' buffers
+  // long windows in a batch of at most half as many rows as SMs: each row
+  // split over a cluster (2 CTAs, or 4 up to a quarter as many rows as SMs)
+  // that merges its histograms through distributed shared memory
+  int auto_cluster = 0;
   if (want != TOPK_PATH_AUTO)
     pl.path = want;
   else if (f32 && row_stride <= TOPK_DECODE_MAX_STRIDE)
     pl.path = TOPK_PATH_DECODE;
-  else if (k > TOPK_K_FAST)
+  else if (f32 && row_stride >= kClusterMinStride && 2 * (int64_t)num_rows <= d.sms &&
+           d.stream_clusters[cluster_index(2)] > 0) {
+    pl.path = TOPK_PATH_STREAM;
+    auto_cluster = 4 * (int64_t)num_rows <= d.sms && d.stream_clusters[cluster_index(4)] > 0 ? 4 : 2;
+  } else if (k > TOPK_K_FAST)
     pl.path = TOPK_PATH_MULTIPASS;
   else
     pl.path = d.split_ctas_per_sm > 0 ? TOPK_PATH_SPLIT : TOPK_PATH_PIPE;
@@ -236,7 +247,7 @@ Plan make_plan(const DeviceInfo& d, int64_t row_stride, int32_t k, int32_t num_r
     if (cfg && cfg->max_ctas > 0 && pl.grid > cfg->max_ctas) pl.grid = cfg->max_ctas;
     return pl;
   }
-  pl.cluster = (cfg && cfg->cluster_size > 0) ? cfg->cluster_size : 1;
+  pl.cluster = (cfg && cfg->cluster_size > 0) ? cfg->cluster_size : auto_cluster > 0 ? auto_cluster : 1;
   int64_t clusters;
   if (pl.cluster == 1) {
     clusters = (int64_t)d.sms * d.stream_ctas_per_sm;

@@ -170,12 +170,18 @@ def test_plan_reports_the_launch(cuda_device):
     assert plan["path"] == binding.PATHS["split"]
     assert plan["threads_per_cta"] == 512, "8 streaming and 8 finishing warps"
     assert plan["grid_ctas"] == sms, "one CTA per SM"
-    small = binding.topk_packed_plan(140000, 2048, 7)
-    assert small["grid_ctas"] == 7 and small["path"] == binding.PATHS["split"], "decode-like batches"
+    small = binding.topk_packed_plan(140000, 2048, sms // 2 + 7)
+    assert small["grid_ctas"] == sms // 2 + 7 and small["path"] == binding.PATHS["split"]
     dec = binding.topk_packed_plan(8192, 2048, 64)
     assert dec["path"] == binding.PATHS["decode"] and dec["grid_ctas"] == 64 and dec["threads_per_cta"] == 1024
     assert binding.topk_packed_plan(binding.DECODE_MAX_STRIDE, 2048, 64)["path"] == binding.PATHS["decode"]
     assert binding.topk_packed_plan(binding.DECODE_MAX_STRIDE + 1, 2048, 64)["path"] == binding.PATHS["split"]
+    few = binding.topk_packed_plan(327680, 2048, sms // 2)
+    assert few["path"] == binding.PATHS["stream"] and few["cluster_size"] == 2, "few long rows: 2-CTA clusters"
+    fewer = binding.topk_packed_plan(327680, 2048, sms // 4)
+    assert fewer["path"] == binding.PATHS["stream"] and fewer["cluster_size"] == 4
+    assert binding.topk_packed_plan(327680, 2048, sms // 2 + 1)["path"] == binding.PATHS["split"]
+    assert binding.topk_packed_plan(65535, 2048, 8)["path"] == binding.PATHS["split"]
     pipe = binding.topk_packed_plan(140000, 2048, 4096, path="pipe")
     assert pipe["threads_per_cta"] == 256, "8 warps, each streaming its own block"
     assert pipe["grid_ctas"] == 2 * sms, "two pipelined CTAs per SM"
@@ -570,3 +576,17 @@ def test_decode_kernel_refuses_long_strides(cuda_device):
     with pytest.raises(binding.TopkError):
         run(w, path="decode")
     assert np.array_equal(run(w).cpu().numpy(), oracle_host(p))
+
+
+def test_few_long_rows_full_size(cuda_device):
+    """Fewer rows than half the SMs, long windows: the automatic choice splits
+    each row over a cluster that merges histograms through distributed shared
+    memory; same bits as the split kernel and the oracle's sampled rows."""
+    w = wl.few_long(device=cuda_device)
+    plan = binding.topk_packed_plan(w.row_stride, w.k, w.num_rows)
+    assert plan["path"] == binding.PATHS["stream"] and plan["cluster_size"] > 1
+    out = _full_size(w, sample=32)
+    assert torch.equal(out, run(w, path="split"))
+    w16 = wl.few_long(device=cuda_device, rows=16)
+    assert binding.topk_packed_plan(w16.row_stride, w16.k, w16.num_rows)["cluster_size"] == 4
+    assert np.array_equal(run(w16).cpu().numpy(), oracle_rows(w16, torch.arange(16)))
