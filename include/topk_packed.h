@@ -231,6 +231,23 @@ TOPK_API int topk_last_cuda_error(void);
  *          unspecified.  Every copy a kernel issued has landed before it exits.
  *   bit 1: an output position at or past k was computed (a selection that is
  *          not exact); the position is not written.  Never expected.
+ *   bit 2 and bits 8-15 (only in libtopk_packed_checked.so, the same library
+ *          compiled with TOPK_CHECKED for testing): a bounds check failed.
+ *          That build checks, at run time, every global-memory address it
+ *          computes (window loads and bulk copies against the row's window
+ *          rounded out to 16 bytes, page-table reads against the window
+ *          length, descriptor reads against num_rows) and every shared-memory
+ *          index that is not in range by construction; a failed check sets
+ *          bit 2, the access is skipped, and bits 8-15 keep the site of the
+ *          first failure:
+ *            1 a row's window leaves its buffer row (the precondition
+ *              row_starts[i] + n <= row_stride; recorded, the row still read),
+ *            2 a descriptor read for a row outside [0, num_rows),
+ *            3 a window load, 4 a window bulk copy, 5 a page-table read
+ *              outside the window, 6 a shared page-stage read, 7 a candidate
+ *              store, 8 a region or list count, 9 a staged output position,
+ *              10 a sample load.
+ *          The normal library compiles every check away.
  * topk_packed_device_flags copies the word of the current device into *flags
  * (after the work queued on `stream` so far) and, when `reset` is non-zero,
  * clears it.  It synchronizes `stream`.  A reset races with launches running

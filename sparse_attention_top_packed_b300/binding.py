@@ -5,15 +5,22 @@ Every function has the name and argument order of its C counterpart in
 C library validates sizes and launches the CUDA kernels.  There is no
 fallback: if the shared library is missing or the device is not sm_103a the
 call raises.
+
+``checked_build()`` routes the calls made inside it to
+libtopk_packed_checked.so, the same library compiled with run-time bounds
+checks (a failed check sets bit 2 of the diagnostics word and records its
+site in bits 8-15); it is for testing, not for speed.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_NAME = "libtopk_packed.so"
+CHECKED_LIB_NAME = "libtopk_packed_checked.so"
 
 TOPK_OK = 0
 STATUS_NAMES = {0: "TOPK_OK", 1: "TOPK_ERR_INVALID_ARG", 2: "TOPK_ERR_UNSUPPORTED",
@@ -36,24 +43,52 @@ class LaunchConfig(ctypes.Structure):
                 ("test_flags", ctypes.c_uint32), ("dependent_launch", ctypes.c_int32)]
 
 
-_lib = None
+# Diagnostics word (topk_packed_device_flags).
+FLAG_STREAM_WAIT_TIMEOUT = 1
+FLAG_BAD_OUTPUT_POSITION = 2
+FLAG_OUT_OF_BOUNDS = 4  # checked build only; bits 8-15: the site of the first failed check
+CHECK_SITES = {1: "row window leaves its buffer row", 2: "descriptor row index", 3: "window load",
+               4: "window bulk copy", 5: "page-table read", 6: "page-stage read", 7: "candidate store",
+               8: "region or list count", 9: "staged output position", 10: "sample load"}
 
 
-def library_path() -> str:
-    return os.path.join(HERE, LIB_NAME)
+def check_site(flags: int) -> int:
+    """The site of the first failed bounds check recorded in a diagnostics word (0: none)."""
+    return (int(flags) >> 8) & 0xFF
 
 
-def available() -> bool:
-    return os.path.exists(library_path())
+_libs: dict = {}
+_checked = False
+
+
+def library_path(checked: Optional[bool] = None) -> str:
+    use = _checked if checked is None else checked
+    return os.path.join(HERE, CHECKED_LIB_NAME if use else LIB_NAME)
+
+
+def available(checked: bool = False) -> bool:
+    return os.path.exists(library_path(checked))
+
+
+@contextlib.contextmanager
+def checked_build():
+    """Calls made inside the block go to the bounds-checked library."""
+    global _checked
+    old = _checked
+    _checked = True
+    try:
+        yield
+    finally:
+        _checked = old
 
 
 def _load():
-    global _lib
-    if _lib is not None:
-        return _lib
+    lib = _libs.get(_checked)
+    if lib is not None:
+        return lib
     path = library_path()
     if not os.path.exists(path):
-        raise TopkError(-1, f"{LIB_NAME} is not built (run __graft_entry__.build() or "
+        raise TopkError(-1, f"{os.path.basename(path)} is not built (run __graft_entry__.build() or "
                             f"python -m sparse_attention_top_packed_b300.build)")
     lib = ctypes.CDLL(path)
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
@@ -73,7 +108,7 @@ def _load():
     lib.topk_last_cuda_error.argtypes = []
     lib.topk_packed_device_flags.restype = ctypes.c_int
     lib.topk_packed_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
-    _lib = lib
+    _libs[_checked] = lib
     return lib
 
 

@@ -56,7 +56,7 @@ struct RegSrc {
 #pragma unroll
     for (int u = 0; u < QPT; ++u) {
       const int64_t q = (int64_t)u * kThreads + threadIdx.x;
-      v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = q < nq ? load_window_quad(r, q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < QPT; ++u) {
@@ -108,7 +108,7 @@ __device__ __forceinline__ void emit(const RegSrc<QPT>& src, const Selection& se
       if (is_gt[e] || (is_eq[e] && q < sel.quota)) {
         const uint32_t pos = g + (q < sel.quota ? q : sel.quota);
         if (pos < k)
-          out_row[pos] = page_slot(page_row, page_bits, src.index(u, e));
+          out_row[pos] = page_slot(page_row, page_bits, src.index(u, e), src.L);
         else
           atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
       }

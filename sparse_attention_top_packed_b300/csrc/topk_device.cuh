@@ -42,6 +42,67 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // The diagnostic word (the library is one translation unit).
 __device__ uint32_t g_device_flags;
 
+// ---------------------------------------------------------------------------
+// Bounds checks of the checked build (compiled with TOPK_CHECKED).  Every
+// global-memory access whose address is computed (window loads and bulk
+// copies, page-table reads, descriptor reads) and every shared-memory index
+// that is not in range by construction (a bin taken with a mask of the
+// table's size is) goes through in_bounds(ok, site).  In the normal build
+// that is the constant true and costs nothing.  In the checked build a false
+// `ok` sets bit 2 of the diagnostics word, records `site` in bits 8-15 if no
+// violation was recorded before, and the caller skips the access (a load
+// gives zero).  Nothing traps.
+// ---------------------------------------------------------------------------
+#ifdef TOPK_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+constexpr uint32_t kFlagOutOfBounds = 4u;
+constexpr int kSiteShift = 8;
+constexpr uint32_t kSiteMask = 0xFFu << kSiteShift;
+
+// Which check failed first (bits 8-15 of the diagnostics word).
+enum CheckSite : uint32_t {
+  kSiteRowWindow = 1,   // a row's window leaves its buffer row (a broken precondition: recorded, not skipped)
+  kSiteRowIndex = 2,    // a descriptor read for a row outside [0, num_rows)
+  kSiteWindowLoad = 3,  // a plain load of quads outside the row's window rounded out to 16 bytes
+  kSiteWindowCopy = 4,  // a bulk copy of quads outside the row's window rounded out to 16 bytes
+  kSitePageRead = 5,    // a page-table read for a window index outside [0, L)
+  kSitePageStage = 6,   // a read of a shared page stage outside the entries staged
+  kSiteCandidate = 7,   // a candidate stored outside its region or the positions reserved
+  kSiteRegion = 8,      // a region or list count beyond its capacity
+  kSiteStaging = 9,     // a staged output position beyond the staging row
+  kSiteSampleLoad = 10, // a sample quad outside the window
+};
+
+#ifdef TOPK_CHECKED
+__device__ __noinline__ void record_violation(uint32_t site) {
+  uint32_t cur = *reinterpret_cast<volatile uint32_t*>(&g_device_flags);
+  for (int i = 0; i < 64; ++i) {  // bounded: every failed exchange means another thread wrote the word
+    uint32_t want = cur | kFlagOutOfBounds;
+    if ((cur & kSiteMask) == 0u) want |= (site << kSiteShift) & kSiteMask;
+    if (want == cur) return;
+    const uint32_t prev = atomicCAS(&g_device_flags, cur, want);
+    if (prev == cur) return;
+    cur = prev;
+  }
+  atomicOr(&g_device_flags, kFlagOutOfBounds);
+}
+#endif
+
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t site) {
+#ifdef TOPK_CHECKED
+  if (!ok) record_violation(site);
+  return ok;
+#else
+  (void)ok;
+  (void)site;
+  return true;
+#endif
+}
+
 struct Params {
   const float* scores;
   int64_t row_stride;
@@ -160,17 +221,49 @@ struct Row {
   const int32_t* page_row;  // page_table + table_row * pt_stride; null without a page table
 };
 
+// Checked build: the row index of a descriptor read, and the caller's
+// precondition 0 <= start, start + L <= row_stride for a row that is read.
+__device__ __forceinline__ bool row_index_ok(const Params& p, int64_t row) {
+  return in_bounds(row >= 0 && row < p.num_rows, kSiteRowIndex);
+}
+
+__device__ __forceinline__ void check_row_window(const Params& p, int32_t L, int32_t start) {
+  if constexpr (kChecked)
+    if (L > p.k) in_bounds(start >= 0 && (int64_t)start + L <= p.row_stride, kSiteRowWindow);
+}
+
 __device__ __forceinline__ Row load_row(const Params& p, int32_t row) {
   Row r;
-  const int32_t L = __ldg(p.seq_lens + row);
+  int32_t L = 0, start = 0;
+  if (row_index_ok(p, row)) {
+    L = __ldg(p.seq_lens + row);
+    start = __ldg(p.row_starts + row);
+  }
+  check_row_window(p, L, start);
   r.L = L > 0 ? L : 0;
-  const float* w = p.scores + (int64_t)row * p.row_stride + __ldg(p.row_starts + row);
+  const float* w = p.scores + (int64_t)row * p.row_stride + start;
   const uintptr_t a = reinterpret_cast<uintptr_t>(w);
   r.head = (int32_t)((a & 15u) >> 2);
   r.base4 = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
-  const int64_t table_row = p.row_to_batch ? (int64_t)__ldg(p.row_to_batch + row) : (int64_t)row;
+  const int64_t table_row = p.row_to_batch && row_index_ok(p, row) ? (int64_t)__ldg(p.row_to_batch + row) : (int64_t)row;
   r.page_row = p.page_table ? p.page_table + table_row * p.pt_stride : nullptr;
   return r;
+}
+
+// Checked build: quads [q, q + n) of r.base4 lie inside the row's window
+// rounded out to 16 bytes (EPQ elements a quad).
+template <int EPQ = 4>
+__device__ __forceinline__ bool window_quads_ok(const Row& r, int64_t q, int64_t n, uint32_t site) {
+  if constexpr (!kChecked) return true;
+  const int64_t nq = ((int64_t)r.L + r.head + EPQ - 1) / EPQ;
+  return in_bounds(q >= 0 && n >= 0 && q + n <= nq, site);
+}
+
+// A 16-byte window load, zero when the checked build rejects it.
+template <int EPQ = 4>
+__device__ __forceinline__ float4 load_window_quad(const Row& r, int64_t q, uint32_t site = kSiteWindowLoad) {
+  if (!window_quads_ok<EPQ>(r, q, 1, site)) return make_float4(0.f, 0.f, 0.f, 0.f);
+  return __ldg(r.base4 + q);
 }
 
 // The part of a row one CTA of a cluster owns: quads [q0, q1) of base4, window
@@ -193,9 +286,11 @@ __device__ __forceinline__ Part part_of(const Row& r, uint32_t rank, uint32_t pa
   return s;
 }
 
-// Section 1's transform: page from the high bits of j, offset from the low bits.
-__device__ __forceinline__ int32_t page_slot(const int32_t* page_row, int32_t page_bits, int32_t j) {
+// Section 1's transform: page from the high bits of j, offset from the low
+// bits (j a window index of a window of length L).
+__device__ __forceinline__ int32_t page_slot(const int32_t* page_row, int32_t page_bits, int32_t j, int32_t L) {
   if (page_row == nullptr) return j;  // no page table: the window index itself
+  if (!in_bounds((uint32_t)j < (uint32_t)L, kSitePageRead)) return 0;
   return __ldg(page_row + (j >> page_bits)) * (1 << page_bits) + (j & ((1 << page_bits) - 1));
 }
 
@@ -205,7 +300,7 @@ __device__ __forceinline__ void emit_whole_window(const Params& p, int32_t row, 
                                                   uint32_t part, uint32_t parts) {
   int32_t* o = p.out + (int64_t)row * p.k;
   for (int32_t t = (int32_t)(part * NT + threadIdx.x); t < p.k; t += (int32_t)(parts * NT))
-    o[t] = t < r.L ? page_slot(r.page_row, p.page_bits, t) : -1;
+    o[t] = t < r.L ? page_slot(r.page_row, p.page_bits, t, r.L) : -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -491,6 +586,19 @@ struct GlobalSrc {
   const float4* base4;
   int64_t q0, q1;
   int32_t head, lo, hi;
+  int32_t L;  // the row's window length
+
+  __device__ __forceinline__ float4 load(int64_t q) const {
+    if constexpr (kChecked) {
+      Row r;
+      r.L = L;
+      r.base4 = base4;
+      r.head = head;
+      r.page_row = nullptr;
+      return load_window_quad(r, q);
+    }
+    return __ldg(base4 + q);
+  }
 
   // hist[(key >> shift) & (nbins-1)] += 1 for every element whose key matches
   // prefix T under mask M.
@@ -502,7 +610,7 @@ struct GlobalSrc {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t qq = q + (int64_t)u * NT;
-        v[u] = qq < q1 ? __ldg(base4 + qq) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = qq < q1 ? load(qq) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -525,7 +633,7 @@ struct GlobalSrc {
   __device__ __forceinline__ void tile(int64_t t, uint32_t key[4], int32_t j[4], bool valid[4]) const {
     const int64_t q = q0 + t * NT + threadIdx.x;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q < q1) v = __ldg(base4 + q);
+    if (q < q1) v = load(q);
     const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -659,7 +767,7 @@ __device__ __forceinline__ Selection select_levels(SelectShared& S, const Src& s
 template <int NT, class Src>
 __device__ __forceinline__ void emit_selected(const Src& src, const Selection& sel, int32_t* out_row,
                                               uint32_t k_row, const int32_t* page_row,
-                                              int32_t page_bits, SelectShared& S, ScanParity& par) {
+                                              int32_t page_bits, int32_t L, SelectShared& S, ScanParity& par) {
   uint32_t gt_run = 0, eq_run = 0;
   const int64_t nt = src.tiles();
   for (int64_t t = 0; t < nt; ++t) {
@@ -685,7 +793,7 @@ __device__ __forceinline__ void emit_selected(const Src& src, const Selection& s
       if (is_gt[e] || (is_eq[e] && q < sel.quota)) {
         const uint32_t pos = sel.off + g + (q < sel.quota ? q : sel.quota);
         if (pos < k_row)
-          out_row[pos] = page_slot(page_row, page_bits, j[e]);
+          out_row[pos] = page_slot(page_row, page_bits, j[e], L);
         else
           atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
       }
@@ -704,14 +812,14 @@ template <int CLUSTER, int NT>
 __device__ __forceinline__ void select_from_global(const Params& p, int32_t row, const Row& r,
                                                    const Part& part, SelectShared& S,
                                                    ScanParity& par) {
-  const GlobalSrc<NT> src{r.base4, part.q0, part.q1, r.head, part.lo, part.hi};
+  const GlobalSrc<NT> src{r.base4, part.q0, part.q1, r.head, part.lo, part.hi, r.L};
   for (int b = threadIdx.x; b < kBins1; b += NT) S.hist1[b] = 0u;
   __syncthreads();
   src.histogram(S.hist1, 0u, 0u, kShift1, kBins1 - 1);
   __syncthreads();
   if constexpr (CLUSTER > 1) cluster_sync_all();
   const Selection sel = select_levels<CLUSTER, NT>(S, src, (uint32_t)p.k, par);
-  emit_selected<NT>(src, sel, p.out + (int64_t)row * p.k, (uint32_t)p.k, r.page_row, p.page_bits, S, par);
+  emit_selected<NT>(src, sel, p.out + (int64_t)row * p.k, (uint32_t)p.k, r.page_row, p.page_bits, r.L, S, par);
 }
 
 }  // namespace topk

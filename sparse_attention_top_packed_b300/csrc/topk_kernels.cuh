@@ -68,6 +68,8 @@ struct WarpProducer {
   int64_t row;      // row of the current slice
   uint32_t issued;  // chunks issued so far
   uint32_t pad_;
+  const char* wbeg;  // checked build: the row's window rounded out to 16 bytes
+  const char* wend;
 };
 
 struct StreamShared {
@@ -119,6 +121,10 @@ __device__ __noinline__ void producer_next_row(WarpProducer& P, const Params& p,
     if (sl.q1 > sl.q0) {
       P.src = reinterpret_cast<const char*>(r.base4 + sl.q0);
       P.left = (sl.q1 - sl.q0) * 16;
+      if constexpr (kChecked) {
+        P.wbeg = reinterpret_cast<const char*>(r.base4);
+        P.wend = P.wbeg + (((int64_t)r.L + r.head + 3) >> 2) * 16;
+      }
       return;
     }
   }
@@ -138,8 +144,12 @@ __device__ __forceinline__ void producer_issue(StreamShared& S, const Params& p,
   }
   const uint32_t nb = (uint32_t)min((int64_t)kChunkBytes, P.left);
   fence_proxy_async_smem();  // the warp's reads of the slot precede the async-proxy write
-  mbar_arrive_expect_tx(&S.full[w][slot], nb);
-  bulk_copy_g2s(&S.ring[w][slot][0], P.src, nb, &S.full[w][slot], policy);
+  if (!in_bounds(P.src >= P.wbeg && P.src + nb <= P.wend, kSiteWindowCopy)) {
+    mbar_arrive(&S.full[w][slot]);  // checked build: the phase completes without the copy
+  } else {
+    mbar_arrive_expect_tx(&S.full[w][slot], nb);
+    bulk_copy_g2s(&S.ring[w][slot][0], P.src, nb, &S.full[w][slot], policy);
+  }
   P.src += nb;
   P.left -= nb;
   ++P.issued;
@@ -186,8 +196,10 @@ __device__ __forceinline__ void append_flagged(StreamShared& S, int w, const flo
       atomicAdd(&S.sel.hist1[bin], 1u);
       mbin = max(mbin, bin);
     }
-    S.list_key[w][pos] = key;
-    S.list_j[w][pos] = jb + e;
+    if (in_bounds(pos < (uint32_t)kWarpCap, kSiteCandidate)) {
+      S.list_key[w][pos] = key;
+      S.list_j[w][pos] = jb + e;
+    }
     ++pos;
   }
 }
@@ -282,7 +294,7 @@ struct ListSrc {
 
 // Ordered emission from the lists: warp w's selected entries follow those of
 // warps 0..w-1 (their slices precede w's in the window).
-__device__ __forceinline__ void emit_from_lists(StreamShared& S, const Selection& sel, int32_t* out_row,
+__device__ __forceinline__ void emit_from_lists(StreamShared& S, const Selection& sel, int32_t* out_row, int32_t L,
                                                 uint32_t k_row, const int32_t* page_row,
                                                 int32_t page_bits) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -317,7 +329,7 @@ __device__ __forceinline__ void emit_from_lists(StreamShared& S, const Selection
     if (is_gt || (is_eq && ql < sel.quota)) {
       const uint32_t pos = sel.off + gl + (ql < sel.quota ? ql : sel.quota);
       if (pos < k_row)
-        out_row[pos] = page_slot(page_row, page_bits, S.list_j[w][i]);
+        out_row[pos] = page_slot(page_row, page_bits, S.list_j[w][i], L);
       else
         atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
     }
@@ -327,11 +339,11 @@ __device__ __forceinline__ void emit_from_lists(StreamShared& S, const Selection
 }
 
 template <int CLUSTER>
-__device__ __noinline__ void finish_from_lists(const Params& p, int64_t row, const int32_t* page_row,
+__device__ __noinline__ void finish_from_lists(const Params& p, int64_t row, const int32_t* page_row, int32_t L,
                                                StreamShared& S, ScanParity& par) {
   const ListSrc src{&S};
   const Selection sel = select_levels<CLUSTER, kStreamThreads>(S.sel, src, (uint32_t)p.k, par);
-  emit_from_lists(S, sel, p.out + row * p.k, (uint32_t)p.k, page_row, p.page_bits);
+  emit_from_lists(S, sel, p.out + row * p.k, L, (uint32_t)p.k, page_row, p.page_bits);
 }
 
 template <int CLUSTER>
@@ -360,7 +372,7 @@ __device__ __noinline__ uint32_t stream_sample_threshold(StreamShared& S, const 
   };
   for (int64_t s = tid; s < ns; s += kStreamThreads) {
     const int64_t q = quad(s);
-    const float4 v = __ldg(r.base4 + q);
+    const float4 v = load_window_quad(r, q, kSiteSampleLoad);
 #pragma unroll
     for (int e = 0; e < 4; ++e) atomicAdd(&S.sel.hist1[key_at(q, v, e) >> kShift1], 1u);
   }
@@ -370,7 +382,7 @@ __device__ __noinline__ uint32_t stream_sample_threshold(StreamShared& S, const 
   const Pick a = block_pick<kBins1, 1, kStreamThreads>(S.sel.hist1, R, par.next(S.sel), par.next_pick(S.sel));
   for (int64_t s = tid; s < ns; s += kStreamThreads) {
     const int64_t q = quad(s);
-    const float4 v = __ldg(r.base4 + q);
+    const float4 v = load_window_quad(r, q, kSiteSampleLoad);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t key = key_at(q, v, e);
@@ -405,6 +417,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
     P.left = 0;
     P.src = nullptr;
     P.issued = 0;
+    P.wbeg = P.wend = nullptr;
     for (uint32_t s = 0; s < (uint32_t)kStages; ++s) producer_issue<CLUSTER>(S, p, ncl, rank, w, s, policy);
   }
   __syncthreads();
@@ -485,7 +498,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
       if (lane == 0) producer_issue<CLUSTER>(S, p, ncl, rank, w, slot, policy);
       if (!over && (c <= 3 || (c & 3) == 0)) warp_raise_threshold(S, k, mbin);
     }
-    if (lane == 0) S.count[w] = over ? 0u : count;
+    if (lane == 0) S.count[w] = over || !in_bounds(count <= (uint32_t)kWarpCap, kSiteRegion) ? 0u : count;
 
     // ---- end of the row's stream: select on the lists, or fall back when a
     // list overflowed or the sampled threshold left fewer than k candidates
@@ -511,7 +524,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(Params p
     if (any_over)
       finish_from_global<CLUSTER>(p, row, r, part, S.sel, par);
     else
-      finish_from_lists<CLUSTER>(p, row, r.page_row, S, par);
+      finish_from_lists<CLUSTER>(p, row, r.page_row, r.L, S, par);
   }
 
   // Every issued chunk was waited for, so nothing is in flight -- unless a

@@ -453,13 +453,13 @@ __device__ __forceinline__ void take_half(const Row& r, int64_t nq, int64_t cq, 
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int64_t q = cq + threadIdx.x + (2 * h + u) * kThreads;
-      v[u] = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = q < nq ? load_window_quad(r, q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     x[0] = v[0].x; x[1] = v[0].y; x[2] = v[0].z; x[3] = v[0].w;
     x[4] = v[1].x; x[5] = v[1].y; x[6] = v[1].z; x[7] = v[1].w;
   } else {
     const int64_t q = cq + threadIdx.x + h * kThreads;
-    const float4 v = q < nq ? __ldg(r.base4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 v = q < nq ? load_window_quad<E::kPerQuad>(r, q) : make_float4(0.f, 0.f, 0.f, 0.f);
     float y[8];
     E::decode(v, y);
 #pragma unroll
@@ -526,8 +526,10 @@ __device__ __forceinline__ void append(Shared& S, const float x[8], uint32_t m, 
   for (uint32_t mm = m; mm; mm &= mm - 1u) {
     const int e = __ffs(mm) - 1;
     const uint32_t key = key_of(pick8(x, e));
-    S.bkey[pos] = key;
-    S.bj[pos] = index8<E>(jb0, e);
+    if (in_bounds(pos < (uint32_t)kCap, kSiteCandidate)) {
+      S.bkey[pos] = key;
+      S.bj[pos] = index8<E>(jb0, e);
+    }
     ++pos;
     atomicAdd(&S.hist2[key >> 21], 1u);
   }
@@ -632,7 +634,7 @@ __device__ __noinline__ void emit_selected(Shared& S, const Params& p, const Row
       uint32_t pos = pos0 + incl - c;
       for (uint32_t b = word; b; b &= b - 1u) {
         if (pos < k)
-          o[pos] = page_slot(r.page_row, p.page_bits, seg_lo + i * 32 + (__ffs(b) - 1));
+          o[pos] = page_slot(r.page_row, p.page_bits, seg_lo + i * 32 + (__ffs(b) - 1), r.L);
         else
           atomicOr(&g_device_flags, kFlagBadOutputPosition);  // never expected
         ++pos;
@@ -669,7 +671,8 @@ struct RowRaw {
 };
 
 __device__ __forceinline__ RowRaw load_row_raw(const Params& p, int64_t row) {
-  RowRaw x;
+  RowRaw x = {0, 0, (int32_t)row};
+  if (!row_index_ok(p, row)) return x;
   x.L = __ldg(p.seq_lens + row);
   x.start = __ldg(p.row_starts + row);
   x.table_row = p.row_to_batch ? __ldg(p.row_to_batch + row) : (int32_t)row;
@@ -690,6 +693,7 @@ __device__ __forceinline__ int64_t quads_of(const Row& r) {
 
 template <class E = ElemF32>
 __device__ __forceinline__ Row make_row(const Params& p, int64_t row, const RowRaw& x) {
+  check_row_window(p, x.L, x.start);
   Row r;
   r.L = x.L > 0 ? x.L : 0;
   const uintptr_t a = elem_addr<E>(p, row, x.start);
@@ -709,6 +713,8 @@ struct WCursor {
   uint32_t issued;
   int32_t lo, hi;        // the CTA's rows
   const uint32_t* bits;  // which of them need a selection (sched::balanced_range)
+  const float4* wbeg;    // checked build: the row's window rounded out to 16 bytes
+  const float4* wend;
 };
 
 // Whole warp: moves the cursor to the block of its next row with seq_len > k
@@ -726,17 +732,26 @@ __device__ __forceinline__ bool cursor_next_row(WCursor& cur, const Params& p, i
   if (row == ahead_row) {
     L = ahead.L;
     st = ahead.start;
-  } else {
+  } else if (row_index_ok(p, row)) {
     L = __ldg(p.seq_lens + row);
     st = __ldg(p.row_starts + row);
+  } else {
+    L = 0;
+    st = 0;
   }
+  check_row_window(p, L, st);
   cur.row = (int32_t)row;
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.scores + row * p.row_stride + st);
   const int32_t head = (int32_t)((a & 15u) >> 2);
   int64_t q0, q1;
-  warp_block(((int64_t)L + head + 3) >> 2, w, q0, q1);
+  const int64_t nq = ((int64_t)L + head + 3) >> 2;
+  warp_block(nq, w, q0, q1);
   cur.src = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u) + q0;
   cur.left = (int32_t)(q1 - q0);
+  if constexpr (kChecked) {
+    cur.wbeg = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
+    cur.wend = cur.wbeg + nq;
+  }
   return true;
 }
 
@@ -750,8 +765,12 @@ __device__ __forceinline__ bool warp_issue(Ring<NS>& R, WCursor& cur, const Para
   const uint32_t s = cur.issued % NS;
   const uint32_t nquads = (uint32_t)min(kWChunkQuads, cur.left);
   if ((threadIdx.x & 31) == 0) {
-    mbar_arrive_expect_tx(&R.full[w][s], nquads * 16u);
-    bulk_copy_g2s(&R.st[w][s][0], cur.src, nquads * 16u, &R.full[w][s], policy);
+    if (!in_bounds(cur.src >= cur.wbeg && cur.src + nquads <= cur.wend, kSiteWindowCopy)) {
+      mbar_arrive(&R.full[w][s]);  // checked build: the phase completes without the copy
+    } else {
+      mbar_arrive_expect_tx(&R.full[w][s], nquads * 16u);
+      bulk_copy_g2s(&R.st[w][s][0], cur.src, nquads * 16u, &R.full[w][s], policy);
+    }
   }
   cur.src += nquads;
   cur.left -= nquads;
@@ -774,14 +793,17 @@ struct Deferred {
   uint32_t next;            // this lane's next position to load; next - 32 and
   uint32_t first, end;      // next - 64 are in the pipeline if in [first, end)
   int32_t ja, jb, pgb;
+  int32_t L;                // the row's window length
 };
 
 // The indices of the row were written by every warp: a consumer barrier must
 // separate that emission from the first deferred_step / deferred_flush.
-__device__ __forceinline__ void deferred_start(Deferred& d, int32_t* o, const int32_t* page_row, uint32_t k) {
+__device__ __forceinline__ void deferred_start(Deferred& d, int32_t* o, const int32_t* page_row, uint32_t k,
+                                               int32_t L) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   d.o = o;
   d.page_row = page_row;
+  d.L = L;
   d.first = (uint32_t)((uint64_t)k * w / kWarps) + lane;
   d.next = d.first;
   d.end = (uint32_t)((uint64_t)k * (w + 1) / kWarps);
@@ -795,7 +817,7 @@ __device__ __forceinline__ void deferred_step(Deferred& d, int32_t page_bits) {
   if (tb >= d.first && tb < d.end) __stcg(d.o + tb, d.pgb * (1 << page_bits) + (d.jb & ((1 << page_bits) - 1)));
   if (ta >= d.first && ta < d.end) {
     d.jb = d.ja;
-    d.pgb = __ldg(d.page_row + (d.ja >> page_bits));
+    d.pgb = in_bounds((uint32_t)d.ja < (uint32_t)d.L, kSitePageRead) ? __ldg(d.page_row + (d.ja >> page_bits)) : 0;
   }
   if (d.next < d.end) d.ja = __ldcg(d.o + d.next);  // written by other warps before a barrier (read from L2)
   d.next += 32u;
@@ -915,11 +937,16 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
             const int e1 = (int)(kBits <= 32 ? __ffs((uint32_t)mm) : __ffsll((unsigned long long)mm)) - 1;
             const uint32_t x0 = E::bits_at(sf, e0);
             const uint32_t x1 = e1 >= 0 ? E::bits_at(sf, e1) : 0u;
-            rraw[pos] = x0;
-            rj[pos] = jb + e0;
+            // the lane's positions lie below wcnt + tot (checked build)
+            if (in_bounds(pos < wcnt + tot, kSiteCandidate)) {
+              rraw[pos] = x0;
+              rj[pos] = jb + e0;
+            }
             if (e1 >= 0) {
-              rraw[pos + 1] = x1;
-              rj[pos + 1] = jb + e1;
+              if (in_bounds(pos + 1 < wcnt + tot, kSiteCandidate)) {
+                rraw[pos + 1] = x1;
+                rj[pos + 1] = jb + e1;
+              }
               mm &= mm - 1u;
             }
             pos += e1 >= 0 ? 2u : 1u;
@@ -955,7 +982,8 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
 __device__ __forceinline__ void keys_and_histogram(Shared& S) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   __syncwarp();  // the region's count was written by one lane of this warp
-  const uint32_t base = S.rbase[w], cnt = S.rcnt[w];
+  const uint32_t base = S.rbase[w];
+  const uint32_t cnt = in_bounds(base + S.rcnt[w] <= (uint32_t)kCap, kSiteRegion) ? S.rcnt[w] : 0u;
   const uint32_t tk = S.fh_tk, sh = S.fh_sh;
   uint32_t top = 0;
   for (uint32_t i0 = 0; i0 < cnt; i0 += 128) {  // 4 entries a lane, loads issued together
@@ -1084,7 +1112,7 @@ __device__ __forceinline__ void publish_hint(Shared& S, uint32_t hr, uint32_t hi
 
 // Where an emission puts the t-th selected window index j of a row.
 // OutRaw: j itself, into the output row in global memory (the page transform
-// follows separately).
+// follows separately; positions below k are the caller's guarantee).
 struct OutRaw {
   int32_t* o;
   __device__ __forceinline__ void put(uint32_t q, int32_t j) const { __stcg(o + q, j); }
@@ -1092,26 +1120,9 @@ struct OutRaw {
 
 // OutShared: j itself, into a staging row in shared memory.
 struct OutShared {
-  int32_t* o;
-  __device__ __forceinline__ void put(uint32_t q, int32_t j) const { o[q] = j; }
-};
-
-// OutPaged: the final value, page_row[j >> page_bits] * page_size + the
-// offset (section 1 of the page), the page read from a shared-memory copy of
-// the page-table row when there is one, else from global memory; j itself
-// without a page table.
-struct OutPaged {
-  int32_t* o;
-  const int32_t* stage;     // page_row[0 ..] in shared memory, or null
-  const int32_t* page_row;  // the row's page-table row, or null (raw indices)
-  int32_t page_bits;
+  int32_t* o;  // kBins2 entries
   __device__ __forceinline__ void put(uint32_t q, int32_t j) const {
-    int32_t v = j;
-    if (page_row != nullptr) {
-      const int32_t pg = stage != nullptr ? stage[j >> page_bits] : __ldg(page_row + (j >> page_bits));
-      v = pg * (1 << page_bits) + (j & ((1 << page_bits) - 1));
-    }
-    __stcg(o + q, v);
+    if (in_bounds(q < (uint32_t)kBins2, kSiteStaging)) o[q] = j;
   }
 };
 
@@ -1130,7 +1141,7 @@ struct OutPaged {
 // cannot settle it: the rank lies above its range, or more than 32 candidates
 // share its bin.  Also proposes the next row's hint (rank hr) and fine shift.
 //
-// `out`: where the row's k selected window indices go (OutRaw, OutPaged).
+// `out`: where the row's k selected window indices go (OutRaw, OutShared).
 template <class Out>
 __device__ __forceinline__ bool select_emit_fine(Shared& S, const Out& out, int32_t L, uint32_t n, uint32_t k,
                                                  uint32_t hr) {
@@ -1329,7 +1340,7 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Out& out, int3
 // Fast rows whose selection took the generic path: every warp's region is in
 // ascending window index and the regions follow each other in warp order, so
 // the selected entries' output positions are prefix counts.
-// `out`: where the selected window indices go (OutRaw, OutPaged).
+// `out`: where the selected window indices go (OutRaw, OutShared).
 template <class Out>
 __device__ __forceinline__ void emit_ordered(Shared& S, const Out& out, uint32_t k, const Rule sel) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -1405,7 +1416,7 @@ __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const 
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int64_t s = s0 + (int64_t)u * kThreads;
-      v[u] = s < ns ? __ldg(r.base4 + sample_quad(s, ns, nq)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = s < ns ? load_window_quad<EPQ>(r, sample_quad(s, ns, nq), kSiteSampleLoad) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -1451,7 +1462,8 @@ __device__ __noinline__ void sample_threshold(Shared& S, const Params& p, const 
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int64_t s = s0 + (int64_t)u * kThreads;
-        v[u] = s < ns ? __ldg(r.base4 + sample_quad(s, ns, nq)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = s < ns ? load_window_quad<EPQ>(r, sample_quad(s, ns, nq), kSiteSampleLoad)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -1540,6 +1552,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
   cur.lo = (int32_t)lo;
   cur.hi = (int32_t)hi;
   cur.bits = M.range.bits;
+  cur.wbeg = cur.wend = nullptr;
   for (int s = 0; s < kWStages; ++s) warp_issue(R, cur, p, w, policy, lo, nx);
   test_unsatisfied_wait(p, &M.never, timed_out);
 
@@ -1641,7 +1654,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
     if (tid == 0 && !emitted) publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
     if (!redo) {
       if (!emitted) emit_ordered(S, OutRaw{p.out + row * p.k}, k, sel);
-      if (r.page_row != nullptr) deferred_start(dfr, p.out + row * p.k, r.page_row, k);  // else j is final
+      if (r.page_row != nullptr) deferred_start(dfr, p.out + row * p.k, r.page_row, k, r.L);  // else j is final
     } else {
       emit_selected(S, p, r, row, sel);
     }

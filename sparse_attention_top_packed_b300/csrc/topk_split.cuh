@@ -152,7 +152,19 @@ struct SCursor {
   int32_t nL, nstart; // its descriptor, loaded ahead
   int64_t lo, hi;
   const uint32_t* bits;
+  const float4* wbeg;  // checked build: the row's window rounded out to 16 bytes
+  const float4* wend;
 };
+
+// The descriptor of row c.nrow (in the CTA's range), loaded ahead.
+__device__ __forceinline__ void scursor_load_next(SCursor& c, const Params& p) {
+  c.nL = 0;
+  c.nstart = 0;
+  if (c.nrow < c.hi && row_index_ok(p, c.nrow)) {
+    c.nL = __ldg(p.seq_lens + c.nrow);
+    c.nstart = __ldg(p.row_starts + c.nrow);
+  }
+}
 
 __device__ __forceinline__ void scursor_init(SCursor& c, const Params& p, int64_t lo, int64_t hi,
                                              const uint32_t* bits) {
@@ -162,13 +174,9 @@ __device__ __forceinline__ void scursor_init(SCursor& c, const Params& p, int64_
   c.lo = lo;
   c.hi = hi;
   c.bits = bits;
+  c.wbeg = c.wend = nullptr;
   c.nrow = sched::next_selected_row(p, bits, lo, hi, lo);
-  c.nL = 0;
-  c.nstart = 0;
-  if (c.nrow < hi) {
-    c.nL = __ldg(p.seq_lens + c.nrow);
-    c.nstart = __ldg(p.row_starts + c.nrow);
-  }
+  scursor_load_next(c, p);
 }
 
 // Moves to the block of row c.nrow and loads the descriptor of the row after
@@ -177,17 +185,20 @@ template <class E>
 __device__ __forceinline__ bool scursor_advance(SCursor& c, const Params& p, int w) {
   if (c.nrow >= c.hi) return false;
   const int64_t row = c.nrow;
+  check_row_window(p, c.nL, c.nstart);
   const uintptr_t a = elem_addr<E>(p, row, c.nstart);
   const int32_t head = (int32_t)((a & 15u) / E::kBytes);
   int64_t q0, q1;
-  warp_block_of<kSW>(((int64_t)c.nL + head + E::kPerQuad - 1) / E::kPerQuad, w, q0, q1);
+  const int64_t nq = ((int64_t)(c.nL > 0 ? c.nL : 0) + head + E::kPerQuad - 1) / E::kPerQuad;
+  warp_block_of<kSW>(nq, w, q0, q1);
   c.src = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u) + q0;
   c.left = (int32_t)(q1 - q0);
-  c.nrow = sched::next_selected_row(p, c.bits, c.lo, c.hi, row + 1);
-  if (c.nrow < c.hi) {
-    c.nL = __ldg(p.seq_lens + c.nrow);
-    c.nstart = __ldg(p.row_starts + c.nrow);
+  if constexpr (kChecked) {
+    c.wbeg = reinterpret_cast<const float4*>(a & ~(uintptr_t)15u);
+    c.wend = c.wbeg + nq;
   }
+  c.nrow = sched::next_selected_row(p, c.bits, c.lo, c.hi, row + 1);
+  scursor_load_next(c, p);
   return true;
 }
 
@@ -202,8 +213,12 @@ __device__ __forceinline__ bool scursor_issue(typename SplitSmem<E>::RingT& R, S
   const uint32_t s = c.issued % kStages;
   const uint32_t nquads = (uint32_t)min(kChunk, c.left);
   if ((threadIdx.x & 31) == 0) {
-    mbar_arrive_expect_tx(&R.full[w][s], nquads * 16u);
-    bulk_copy_g2s(&R.st[w][s][0], c.src, nquads * 16u, &R.full[w][s], policy);
+    if (!in_bounds(c.src >= c.wbeg && c.src + nquads <= c.wend, kSiteWindowCopy)) {
+      mbar_arrive(&R.full[w][s]);  // checked build: the phase completes without the copy
+    } else {
+      mbar_arrive_expect_tx(&R.full[w][s], nquads * 16u);
+      bulk_copy_g2s(&R.st[w][s][0], c.src, nquads * 16u, &R.full[w][s], policy);
+    }
   }
   c.src += nquads;
   c.left -= nquads;
@@ -414,7 +429,14 @@ __device__ __forceinline__ void finish_row(SplitSmem<E>& M, uint32_t b, const Pa
       const int t = tid + u * kThreads;
       // a staged index is always inside the window; the test only keeps a
       // broken hand-over from reading outside the page-table row
-      const bool ok = t < (int)k && pr != nullptr && (uint32_t)jv[u] < (uint32_t)r.L;
+      bool ok = t < (int)k && pr != nullptr && (uint32_t)jv[u] < (uint32_t)r.L;
+      if constexpr (kChecked) {
+        if (t < (int)k && pr != nullptr) {
+          ok = in_bounds((uint32_t)jv[u] < (uint32_t)r.L, kSitePageRead);
+          if (ok && ps.staged)
+            ok = in_bounds((jv[u] >> pb) < ps.count && ps.off + (jv[u] >> pb) < kPageStage, kSitePageStage);
+        }
+      }
       pg[u] = ok ? (ps.staged ? pst[jv[u] >> pb] : __ldg(pr + (jv[u] >> pb))) : 0;
     }
 #pragma unroll

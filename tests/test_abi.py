@@ -45,6 +45,26 @@ def test_library_exports_nothing_else(lib):
     assert exported == set(declared_functions())
 
 
+def test_checked_library_exports_the_same_functions(lib):
+    """The bounds-checked build is the same ABI."""
+    path = binding.library_path(checked=True)
+    assert os.path.exists(path)
+    checked = ctypes.CDLL(path)
+    assert all(hasattr(checked, n) for n in declared_functions())
+    out = os.popen(f"nm -D --defined-only {path}").read()
+    assert {line.split()[-1] for line in out.splitlines() if " T " in line} == set(declared_functions())
+    with binding.checked_build():
+        assert binding.library_path() == path
+        assert binding.topk_status_string(0)
+    assert binding.library_path() != path
+
+
+def test_check_site_field():
+    assert binding.check_site(binding.FLAG_OUT_OF_BOUNDS | (5 << 8)) == 5
+    assert binding.check_site(binding.FLAG_STREAM_WAIT_TIMEOUT) == 0
+    assert set(binding.CHECK_SITES) == set(range(1, 11))
+
+
 def test_status_strings(lib):
     for code, name in binding.STATUS_NAMES.items():
         assert binding.topk_status_string(code)
@@ -111,8 +131,8 @@ def test_null_page_table_means_raw_indices_and_frees_page_arguments(lib):
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
-    monkeypatch.setattr(binding, "_lib", None)
-    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
+    monkeypatch.setattr(binding, "_libs", {})
+    monkeypatch.setattr(binding, "library_path", lambda checked=None: str(tmp_path / "missing.so"))
     with pytest.raises(binding.TopkError):
         binding.topk_status_string(0)
 
