@@ -1137,9 +1137,15 @@ struct OutShared {
 // largest pair T; each warp's output position is the prefix of the warps'
 // selected counts, and its compacted candidates are written with ballots.
 //
-// Returns false (uniformly, before touching the buffer) when the histogram
-// cannot settle it: the rank lies above its range, or more than 32 candidates
-// share its bin.  Also proposes the next row's hint (rank hr) and fine shift.
+// A split bin of more than 32 candidates that share one key (ties, common
+// with bf16 scores) is settled by window order (the lowest indices win); one
+// with several keys is narrowed by a second fine level over its entries.
+//
+// Returns false (uniformly) when the histograms cannot settle it: the rank
+// lies above the fine range (before the buffer is touched), or the second
+// level's target still holds more than 32 candidates of several keys (the
+// regions are then compacted: every entry at or above the first bin kept).
+// Also proposes the next row's hint (rank hr) and fine shift.
 //
 // `out`: where the row's k selected window indices go (OutRaw, OutShared).
 template <class Out>
@@ -1175,10 +1181,8 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Out& out, int3
   }
   const uint32_t rem = r - pk.above;     // rank of the k-th largest inside its bin, 1 <= rem <= count
   const bool split = pk.count != rem;    // only part of the bin is taken
-  // more than 32 entries in a split bin: too many to rank in a warp.  When
-  // they all share one key (ties, common with bf16 scores) the lowest window
-  // indices win, which prefix counts settle; otherwise the generic selection
-  // runs on the compacted buffer (it keeps every entry at or above the bin).
+  // more than 32 entries in a split bin: too many to rank in a warp (settled
+  // by window order when they share one key, else by a second fine level)
   const bool crowded = split && pk.count > 32u;
 
   // compaction of the warp's region to the entries at or above the bin, in
@@ -1253,41 +1257,117 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Out& out, int3
   }
   if (threadIdx.x == 0) publish_hint(S, hr, hint_ok, hint, hint_sh, true, n, k, L);
   cbar();
-  // a crowded bin with several keys: the generic selection, on the compacted
-  // regions (uniform: every warp reads the same published ranges)
-  uint32_t quota = 0u;  // crowded single-key bin: this warp's entries of the bin that are taken
+  // The target: bin t_bin of bins of 2^t_sh keys from tk, of which the t_rem
+  // largest pairs are taken.  A crowded bin with several keys is narrowed by a
+  // second fine level over its entries: 2^11 sub-bins of it (single keys when
+  // the bin is narrower), picked like the first.  Uniform: every warp reads
+  // the same published ranges and histograms.
+  uint32_t t_sh = sh, t_bin = bin, t_rem = rem, t_count = pk.count, t_cin = cin;
+  bool t_split = split, t_crowded = crowded;
   if (crowded) {
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u, before = 0u;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
     for (int x = 0; x < kWarps; ++x) {
       lo = min(lo, S.wkmin[x]);
       hi = max(hi, S.wkmax[x]);
-      before += x < w ? S.wcin[x] : 0u;
     }
-    if (lo != hi) return false;
-    quota = rem > before ? min(rem - before, cin) : 0u;
+    if (lo != hi) {
+      const uint32_t ssh = sh > 11u ? sh - 11u : 0u;
+      const uint32_t smask = (1u << (sh - ssh)) - 1u;
+      for (int i = threadIdx.x; i < kBins2 / 4; i += kThreads)
+        reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0u, 0u, 0u, 0u);
+      cbar();  // also: every warp has read the published ranges above
+      for (uint32_t i = lane; i < wc; i += 32) {
+        const uint32_t off = rkey[i] - tk;
+        if ((off >> sh) == bin) atomicAdd(&S.hist2[(off >> ssh) & smask], 1u);
+      }
+      cbar();
+      fine_publish(S, S.hist2);
+      cbar();
+      fine_totals(S, tot);
+      const FinePick q2 = fine_find(S, S.hist2, tot, rem);
+      t_sh = ssh;
+      t_bin = (bin << (sh - ssh)) | q2.bin;
+      t_rem = rem - q2.above;  // 1 <= t_rem <= t_count
+      t_count = q2.count;
+      t_split = t_count != t_rem;
+      t_crowded = t_split && t_count > 32u;
+      // this warp's entries above the sub-bin and in it (gathered for ranking,
+      // or with their key range when crowded)
+      uint32_t n_above = 0u, n_in = 0u;
+      kmin = 0xFFFFFFFFu;
+      kmax = 0u;
+      for (uint32_t i0 = 0; i0 < wc; i0 += 32) {
+        const uint32_t i = i0 + (uint32_t)lane;
+        const uint32_t key = i < wc ? rkey[i] : 0u;
+        const uint32_t o2 = (key - tk) >> t_sh;
+        const bool ab = i < wc && o2 > t_bin, inb = i < wc && o2 == t_bin;
+        n_above += __popc(__ballot_sync(0xFFFFFFFFu, ab));
+        n_in += __popc(__ballot_sync(0xFFFFFFFFu, inb));
+        if (inb) {
+          kmin = min(kmin, key);
+          kmax = max(kmax, key);
+          if (t_split && !t_crowded) {
+            const uint32_t at = atomicAdd(&S.res_n, 1u);
+            if (at < 32u) {  // fewer than t_count <= 32 are gathered
+              S.res_key[at] = key;
+              S.res_j[at] = rj[i];
+              S.res_w[at] = (uint32_t)w;
+            }
+          }
+        }
+      }
+      kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+      kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+      t_cin = t_split ? n_in : 0u;
+      if (lane == 0) {
+        S.wtot[w] = n_above + (t_split ? 0u : n_in);  // selected for sure
+        S.wcin[w] = t_cin;
+        S.wkmin[w] = kmin;
+        S.wkmax[w] = kmax;
+      }
+      cbar();
+      if (t_crowded) {
+        lo = 0xFFFFFFFFu;
+        hi = 0u;
+#pragma unroll
+        for (int x = 0; x < kWarps; ++x) {
+          lo = min(lo, S.wkmin[x]);
+          hi = max(hi, S.wkmax[x]);
+        }
+        // still several keys: the generic selection, on the compacted regions
+        if (lo != hi) return false;
+      }
+    }
+  }
+  uint32_t quota = 0u;  // crowded single-key target: this warp's entries of it that are taken
+  if (t_crowded) {
+    uint32_t before = 0u;
+#pragma unroll
+    for (int x = 0; x < kWarps; ++x) before += x < w ? S.wcin[x] : 0u;
+    quota = t_rem > before ? min(t_rem - before, t_cin) : 0u;
   }
 
-  // the bin's candidates, ranked: the rem-th largest pair is the threshold T
+  // the target's candidates, ranked: the t_rem-th largest pair is the threshold T
   uint64_t T = 0ull;
   uint32_t pos = 0;
-  if (crowded) {
-    // warp x takes min(max(rem - (bin entries of warps < x), 0), its own)
+  if (t_crowded) {
+    // warp x takes min(max(t_rem - (target entries of warps < x), 0), its own)
     uint32_t acc = 0u;
 #pragma unroll
     for (int x = 0; x < kWarps; ++x) {
       const uint32_t c = S.wcin[x];
-      const uint32_t q = rem > acc ? min(rem - acc, c) : 0u;
+      const uint32_t q = t_rem > acc ? min(t_rem - acc, c) : 0u;
       pos += x < w ? q : 0u;
       acc += c;
     }
-  } else if (split) {
-    const uint32_t m = pk.count;  // == S.res_n
+  } else if (t_split) {
+    const uint32_t m = t_count;  // == S.res_n
     const uint64_t mine = lane < (int)m ? pair_of(S.res_key[lane], S.res_j[lane]) : 0ull;
     const uint32_t mw = lane < (int)m ? S.res_w[lane] : (uint32_t)kWarps;
     uint32_t above = 0;
     for (uint32_t o = 0; o < m; ++o) above += __shfl_sync(0xFFFFFFFFu, mine, o) > mine ? 1u : 0u;
-    const uint32_t tb = __ballot_sync(0xFFFFFFFFu, lane < (int)m && above == rem - 1u);
+    const uint32_t tb = __ballot_sync(0xFFFFFFFFu, lane < (int)m && above == t_rem - 1u);
     T = __shfl_sync(0xFFFFFFFFu, mine, __ffs(tb) - 1);
     pos = __popc(__ballot_sync(0xFFFFFFFFu, lane < (int)m && mine >= T && mw < (uint32_t)w));
   }
@@ -1298,7 +1378,7 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Out& out, int3
   // ballots first, then the stores
   // o: the output row (or its staging copy)
   bool bad = false;
-  uint32_t seen = 0u;  // crowded bin: its entries met so far in this warp's region
+  uint32_t seen = 0u;  // crowded target: its entries met so far in this warp's region
   for (uint32_t i0 = 0; i0 < wc; i0 += 4 * 32) {
     uint32_t key[4], bm[4];
     int32_t jj[4];
@@ -1311,15 +1391,16 @@ __device__ __forceinline__ bool select_emit_fine(Shared& S, const Out& out, int3
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const uint32_t i = i0 + 32u * u + (uint32_t)lane;
-      const bool above = ((key[u] - tk) >> sh) > bin;
+      const uint32_t o2 = (key[u] - tk) >> t_sh;
+      const bool above = o2 > t_bin, inb = o2 == t_bin;
       bool take;
-      if (crowded) {
-        // the bin's entries in window order: the first `quota` are taken
-        const uint32_t bi = __ballot_sync(0xFFFFFFFFu, i < wc && !above);
-        take = i < wc && (above || seen + __popc(bi & lt) < quota);
+      if (t_crowded) {
+        // the target's entries in window order: the first `quota` are taken
+        const uint32_t bi = __ballot_sync(0xFFFFFFFFu, i < wc && inb);
+        take = i < wc && (above || (inb && seen + __popc(bi & lt) < quota));
         seen += __popc(bi);
       } else {
-        take = i < wc && (!split || above || pair_of(key[u], jj[u]) >= T);
+        take = i < wc && (above || (inb && (!t_split || pair_of(key[u], jj[u]) >= T)));
       }
       bm[u] = __ballot_sync(0xFFFFFFFFu, take);
     }

@@ -294,6 +294,25 @@ def test_pipe_threshold_carried_between_rows(cuda_device, kind, ctas, path):
     assert bad.size == 0, f"rows {bad.tolist()} differ"
 
 
+@pytest.mark.parametrize("lo,hi", [(2300, 6000), (3900, 4400), (2100, 2600)])
+@pytest.mark.parametrize("ctas", [1, 2])
+@pytest.mark.parametrize("path", ["pipe", "split"])
+def test_short_bf16_rows_in_sequence(cuda_device, lo, hi, ctas, path):
+    """Rows a little longer than k with bf16-rounded scores, one after another
+    on one or two CTAs (thresholds carried from row to row): the k-th largest
+    sits where bins of keys hold many distinct values, so the selection's
+    first fine level meets crowded bins of several keys and its second level
+    (or the generic selection) settles them."""
+    rng = np.random.default_rng(lo * 7 + hi)
+    lens = rng.integers(lo, hi + 1, size=48)
+    p = wl.random_problem(rng, rows=48, max_len=hi, k=2048, page_size=64, values="bf16", slack=5,
+                          forced_lens=lens)
+    w = host_problem_to_device(p, cuda_device)
+    got = run(w, path=path, max_ctas=ctas).cpu().numpy()
+    bad = np.nonzero((got != oracle_host(p)).any(axis=1))[0]
+    assert bad.size == 0, f"rows {bad.tolist()} differ"
+
+
 RAW_CASES = [
     # values, rows, max_len, k: several rows per CTA on one or two CTAs, windows
     # shorter than k among them, so the row-to-row paths run without a table
