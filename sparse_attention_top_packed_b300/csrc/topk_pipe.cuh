@@ -974,13 +974,14 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
   }
 }
 
-// Warp w, after the stream of a fast row (its region's count published):
-// turns the region's raw float bits into keys in place and counts them in the
-// fine histogram (hist2, zero beforehand; bins of 2^fh_sh keys from fh_tk),
-// keys above its range in S.wtop[w].  Touches only region w and hist2 (by
-// atomics); a consumer barrier must follow before the selection.
-__device__ __forceinline__ void keys_and_histogram(Shared& S) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+// The warp that streamed region w, after the stream of a fast row (the
+// region's count published by its lane 0): turns the region's raw float bits
+// into keys in place and counts them in the fine histogram (hist2, zero
+// beforehand; bins of 2^fh_sh keys from fh_tk), keys above its range in
+// S.wtop[w].  Touches only region w and hist2 (by atomics); a barrier must
+// follow before the selection.
+__device__ __forceinline__ void keys_and_histogram(Shared& S, int w) {
+  const int lane = threadIdx.x & 31;
   __syncwarp();  // the region's count was written by one lane of this warp
   const uint32_t base = S.rbase[w];
   const uint32_t cnt = in_bounds(base + S.rcnt[w] <= (uint32_t)kCap, kSiteRegion) ? S.rcnt[w] : 0u;
@@ -1678,7 +1679,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_pipe_kernel(const __grid_const
       deferred_step(dfr, p.page_bits);
     });
     deferred_flush(dfr, p.page_bits);  // the previous fast row's transform, if unfinished
-    keys_and_histogram(S);  // this warp's region, written by this warp
+    keys_and_histogram(S, w);  // this warp's region, written by this warp
     if (w == 0) {
       // the CTA's next row that needs a selection, for the hint
       int32_t nl = has_next && nx.L > p.k ? nx.L : 0;

@@ -10,21 +10,23 @@
 // end of a row:
 //
 //  * Streaming warps (warps 8 on) only stream: each takes its block of a row
-//    through its own ring of 4 KB stages (128 KB in flight per SM) into its
-//    part of one of two row states ("sets"), then hands the set over and goes
-//    on with the next row in the other set.  Their loop only compares and
-//    appends raw candidates (topk_pipe.cuh, stream_row_wb).  Their rings run
-//    ahead on their own: each warp's cursor finds the next row in the CTA's
-//    bitmask and has its descriptor loaded a row ahead, so a row change costs
-//    no round trip.
+//    through its own ring of TMA stages (two of 8 KB for 32-bit scores, four
+//    of 4 KB for 16-bit ones: 128 KB in flight per SM) into its part of one
+//    of two row states ("sets"), then hands the set over and goes on with the
+//    next row in the other set.  Their loop only compares and appends raw
+//    candidates (topk_pipe.cuh, stream_row_wb); for a row shorter than
+//    kKeysOnStreamMaxLen they also turn their parts into keys and the fine
+//    histogram before the hand-over.  Their rings run ahead on their own: each
+//    warp's cursor finds the next row in the CTA's bitmask and has its
+//    descriptor loaded a row ahead, so a row change costs no round trip.
 //  * Finishing warps (warps 0-7) take a full set, turn its candidates into
-//    keys and the fine histogram (joining the streaming warps' parts pairwise
-//    into the eight regions of the selection when there are sixteen of them),
-//    select and emit its row --
+//    keys and the fine histogram (for rows of at least kKeysOnStreamMaxLen;
+//    joining the streaming warps' parts pairwise into the eight regions of the
+//    selection when there are sixteen of them), select and emit its row --
 //    the window indices staged in shared memory, then mapped through the page
 //    table -- and prepare the set for the row two streamed rows later: its
 //    descriptor (read by the streaming warps), its admission rule (the key
-//    that about 1.25 k candidates of this row reach, scaled to the new length,
+//    that about 1.15 k candidates of this row reach, scaled to the new length,
 //    or a sample of the new row, or the whole row when small), and a bulk copy
 //    of its page-table row into shared memory, so that the page transform
 //    reads no global memory.  Descriptors are loaded a row ahead.  While a set
@@ -72,6 +74,17 @@ constexpr int kPageStage = 1536;             // page-table entries a set can sta
 // Cost floor of a row in the balanced split (elements): the finishing warps
 // need about as long per row as the stream takes for this many elements.
 constexpr uint32_t kSplitCostFloor = 98304;
+// Rows shorter than this (elements) have their candidates turned into keys
+// and the fine histogram by the streaming warps, at the end of their stream;
+// longer rows leave it to the finishing warps.  Measured on B300: a row's
+// finishing takes about 7 us whatever its length, and the stream takes about
+// as long for a row of about 68 K elements, so below this length the
+// streaming warps would otherwise wait for the finishing warps.  Both sides
+// decide from the row's seq_len.  (With sixteen streaming warps the parts are
+// merged into regions first, by the finishing warps.)
+constexpr int32_t kKeysOnStreamMaxLen = 65536;
+
+__device__ __forceinline__ bool keys_on_stream(int32_t L) { return kSW == kWarps && L < kKeysOnStreamMaxLen; }
 
 // The row a set is prepared for, as the streaming warps read it.
 struct SetRow {
@@ -352,7 +365,7 @@ __device__ __forceinline__ void finish_row(SplitSmem<E>& M, uint32_t b, const Pa
   const Row r = make_row<E>(p, R, d);
   const int64_t nq = quads_of<E>(r);
   if constexpr (kSW > kWarps) merge_parts(S);
-  pipe::keys_and_histogram(S);
+  if (!keys_on_stream(d.L)) pipe::keys_and_histogram(S, tid >> 5);
   if (tid == 0) {
     S.next_len = next_len > p.k ? next_len : 0;
     S.hint_rank = pipe::hint_rank_for(k, r.L, S.next_len);
@@ -567,6 +580,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
       const int64_t nq = quads_of<E>(r);
       stream_row_wb<kStages, kSW, Shape<E>::kChunk, E>(M.set[b], M.ring, sw, r, nq, g, timed_out, stream_wait_limit(p),
                                                       [&] { scursor_issue<E>(M.ring, cur, p, sw, policy); });
+      if (keys_on_stream(sr.L)) pipe::keys_and_histogram(M.set[b], sw);
       sbar();  // every streaming warp has written its region
       if (tid == kThreads) mbar_arrive(&M.set_full[b]);
     }
