@@ -19,6 +19,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -163,6 +164,12 @@ __device__ __forceinline__ float edge_float(uint32_t b) { return key_floor_float
 // binary32 value -- so keys, order and ties are those of the same values
 // stored as 32-bit floats.  bits_at gives the binary32 pattern of element e of
 // a run of elements.
+//
+// The 16-bit types also compare a 32-bit word of two elements with a
+// threshold in one packed instruction: for an element x of the type and any
+// float t, x >= t exactly when x >= the smallest value of the type that is at
+// least t (t rounded toward +inf), which is what threshold_pair holds in both
+// halves; ge_pair gives bit 0 for the low element, bit 1 for the high one.
 // ---------------------------------------------------------------------------
 struct ElemF32 {
   static constexpr int kPerQuad = 4, kBytes = 4;
@@ -189,6 +196,15 @@ struct ElemBF16 {
   __device__ __forceinline__ static uint32_t bits_at(const void* run, int e) {
     return (uint32_t)static_cast<const uint16_t*>(run)[e] << 16;
   }
+  __device__ __forceinline__ static uint32_t threshold_pair(float t) {
+    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_ru(t));
+    return h | (h << 16);
+  }
+  __device__ __forceinline__ static uint32_t ge_pair(uint32_t w, uint32_t t2) {
+    const uint32_t m = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&t2));
+    return (m & 1u) | ((m >> 15) & 2u);
+  }
 };
 
 // IEEE binary16, decoded by the CUDA conversion.
@@ -205,6 +221,14 @@ struct ElemF16 {
   }
   __device__ __forceinline__ static uint32_t bits_at(const void* run, int e) {
     return __float_as_uint(value(static_cast<const uint16_t*>(run)[e]));
+  }
+  __device__ __forceinline__ static uint32_t threshold_pair(float t) {
+    const uint32_t h = __half_as_ushort(__float2half_ru(t));
+    return h | (h << 16);
+  }
+  __device__ __forceinline__ static uint32_t ge_pair(uint32_t w, uint32_t t2) {
+    const uint32_t m = __hge2_mask(*reinterpret_cast<const __half2*>(&w), *reinterpret_cast<const __half2*>(&t2));
+    return (m & 1u) | ((m >> 15) & 2u);
   }
 };
 

@@ -866,6 +866,8 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
   int64_t q0, q1;
   warp_block_of<NW>(nq, w, q0, q1);
   const float tf = S.rule.tf;
+  uint32_t t2 = 0u;  // 16-bit elements: the threshold in both halves of a word
+  if constexpr (EPQ == 8) t2 = E::threshold_pair(tf);
   const int rot = lane & 7;  // rotated quad order: the 8 lanes of a load phase hit 8 distinct bank groups
   const uint32_t lt = lanemask_lt();
   uint32_t* rraw = S.bkey + w * kReg;  // raw float bits here; keys after keys_and_histogram
@@ -886,11 +888,18 @@ __device__ __forceinline__ void stream_row_wb(Shared& S, Ring<NS, NW, CQ>& R, in
 #pragma unroll
     for (int u = 0; u < QPL; ++u) {
       const float4 v = st[QPL * lane + ((u + rot) & (QPL - 1))];
-      float x[EPQ];
-      E::decode(v, x);
+      if constexpr (EPQ == 8) {
+        // two elements a packed compare; element 2i is the low half of word i
+        const uint32_t wv[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w)};
 #pragma unroll
-      for (int c = 0; c < EPQ; ++c)
-        if (x[c] >= tf) mr |= (Mask)1u << (EPQ * u + c);
+        for (int i = 0; i < 4; ++i) mr |= (Mask)E::ge_pair(wv[i], t2) << (EPQ * u + 2 * i);
+      } else {
+        float x[EPQ];
+        E::decode(v, x);
+#pragma unroll
+        for (int c = 0; c < EPQ; ++c)
+          if (x[c] >= tf) mr |= (Mask)1u << (EPQ * u + c);
+      }
     }
     // bit e: element e of the lane's kBits (rotate left by EPQ rot)
     Mask m = rot == 0 ? mr : (Mask)((mr << (EPQ * rot)) | (mr >> (kBits - EPQ * rot)));
