@@ -91,7 +91,7 @@ class ClockSampler:
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -127,7 +127,7 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-        sm, mx, reasons = [], None, set()
+        sm, mem, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for t, line in self.lines:
             if self.t0 is None or not (self.t0 - 0.15 <= t <= self.t1 + 0.15):
@@ -137,6 +137,8 @@ class ClockSampler:
                 continue
             try:
                 sm.append(float(parts[1]))
+                if len(parts) > 9:
+                    mem.append(float(parts[9]))
                 mx = float(parts[2])
             except ValueError:
                 continue
@@ -144,6 +146,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "mem_mhz": statistics.median(mem) if mem else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -189,6 +192,24 @@ def prepare_timing(w, steps: int, warmup: int, flush: bool, device, launch):
     return args, stream, scratch, starts, ends
 
 
+def device_copy_gbs(device, nbytes: int = 1 << 29, reps: int = 5) -> float:
+    """This GPU's plain copy rate right now (read + write bytes of a 512 MB
+    torch copy, best of `reps`, CUDA events): context for the roofline,
+    whose peak is the pool's measured figure."""
+    a = torch.empty(nbytes // 4, dtype=torch.float32, device=device).fill_(1.0)
+    b = torch.empty_like(a)
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize(device)
+        best = min(best, e0.elapsed_time(e1))
+    del a, b
+    return 2 * nbytes / (best / 1e3) / 1e9
+
+
 def run_ours(a, rank: int, world: int, device) -> dict:
     from sparse_attention_top_packed_b300 import binding
 
@@ -210,6 +231,7 @@ def run_ours(a, rank: int, world: int, device) -> dict:
         torch.cuda.synchronize(device)
         launch = lambda args_, stream_: graph.replay()  # noqa: E731
 
+    copy_gbs = device_copy_gbs(device)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -252,7 +274,7 @@ def run_ours(a, rank: int, world: int, device) -> dict:
     e2e = run_e2e(a, w, device) if rank == 0 else None
     result = {
         "step_ms": step_ms, "kernel_ms": kernel_ms, "alg_bytes": alg_bytes, "flush": flush,
-        "clocks": clocks, "e2e": e2e, "workload": w, "out": out, "device_flags": flags,
+        "clocks": clocks, "e2e": e2e, "workload": w, "out": out, "device_flags": flags, "copy_gbs": copy_gbs,
     }
     return result
 
@@ -507,7 +529,10 @@ def main():
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
                          if peaks["source"] == "measured" else "fallback 6.4 TB/s",
                          "algorithmic_bytes_per_launch": r["alg_bytes"],
-                         "kernel": KERNEL_NAMES.get(plan["path"], "?")},
+                         "kernel": KERNEL_NAMES.get(plan["path"], "?"),
+                         "device_copy_gbs": r["copy_gbs"],
+                         "device_copy_note": "this GPU's 512 MB torch copy rate (read+write bytes, best of 5) "
+                                             "just before the timed region; the peak above is the pool's"},
             "gpu_launches": a.steps,
             "clocks": r["clocks"],
             "e2e": r["e2e"],
