@@ -45,6 +45,8 @@ WORKLOAD_TEXT = {
     "decode": "decode-like: 64 rows x 8192 fp32, k=2048, page 64",
     "tiny": "tiny: 8 rows, windows 1..300 at unaligned offsets, k=32, page 64",
     "fewlong": "few long rows: 64 rows x 327680 fp32 (fewer rows than SMs), k=2048, page 64",
+    "drift": "prefill chunk ISL 70000 with drifting scores: row q of a request holds N(0,1)*s_q + m_q, "
+             "m_q = 0.5 sin(2 pi q/300) + 0.05 N(0,1), s_q = 1 + 0.25 sin(2 pi q/450), k=2048, page 64",
 }
 L2_BYTES = 126 * 1024 * 1024
 

@@ -1022,12 +1022,15 @@ __device__ __forceinline__ void keys_and_histogram(Shared& S, int w) {
 }
 
 // Rank the next row's admission threshold should reach in this row: about
-// 1.15 k in a row of the next row's length (binomial noise at that rank is a
-// few percent of k, so the next row still admits at least k), capped by the
-// buffer.  0 when there is no next row.
-__device__ __forceinline__ uint32_t hint_rank_for(uint32_t k, int32_t L, int32_t next_len) {
+// m20 / 20 k in a row of the next row's length (with m20 = 23, 1.15 k: the
+// binomial noise at that rank is a few percent of k, so the next row still
+// admits at least k when its scores are distributed like this row's), capped
+// by the buffer.  0 when there is no next row.
+constexpr uint32_t kHintMargin20 = 23;
+__device__ __forceinline__ uint32_t hint_rank_for(uint32_t k, int32_t L, int32_t next_len,
+                                                  uint32_t m20 = kHintMargin20) {
   if (next_len <= 0) return 0u;
-  return (uint32_t)min((int64_t)23 * k * L / (20 * (int64_t)next_len) + 1, (int64_t)kCap);
+  return (uint32_t)min((int64_t)m20 * k * L / (20 * (int64_t)next_len) + 1, (int64_t)kCap);
 }
 
 // Fine shift for a row whose threshold key sits about `d` keys below its k-th

@@ -71,6 +71,8 @@ static_assert(!kRegSplit || kSW * 32 * kStreamRegs + kThreads * kFinishRegs <= k
 static_assert(!kRegSplit || kLaunchRegs * kBlockThreads <= 65536, "launch allocation exceeds the register file");
 static_assert(kSW == kWarps || 2 * kPart == kRegion, "two streaming parts make one selection region");
 constexpr int kPageStage = 1536;             // page-table entries a set can stage (6 KB)
+constexpr uint32_t kHintMargin20Max = 40;    // the hint's widest target: 2 k
+constexpr uint32_t kMissSampleRows = 8;      // rows a set samples after a hinted row missed
 // Cost floor of a row in the balanced split (elements): the finishing warps
 // need about as long per row as the stream takes for this many elements.
 constexpr uint32_t kSplitCostFloor = 98304;
@@ -85,6 +87,21 @@ constexpr uint32_t kSplitCostFloor = 98304;
 constexpr int32_t kKeysOnStreamMaxLen = 65536;
 
 __device__ __forceinline__ bool keys_on_stream(int32_t L) { return kSW == kWarps && L < kKeysOnStreamMaxLen; }
+
+// How far the hints of each set are trusted (finishing thread 0's, one
+// register: byte b the margin of set b -- the hint's target in twentieths of
+// k --, byte 2 + b the rows set b still takes its thresholds from samples).
+struct HintAdapt {
+  uint32_t v = pipe::kHintMargin20 | (pipe::kHintMargin20 << 8);
+  __device__ __forceinline__ uint32_t field(uint32_t i) const { return (v >> (8u * i)) & 0xFFu; }
+  __device__ __forceinline__ void set_field(uint32_t i, uint32_t x) {
+    v = (v & ~(0xFFu << (8u * i))) | ((x & 0xFFu) << (8u * i));
+  }
+  __device__ __forceinline__ uint32_t margin(uint32_t b) const { return field(b); }
+  __device__ __forceinline__ void set_margin(uint32_t b, uint32_t x) { set_field(b, x); }
+  __device__ __forceinline__ uint32_t left(uint32_t b) const { return field(2u + b); }
+  __device__ __forceinline__ void set_left(uint32_t b, uint32_t x) { set_field(2u + b, x); }
+};
 
 // The row a set is prepared for, as the streaming warps read it.
 struct SetRow {
@@ -249,7 +266,7 @@ __device__ __forceinline__ bool scursor_issue(typename SplitSmem<E>::RingT& R, S
 // (done by the caller).  Ends with a finishing barrier.
 template <class E>
 __device__ __forceinline__ void prepare_set(SplitSmem<E>& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
-                                            int64_t hi) {
+                                            int64_t hi, HintAdapt& ha) {
   pipe::Shared& S = M.set[b];
   if (R >= hi) {
     if (threadIdx.x == 0) M.srow[b].row = hi;
@@ -260,8 +277,11 @@ __device__ __forceinline__ void prepare_set(SplitSmem<E>& M, uint32_t b, const P
   const int64_t nq = quads_of<E>(r);
   const bool small = r.L + r.head <= kPart;  // every element fits its streaming warp's part
   if (threadIdx.x == 0) {
-    const bool hinted = !small && S.hint_valid != 0u;  // thread 0's own write
+    // thread 0's own writes: after a miss the set samples its next rows
+    const uint32_t left = ha.left(b);
+    const bool hinted = !small && S.hint_valid != 0u && left == 0u;
     S.sample = (!small && !hinted) ? 1u : 0u;
+    if (!small && left != 0u) ha.set_left(b, left - 1u);
     S.overflow = 0u;
     S.res_n = 0u;
     if (small) {
@@ -358,7 +378,7 @@ __device__ __forceinline__ void merge_parts(pipe::Shared& S) {
 // barrier.
 template <class E>
 __device__ __forceinline__ void finish_row(SplitSmem<E>& M, uint32_t b, const Params& p, int64_t R, const RowRaw& d,
-                                           int32_t next_len, uint32_t parity, bool& timed_out) {
+                                           int32_t next_len, uint32_t parity, bool& timed_out, HintAdapt& ha) {
   pipe::Shared& S = M.set[b];
   const int tid = threadIdx.x;
   const uint32_t k = (uint32_t)p.k;
@@ -368,7 +388,7 @@ __device__ __forceinline__ void finish_row(SplitSmem<E>& M, uint32_t b, const Pa
   if (!keys_on_stream(d.L)) pipe::keys_and_histogram(S, tid >> 5);
   if (tid == 0) {
     S.next_len = next_len > p.k ? next_len : 0;
-    S.hint_rank = pipe::hint_rank_for(k, r.L, S.next_len);
+    S.hint_rank = pipe::hint_rank_for(k, r.L, S.next_len, ha.margin(b));
   }
   pipe::cbar();
   int32_t* stage = reinterpret_cast<int32_t*>(S.hist2);  // the row's indices, before the page transform
@@ -394,6 +414,21 @@ __device__ __forceinline__ void finish_row(SplitSmem<E>& M, uint32_t b, const Pa
       hint_sh = (hint_ok && sel.tk > hint.tk) ? pipe::fine_shift(sel.tk - hint.tk) : S.fh_sh;
     }
   } else {
+    // The hint adapts to how far the scores move between this set's rows. A
+    // hinted row that admitted fewer than k (its threshold was too high)
+    // widens the hint's target by half, up to 2 k, and has the set's next
+    // kMissSampleRows rows take their thresholds from samples; a hinted row
+    // that overflowed narrows it.  Every hinted row that needs no redo brings
+    // it one twentieth of k back toward 1.15 k (below).
+    if (tid == 0 && S.sample == 0u) {
+      const uint32_t m = ha.margin(b);
+      if (S.overflow != 0u) {
+        ha.set_margin(b, max(m - m / 4u, pipe::kHintMargin20));
+      } else {
+        ha.set_margin(b, min(m + m / 2u, kHintMargin20Max));
+        ha.set_left(b, kMissSampleRows);
+      }
+    }
     // the threshold was off: the row again, from global memory, exactly
     pipe::cbar();
     for (int i = tid; i < pipe::kBins2 / 4; i += kThreads)
@@ -415,6 +450,7 @@ __device__ __forceinline__ void finish_row(SplitSmem<E>& M, uint32_t b, const Pa
     hint_sh = (hint_ok && sel.tk > hint.tk) ? pipe::fine_shift(sel.tk - hint.tk) : S.fh_sh;
   }
   if (tid == 0 && !emitted) pipe::publish_hint(S, hr, hint_ok, hint, hint_sh, !redo, n, k, r.L);
+  if (tid == 0 && !redo && S.sample == 0u && ha.margin(b) > pipe::kHintMargin20) ha.set_margin(b, ha.margin(b) - 1u);
   if (!redo) {
     if (!emitted) pipe::emit_ordered(S, out, k, sel);
   }
@@ -528,13 +564,14 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
     if (rc < hi) dc = load_row_raw(p, rc);
     if (rn < hi) dn = load_row_raw(p, rn);
     // the first two streamed rows' sets
-    prepare_set(M, 0u, p, rc, dc, hi);
+    HintAdapt ha;  // thread 0's
+    prepare_set(M, 0u, p, rc, dc, hi, ha);
     if (tid == 0) {
       if (rc < hi) ++page_armed[0];
       mbar_arrive(&M.set_free[0]);
     }
     if (rc < hi) {
-      prepare_set(M, 1u, p, rn, dn, hi);
+      prepare_set(M, 1u, p, rn, dn, hi, ha);
       if (tid == 0) {
         if (rn < hi) ++page_armed[1];
         mbar_arrive(&M.set_free[1]);
@@ -547,9 +584,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) topk_split_kernel(const __gr
       RowRaw d2 = {0, 0, 0};
       if (r2 < hi) d2 = load_row_raw(p, r2);  // in flight while the set streams
       wait_emitting(&M.set_full[b], par, timed_out, p, bits, lo, hi, sh);
-      finish_row(M, b, p, rc, dc, r2 < hi ? d2.L : 0, par, timed_out);
+      finish_row(M, b, p, rc, dc, r2 < hi ? d2.L : 0, par, timed_out, ha);
       if (tid == 0) ++page_seen[b];
-      prepare_set(M, b, p, r2, d2, hi);
+      prepare_set(M, b, p, r2, d2, hi, ha);
       if (tid == 0) {
         if (r2 < hi) ++page_armed[b];
         mbar_arrive(&M.set_free[b]);

@@ -40,6 +40,8 @@ from __future__ import annotations
 from dataclasses import dataclass
 from typing import Optional
 
+import math
+
 import numpy as np
 import torch
 
@@ -246,8 +248,30 @@ def mixed(device="cpu", seed_lengths: int = 0, seed_scores: int = 1, total_rows:
                     row_to_batch.to(device), pt.to(device), table_pages, page_size, k, rows)
 
 
+def prefill_drift(device="cpu", seed: int = 0, period_mean: float = 300.0, period_scale: float = 450.0,
+                  jitter: float = 0.05) -> Workload:
+    """The prefill shape with scores whose distribution moves from row to row,
+    as an indexer's scores do along the queries of a request: row q of a
+    request (its q-th causal query) holds N(0,1) * s_q + m_q with
+      m_q = 0.5 sin(2 pi q / period_mean) + jitter * N(0,1)   (seeded),
+      s_q = 1 + 0.25 sin(2 pi q / period_scale).
+    Neighbouring rows differ by about 0.01 of a standard deviation in the mean
+    plus the jitter, so a threshold carried from one row to the next is often
+    too high or too low."""
+    w = prefill(device=device, seed=seed)
+    q_per_req = w.num_rows // 2
+    q = torch.arange(w.num_rows, dtype=torch.float64) % q_per_req
+    g = torch.Generator().manual_seed(seed + 7)
+    m = 0.5 * torch.sin(2 * math.pi * q / period_mean) + jitter * torch.randn(w.num_rows, generator=g,
+                                                                                dtype=torch.float64)
+    sc = 1.0 + 0.25 * torch.sin(2 * math.pi * q / period_scale)
+    w.scores.mul_(sc.to(torch.float32).to(w.scores.device)[:, None]).add_(m.to(torch.float32).to(w.scores.device)[:, None])
+    w.name = "drift"
+    return w
+
+
 NAMED = {"tiny": tiny, "decode": decode, "prefill": prefill, "long": long_context, "mixed": mixed,
-         "fewlong": few_long}
+         "fewlong": few_long, "drift": prefill_drift}
 
 
 def named(name: str, device="cpu", **kw) -> Workload:

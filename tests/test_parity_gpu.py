@@ -220,6 +220,14 @@ def test_prefill_full_size(cuda_device):
     assert torch.equal(out, run(w, path="split"))
 
 
+def test_prefill_with_drifting_scores_full_size(cuda_device):
+    """Rows whose score distribution moves from row to row: carried thresholds
+    miss in both directions, and the rows they miss are redone exactly."""
+    w = wl.prefill_drift(device=cuda_device)
+    out = _full_size(w, sample=384)
+    assert torch.equal(out, run(w, path="pipe"))
+
+
 def test_long_context_full_size(cuda_device):
     w = wl.long_context(device=cuda_device)
     out = _full_size(w, sample=160)

@@ -61,3 +61,18 @@ def test_pages_are_distinct_and_fit_31_bits():
     flat = t.reshape(-1)
     assert flat.unique().numel() == flat.numel()
     assert int(flat.max()) * 64 + 63 < 2 ** 31
+
+
+def test_drift_recipe(monkeypatch):
+    """Each row is N(0,1) * s_q + m_q; with the normal draw stubbed to ones a
+    row holds s_q + m_q, whose smooth part follows the stated sines and whose
+    rest is the 0.05-sigma jitter."""
+    import math
+
+    monkeypatch.setattr(wl, "_normal", lambda shape, seed, device, bf16=False: torch.ones((shape[0], 1)))
+    w = wl.prefill_drift(device="cpu")
+    q = torch.arange(w.num_rows, dtype=torch.float64) % 2048
+    smooth = 1.0 + 0.25 * torch.sin(2 * math.pi * q / 450) + 0.5 * torch.sin(2 * math.pi * q / 300)
+    rest = w.scores[:, 0].to(torch.float64) - smooth
+    assert abs(float(rest.mean())) < 0.005 and 0.045 < float(rest.std()) < 0.055
+    assert w.name == "drift" and w.num_rows == 4096 and w.row_stride == 140000
