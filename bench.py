@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -64,13 +65,24 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6400.0, "source": "fallback", "sm_max_mhz": 2032.0}
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank lines (no string literal in
+    the kernel sources holds a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash() -> str:
+    """First 16 hex digits of the sha256 of the kernel sources' code (file
+    names and contents, comments and blank lines left out): it changes when the
+    kernels do, not when a comment does."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_top_packed_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

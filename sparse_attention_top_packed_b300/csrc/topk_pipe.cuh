@@ -21,7 +21,7 @@
 //
 //  * Admission.  Every row streams with a fixed threshold, a guess at a lower
 //    bound of its k-th largest key: from the CTA's previous row (the key that
-//    about 1.25 k of its candidates reach, scaled to the new length), or from
+//    about 1.15 k of its candidates reach, scaled to the new length), or from
 //    a strided sample of the row itself.  Each lane compares 32 consecutive
 //    floats of a chunk with the threshold and appends the passing ones (order-
 //    preserving key, window index) to the warp's region of the candidate
@@ -1105,7 +1105,7 @@ __device__ __forceinline__ FinePick fine_find(const Shared& S, const uint32_t* h
 }
 
 // Thread 0: the admission rule of the CTA's next row (S.hint).  The row's
-// selection proposed `hint` (reaching rank hr, about 1.25 k scaled to the next
+// selection proposed `hint` (reaching rank hr, about 1.15 k scaled to the next
 // row's length) when hint_ok; otherwise a fast row whose admitted count scales
 // to at least 1.05 k of the next row keeps its own rule.  hr == 0: no next row.
 __device__ __forceinline__ void publish_hint(Shared& S, uint32_t hr, uint32_t hint_ok, const Rule& hint,
