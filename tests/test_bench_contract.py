@@ -32,3 +32,14 @@ def test_reference_arm_prints_one_contract_line():
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_profiles_describe_the_current_kernels():
+    """profiles/dram_traffic.json was captured on the kernel code in the tree
+    (its hash leaves comments out), so the bench reports the measured traffic."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench._code_only("a; // note\n/* block\n comment */b;\n\n  c;  // x") == "a;\nb;\n  c;"
+    for workload in ("prefill", "long", "fewlong", "decode"):
+        assert bench.profiled_traffic(workload), workload
