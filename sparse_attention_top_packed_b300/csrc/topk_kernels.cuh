@@ -11,16 +11,18 @@
 //                          row and streams it through its own ring of TMA bulk
 //                          copies into shared memory, with no block-wide
 //                          synchronisation while streaming.  A running lower
-//                          bound on the k-th largest key (a level-1 histogram
-//                          bin edge that only rises, shared by all warps and
-//                          raised lock-free) drops almost every element at one
+//                          bound on the k-th largest key (first from a sample
+//                          of the whole row, then a level-1 histogram bin edge
+//                          that only rises, shared by all warps and raised
+//                          lock-free) drops almost every element at one
 //                          compare; the few that pass are appended, in window
 //                          order, to the warp's list in shared memory.  Since
 //                          slices are contiguous and in warp order, the lists
 //                          concatenated in warp order are in window order.  The
 //                          radix select then runs on the lists.  A row whose
-//                          candidates overflow a list falls back to the
-//                          multipass procedure for that row.
+//                          candidates overflow a list, or that listed fewer
+//                          than k, falls back to the multipass procedure for
+//                          that row.
 #pragma once
 
 #include "topk_device.cuh"

@@ -36,9 +36,12 @@
 //    barrier any warp finds a rank's bin alone).  Each warp compacts its region
 //    in place to the entries at or above that bin, and the bin's own entries
 //    (at most 32) are gathered and ranked by (key, ~j) in every warp, which
-//    gives the exact k-th largest pair -- a tie goes to the lower j.  When the
-//    histogram cannot settle it (the rank lies above its range, or its bin is
-//    crowded), a radix select over the buffer does.
+//    gives the exact k-th largest pair -- a tie goes to the lower j.  A bin of
+//    more than 32 entries is settled by window order when they share one key,
+//    else by a second fine level over the bin (2^11 sub-bins).  When the
+//    histograms cannot settle it (the rank lies above their range, or the
+//    sub-bin is still crowded with several keys), a radix select over the
+//    buffer does.
 //
 //  * Emission.  Selected entries' output positions are prefix counts over the
 //    ordered regions: each warp writes its selected window indices in
